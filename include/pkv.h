@@ -1,0 +1,241 @@
+/*
+ * pkv.h — C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * The library implements single-token decode attention over a paged KV cache,
+ * with GQA head grouping, fp16/bf16 or INT8 (per-token or per-64-token-group
+ * scale/zero-point) keys and values dequantised inside the kernels, and a
+ * query-aware sparse mode that scores pages by a per-page channel bounding box
+ * and attends only over the top-K pages.
+ *
+ * Sources, cited by short name and section:
+ *   [Gemini page]      "GPU显存占用直降63%！Gemini KV Cache优化实战：FlashAttention-3适配全链路拆解"
+ *   [KV-practice page] "LLM推理中的KV Cache优化与显存管理实践"
+ *   [HBM-layout page]  "Transformer 推理的内存布局优化：从 HBM 带宽利用率的视角重新设计 KV Cache"
+ *   [TinyServe page]   "LLM推理中的KV缓存优化技术与TinyServe实践"
+ *
+ * Conventions (every call):
+ *   - Pointers named *_pages, q, out, k_new, v_new, block_table, seq_lens,
+ *     positions, new_lens, sel_*, scores_out, workspace, dev_status and the
+ *     pointer members of pkv_cache are DEVICE pointers owned by the caller.
+ *     The library allocates no device memory and keeps no pointer after a call
+ *     returns. `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Calls are asynchronous on `stream`. A host-detectable error (null or
+ *     misaligned pointer, unsupported shape or dtype, short workspace) is
+ *     returned before anything is launched. Device pools, q and out must be
+ *     16-byte aligned.
+ *   - Device-detectable errors never trap: the kernel ORs a PKV_DEV_* bit into
+ *     *dev_status (a caller-owned int32 the caller zeroes; may be NULL only if
+ *     the caller accepts losing the report), skips the offending page or token,
+ *     and finishes. Read *dev_status after synchronising the stream.
+ *   - All calls are stateless and re-entrant; two calls that share a workspace
+ *     must not run concurrently.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96) */
+  PKV_ERR_OUT_OF_PAGES = 3,  /* host allocator: not enough free pages */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  PKV_ERR_WORKSPACE = 5      /* workspace too small */
+} pkv_status;
+
+/* Bits ORed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_PAGE 1      /* block-table entry outside [0, num_pages) */
+#define PKV_DEV_BAD_SELECTED 2  /* selected logical page outside the sequence */
+#define PKV_DEV_BAD_POSITION 4  /* append slot beyond the block table / bad length */
+#define PKV_DEV_TIMEOUT 8       /* a bounded wait inside a kernel gave up */
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2, PKV_I8 = 3 } pkv_dtype;
+
+typedef enum {
+  PKV_QUANT_NONE = 0,       /* kv_dtype F16 or BF16: values stored as is */
+  PKV_QUANT_PER_TOKEN = 1,  /* kv_dtype I8: one (scale, zero) per token and kv head
+                               [HBM-layout page, section 二] */
+  PKV_QUANT_PER_GROUP64 = 2 /* kv_dtype I8: one (scale, zero) per 64 tokens and kv head
+                               [Gemini page, 第一章] */
+} pkv_quant;
+
+/*
+ * A paged KV cache (one layer). Fixed-size pages are allocated on demand and
+ * need not be contiguous; a per-sequence block table maps logical page i to a
+ * physical page id [HBM-layout page, sections 二 (layout C) and 三].
+ *
+ * Layouts (all row-major, device memory, caller-owned):
+ *   k_pages, v_pages : [num_pages][num_kv_heads][page_size][head_dim] of kv_dtype.
+ *                      Token slot s of logical page i of a sequence holds its
+ *                      token i * page_size + s.
+ *   kv_sz            : I8 only, fp32 [num_pages][num_kv_heads][page_size / gran][4]
+ *                      with gran = 1 (per token) or 64 (per group); the 4 floats
+ *                      are (k_scale, k_zero, v_scale, v_zero). Restoration:
+ *                      x = (code + 128) * scale + zero.
+ *   tail             : PER_GROUP64 only, fp32
+ *                      [tail_rows][num_kv_heads][2 (K, V)][2 (group parity)][64][head_dim]:
+ *                      original values of each sequence's open (partially filled)
+ *                      64-token group, kept so that every append re-quantises
+ *                      the open group from its members. Row b belongs to batch
+ *                      row b of kv_append. Contents are managed by kv_append.
+ *   page_meta        : optional (NULL = no sparse metadata), fp32
+ *                      [num_pages][num_kv_heads][2][head_dim]: per channel, the
+ *                      minimum (row 0) and maximum (row 1) of the page's valid
+ *                      keys [TinyServe page, section 2.1]; kept in fp32
+ *                      [TinyServe page, section 5.2]. For INT8 keys the box is
+ *                      built from fl32(fl32((c + 128) * s) + z).
+ */
+typedef struct {
+  int32_t num_pages;
+  int32_t page_size;     /* multiple of 16; multiple of 64 for PER_GROUP64 */
+  int32_t num_kv_heads;
+  int32_t head_dim;      /* 64 or 128 */
+  pkv_dtype kv_dtype;    /* F16, BF16 (with QUANT_NONE) or I8 */
+  pkv_quant quant;
+  void* k_pages;
+  void* v_pages;
+  float* kv_sz;
+  float* tail;
+  int32_t tail_rows;
+  float* page_meta;
+} pkv_cache;
+
+/* Status text for a pkv_status value (static string). */
+const char* pkv_status_string(pkv_status s);
+
+/* PKV_ABI_VERSION of the loaded library. */
+int32_t pkv_abi_version(void);
+
+/*
+ * kv_append — write new tokens' K and V into their pages.
+ * [HBM-layout page, section 三 append_kv]: token position pos goes to logical
+ * page pos / page_size, slot pos % page_size, through the block table.
+ *   k_new, v_new : [batch][t_new][num_kv_heads][head_dim] of src_dtype (F16/BF16).
+ *   block_table  : int32 [batch][max_pages] physical page ids (pages must
+ *                  already be allocated for every written position).
+ *   positions    : int32 [batch], position of the first new token of row b
+ *                  (its current length).
+ *   new_lens     : int32 [batch] tokens to write for row b (<= t_new), or NULL
+ *                  for t_new each. The caller updates its seq_lens afterwards.
+ * F16/BF16 caches store the values (converted to kv_dtype). INT8 caches
+ * quantise: per token over head_dim values; per group over the group's
+ * members, re-quantising the open group from the originals kept in `tail`
+ * (closed groups never change). If page_meta is set, the bounding box of every
+ * page the append touched is recomputed from the stored keys.
+ * Quantiser (bit-exact definition, fp32 ops, ties to even):
+ *   s = (max - min) / 255; z = min; code = clamp(rint((x - z) / s), 0, 255) - 128;
+ *   a constant block stores s = 0 and codes -128.
+ * Device errors: PKV_DEV_BAD_POSITION (slot beyond max_pages * page_size or
+ * negative position / length), PKV_DEV_BAD_PAGE; the token is skipped.
+ */
+pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new,
+                         const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                         const int32_t* block_table, int32_t max_pages,
+                         const int32_t* positions, const int32_t* new_lens,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * page_score_topk — relevance of every page of every sequence to each query
+ * head, and the top-K pages [TinyServe page, sections 2.1 and 3.1 phases 1-2]:
+ *   r(q, page) = sum_i (q_i >= 0 ? q_i * max_i : q_i * min_i)      (fp32)
+ * Query head h uses kv head h / (num_q_heads / num_kv_heads); each query head
+ * selects on its own. K = min(top_k, pages of the sequence); ties go to the
+ * lower logical page index; the kept pages are written in ascending order.
+ *   q          : [batch][num_q_heads][head_dim] of q_dtype (F16/BF16/F32).
+ *   seq_lens   : int32 [batch]; sequence b has ceil(seq_lens[b] / page_size) pages.
+ *   sel_pages  : int32 [batch][num_q_heads][top_k] (entries past sel_count are -1).
+ *   sel_count  : int32 [batch][num_q_heads].
+ *   scores_out : fp32 [batch][num_q_heads][max_pages] or NULL; entries past the
+ *                sequence's pages are -inf.
+ * Needs cache->page_meta. Pages per sequence are limited to 16384.
+ * Device errors: PKV_DEV_BAD_PAGE (that page scores -inf).
+ */
+pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                               const void* q, pkv_dtype q_dtype,
+                               const int32_t* block_table, int32_t max_pages,
+                               const int32_t* seq_lens, int32_t top_k,
+                               int32_t* sel_pages, int32_t* sel_count, float* scores_out,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes needed by pkv_paged_decode_attention for these shapes.
+ * sparse != 0 sizes for the selected-pages mode. num_splits as in the call
+ * (0 = automatic, which queries the current device). Returns 0 on bad input.
+ */
+size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                     int32_t sparse, int32_t num_splits);
+
+/*
+ * paged_decode_attention — out[b][h] = softmax(sm_scale * q[b][h] . K^T) V over
+ * the tokens of sequence b [KV-practice page, section 2.1], K and V of kv head
+ * h / G (G = num_q_heads / num_kv_heads), read through the block table and
+ * dequantised in the kernel. Dense mode attends over tokens [0, seq_lens[b]).
+ * Sparse mode (sel_pages != NULL) attends over the tokens of the logical pages
+ * sel_pages[b][h][0 .. sel_count[b][h]) of each query head, softmax
+ * renormalised over them [TinyServe page, section 3.1 phase 3]; the list must
+ * be ascending for the work estimate to be exact (any order gives the same
+ * result).
+ *   q           : [batch][num_q_heads][head_dim] of q_dtype (F16/BF16/F32).
+ *   sel_stride  : row length of sel_pages (its top_k); ignored in dense mode.
+ *   out         : [batch][num_q_heads][head_dim] of out_dtype (F32/F16/BF16).
+ *   num_splits  : number of cooperating thread blocks that share the work
+ *                 (split-K over the whole batch's pages, each block taking an
+ *                 equal share); 0 = one full wave of the device.
+ *   workspace   : >= pkv_attention_workspace_bytes(...) bytes, 256-byte
+ *                 aligned. Its first part holds per-sequence-head arrival
+ *                 counters that must be ZERO before the first call; every call
+ *                 leaves them zero again when it completes. Zero it once
+ *                 (cudaMemsetAsync) after allocating it.
+ * Partial results of each block (running max, sum, accumulator) are merged in
+ * the same launch by the last block to finish each (sequence, kv head).
+ * A sequence with no tokens (or no selected pages) yields zeros.
+ * Device errors: PKV_DEV_BAD_PAGE, PKV_DEV_BAD_SELECTED (chunk skipped),
+ * PKV_DEV_TIMEOUT.
+ */
+pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                      const void* q, pkv_dtype q_dtype, float sm_scale,
+                                      const int32_t* block_table, int32_t max_pages,
+                                      const int32_t* seq_lens,
+                                      const int32_t* sel_pages, const int32_t* sel_count,
+                                      int32_t sel_stride,
+                                      void* out, pkv_dtype out_dtype, int32_t num_splits,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, void* stream);
+
+/*
+ * Host page allocator [HBM-layout page, section 三 allocate_blocks /
+ * free_sequence]: a free list of physical page ids; a sequence needs
+ * ceil(tokens / page_size) pages; an allocation that cannot be met fails
+ * without taking any page. Host memory only; not thread-safe.
+ */
+typedef struct pkv_allocator pkv_allocator;
+
+pkv_status pkv_alloc_create(int32_t num_pages, pkv_allocator** out);
+void pkv_alloc_destroy(pkv_allocator* a);
+/* Grow sequence seq_id so it holds total_tokens tokens; writes all its page ids
+ * into block_table_row[0 .. pages) (host memory, max_pages entries) and -1 past
+ * them. PKV_ERR_OUT_OF_PAGES leaves the allocator unchanged. */
+pkv_status pkv_alloc_reserve(pkv_allocator* a, int64_t seq_id, int32_t total_tokens,
+                             int32_t page_size, int32_t* block_table_row, int32_t max_pages);
+/* Return every page of seq_id to the free list. */
+pkv_status pkv_alloc_free(pkv_allocator* a, int64_t seq_id);
+int32_t pkv_alloc_num_free(const pkv_allocator* a);
+/* Pages of seq_id (0 if unknown). */
+int32_t pkv_alloc_seq_pages(const pkv_allocator* a, int64_t seq_id);
+/* Consistency check: pages that are neither free nor owned by exactly one
+ * sequence (leaked or double-owned) [Gemini page, section 2.3]. */
+int32_t pkv_alloc_check(const pkv_allocator* a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

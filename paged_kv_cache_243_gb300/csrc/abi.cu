@@ -1,0 +1,360 @@
+// C-ABI entry points: argument checks, workspace sizing and kernel dispatch.
+// Every host-detectable error is returned before anything is launched.
+#include <cstdlib>
+#include <mutex>
+#include <unordered_map>
+
+#include "attention_kernel.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+int attn_stage_bytes(int kv_kind, int D) {
+  switch (kv_kind) {
+    case KV_F16:
+    case KV_BF16: return D == 128 ? AttnGeom<128, KV_F16>::STAGE : AttnGeom<64, KV_F16>::STAGE;
+    case KV_I8T: return D == 128 ? AttnGeom<128, KV_I8T>::STAGE : AttnGeom<64, KV_I8T>::STAGE;
+    default: return D == 128 ? AttnGeom<128, KV_I8G>::STAGE : AttnGeom<64, KV_I8G>::STAGE;
+  }
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem_optin = 0;
+};
+
+pkv_status device_info(DeviceInfo& di) {
+  static std::mutex mu;
+  static std::unordered_map<int, DeviceInfo> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) {
+    di = it->second;
+    return PKV_OK;
+  }
+  DeviceInfo d;
+  if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  cache[dev] = d;
+  di = d;
+  return PKV_OK;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel, size)
+// and return how many of its blocks fit on one SM.
+pkv_status prepare_kernel(const void* fn, int threads, size_t smem, int& blocks_per_sm) {
+  static std::mutex mu;
+  struct Key {
+    int dev;
+    const void* fn;
+    size_t smem;
+    bool operator==(const Key& o) const { return dev == o.dev && fn == o.fn && smem == o.smem; }
+  };
+  struct Hash {
+    size_t operator()(const Key& k) const {
+      return std::hash<const void*>()(k.fn) ^ (k.smem * 1315423911u) ^ (size_t)k.dev;
+    }
+  };
+  static std::unordered_map<Key, int, Hash> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  Key key{dev, fn, smem};
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    blocks_per_sm = it->second;
+    return PKV_OK;
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (nb < 1) return PKV_ERR_UNSUPPORTED;
+  cache[key] = nb;
+  blocks_per_sm = nb;
+  return PKV_OK;
+}
+
+pkv_status check_cache(const pkv_cache* c, bool need_pools) {
+  if (!c) return PKV_ERR_INVALID_ARG;
+  if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0) return PKV_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (c->page_size % kChunk != 0) return PKV_ERR_UNSUPPORTED;
+  if (c->kv_dtype == PKV_F16 || c->kv_dtype == PKV_BF16) {
+    if (c->quant != PKV_QUANT_NONE) return PKV_ERR_INVALID_ARG;
+  } else if (c->kv_dtype == PKV_I8) {
+    if (c->quant != PKV_QUANT_PER_TOKEN && c->quant != PKV_QUANT_PER_GROUP64) return PKV_ERR_INVALID_ARG;
+    if (c->quant == PKV_QUANT_PER_GROUP64 && c->page_size % 64 != 0) return PKV_ERR_UNSUPPORTED;
+    if (need_pools && (!c->kv_sz || !aligned16(c->kv_sz))) return PKV_ERR_INVALID_ARG;
+  } else {
+    return PKV_ERR_INVALID_ARG;
+  }
+  if (need_pools) {
+    if (!c->k_pages || !c->v_pages || !aligned16(c->k_pages) || !aligned16(c->v_pages))
+      return PKV_ERR_INVALID_ARG;
+  }
+  if (c->page_meta && !aligned16(c->page_meta)) return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+int kv_kind(const pkv_cache* c) {
+  if (c->kv_dtype == PKV_F16) return KV_F16;
+  if (c->kv_dtype == PKV_BF16) return KV_BF16;
+  return c->quant == PKV_QUANT_PER_TOKEN ? KV_I8T : KV_I8G;
+}
+
+const void* attn_kernel(int kind, int D, int ge) {
+  switch (kind) {
+    case KV_F16: return attn_kernel_f16(D, ge);
+    case KV_BF16: return attn_kernel_bf16(D, ge);
+    case KV_I8T: return attn_kernel_i8t(D, ge);
+    default: return attn_kernel_i8g(D, ge);
+  }
+}
+
+struct AttnPlan {
+  const void* fn = nullptr;
+  int ge = 1, units = 0, stages = 0, ctas = 0;
+  size_t smem = 0;
+  size_t off_m = 0, off_l = 0, off_acc = 0, ws_bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads, bool sparse,
+                          int32_t num_splits, AttnPlan& pl) {
+  pkv_status st = check_cache(c, false);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (num_splits < 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / c->num_kv_heads;
+  pl.ge = sparse ? 1 : G;
+  if (pl.ge != 1 && pl.ge != 2 && pl.ge != 4 && pl.ge != 8) return PKV_ERR_UNSUPPORTED;
+  pl.units = batch * (sparse ? num_q_heads : c->num_kv_heads);
+  const int kind = kv_kind(c);
+  pl.fn = attn_kernel(kind, c->head_dim, pl.ge);
+  if (!pl.fn) return PKV_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  st = device_info(di);
+  if (st != PKV_OK) return st;
+  const int stage = attn_stage_bytes(kind, c->head_dim);
+  const int ring_kb = env_int("PKV_ATTN_RING_KB", 64);
+  int stages = (ring_kb * 1024) / stage;
+  stages = stages < 2 ? 2 : (stages > 32 ? 32 : stages);
+  const int forced = env_int("PKV_ATTN_STAGES", 0);
+  if (forced >= 2 && forced <= 64) stages = forced;
+  size_t smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
+  while (smem > (size_t)di.max_smem_optin && stages > 2) {
+    --stages;
+    smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
+  }
+  if (smem > (size_t)di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
+  pl.stages = stages;
+  pl.smem = smem;
+  if (num_splits > 0) {
+    pl.ctas = num_splits;
+  } else {
+    int nb = 0;
+    st = prepare_kernel(pl.fn, kAttnThreads, smem, nb);
+    if (st != PKV_OK) return st;
+    const int cap = env_int("PKV_ATTN_CTAS_PER_SM", 0);
+    if (cap > 0 && cap < nb) nb = cap;
+    pl.ctas = di.sms * nb;
+  }
+  const size_t slots = (size_t)(pl.ctas + pl.units) * kConsumerWarps;
+  size_t off = align256((size_t)pl.units * 4);
+  pl.off_m = off;
+  off = align256(off + slots * pl.ge * 4);
+  pl.off_l = off;
+  off = align256(off + slots * pl.ge * 4);
+  pl.off_acc = off;
+  off = align256(off + slots * pl.ge * c->head_dim * 4);
+  pl.ws_bytes = off;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_OUT_OF_PAGES: return "out of pages";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace too small or misaligned";
+  }
+  return "unknown status";
+}
+
+int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                     int32_t sparse, int32_t num_splits) {
+  AttnPlan pl;
+  if (plan_attention(cache, batch, num_q_heads, sparse != 0, num_splits, pl) != PKV_OK) return 0;
+  return pl.ws_bytes;
+}
+
+pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                      const void* q, pkv_dtype q_dtype, float sm_scale,
+                                      const int32_t* block_table, int32_t max_pages,
+                                      const int32_t* seq_lens, const int32_t* sel_pages,
+                                      const int32_t* sel_count, int32_t sel_stride, void* out,
+                                      pkv_dtype out_dtype, int32_t num_splits, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  pkv_status st = check_cache(cache, true);
+  if (st != PKV_OK) return st;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
+  if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
+  if (batch < 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !out || !block_table || !seq_lens || !aligned16(q) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  const bool sparse = sel_pages != nullptr;
+  if (sparse && (!sel_count || sel_stride <= 0)) return PKV_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !(sm_scale < 1e30f)) return PKV_ERR_INVALID_ARG;
+  AttnPlan pl;
+  st = plan_attention(cache, batch, num_q_heads, sparse, num_splits, pl);
+  if (st != PKV_OK) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < pl.ws_bytes)
+    return PKV_ERR_WORKSPACE;
+  int nb = 0;
+  st = prepare_kernel(pl.fn, kAttnThreads, pl.smem, nb);
+  if (st != PKV_OK) return st;
+
+  AttnParams p;
+  p.k_pages = static_cast<const uint8_t*>(cache->k_pages);
+  p.v_pages = static_cast<const uint8_t*>(cache->v_pages);
+  p.kv_sz = cache->kv_sz;
+  p.q = q;
+  p.out = out;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.sel_pages = sel_pages;
+  p.sel_count = sel_count;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_counter = reinterpret_cast<int32_t*>(ws);
+  p.ws_m = reinterpret_cast<float*>(ws + pl.off_m);
+  p.ws_l = reinterpret_cast<float*>(ws + pl.off_l);
+  p.ws_acc = reinterpret_cast<float*>(ws + pl.off_acc);
+  p.dev_status = dev_status;
+  p.num_pages = cache->num_pages;
+  p.page_size = cache->page_size;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.group = num_q_heads / cache->num_kv_heads;
+  p.batch = batch;
+  p.max_pages = max_pages;
+  p.sel_stride = sparse ? sel_stride : 0;
+  p.units_per_b = sparse ? num_q_heads : cache->num_kv_heads;
+  p.num_units = pl.units;
+  p.num_ctas = pl.ctas;
+  p.stages = pl.stages;
+  p.q_dtype = q_dtype;
+  p.out_dtype = out_dtype;
+  p.q_scale = sm_scale * 1.4426950408889634f;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), args, pl.smem,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, const void* k_new,
+                         const void* v_new, pkv_dtype src_dtype, const int32_t* block_table,
+                         int32_t max_pages, const int32_t* positions, const int32_t* new_lens,
+                         int32_t* dev_status, void* stream) {
+  pkv_status st = check_cache(cache, true);
+  if (st != PKV_OK) return st;
+  if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (batch < 0 || t_new < 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || t_new == 0) return PKV_OK;
+  if (!k_new || !v_new || !block_table || !positions || !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_INVALID_ARG;
+  if (cache->quant == PKV_QUANT_PER_GROUP64 &&
+      (!cache->tail || !aligned16(cache->tail) || cache->tail_rows < batch))
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)t_new > (long long)max_pages * cache->page_size) return PKV_ERR_INVALID_ARG;
+  AppendParams p;
+  p.k_pages = cache->k_pages;
+  p.v_pages = cache->v_pages;
+  p.kv_sz = cache->kv_sz;
+  p.tail = cache->tail;
+  p.page_meta = cache->page_meta;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.block_table = block_table;
+  p.positions = positions;
+  p.new_lens = new_lens;
+  p.dev_status = dev_status;
+  p.num_pages = cache->num_pages;
+  p.page_size = cache->page_size;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.head_dim = cache->head_dim;
+  p.kv_dtype = cache->kv_dtype;
+  p.quant = cache->quant;
+  p.src_dtype = src_dtype;
+  p.batch = batch;
+  p.t_new = t_new;
+  p.max_pages = max_pages;
+  return launch_append(p, static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                               const void* q, pkv_dtype q_dtype, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* seq_lens, int32_t top_k,
+                               int32_t* sel_pages, int32_t* sel_count, float* scores_out,
+                               int32_t* dev_status, void* stream) {
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if (!cache->page_meta) return PKV_ERR_INVALID_ARG;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (max_pages <= 0 || top_k < 1) return PKV_ERR_INVALID_ARG;
+  if (max_pages > 16384) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !block_table || !seq_lens || !sel_pages || !sel_count) return PKV_ERR_INVALID_ARG;
+  TopkParams p;
+  p.page_meta = cache->page_meta;
+  p.q = q;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.sel_pages = sel_pages;
+  p.sel_count = sel_count;
+  p.scores_out = scores_out;
+  p.dev_status = dev_status;
+  p.num_pages = cache->num_pages;
+  p.page_size = cache->page_size;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.head_dim = cache->head_dim;
+  p.num_q_heads = num_q_heads;
+  p.group = num_q_heads / cache->num_kv_heads;
+  p.batch = batch;
+  p.max_pages = max_pages;
+  p.top_k = top_k;
+  p.q_dtype = q_dtype;
+  return launch_topk(p, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

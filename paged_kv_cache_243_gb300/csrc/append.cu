@@ -1,0 +1,284 @@
+// kv_append kernels: write new tokens into their pages [HBM-layout page,
+// section 三 append_kv: block = pos / block_size, slot = pos % block_size,
+// through the block table], quantising to INT8 when the cache is INT8
+// [HBM-layout page, section 二 per-token; Gemini page, 第一章 per-64-token
+// group], and refreshing the per-page channel bounding boxes of the keys
+// [TinyServe page, section 2.1].
+//
+// The quantiser is an exact fp32 operation sequence (correctly rounded
+// subtract and divide, round half to even), so codes, scales and zero-points
+// are bit-identical to any other IEEE implementation of the same sequence:
+//   s = (max - min) / 255, z = min, code = clamp(rint((x - z) / s), 0, 255) - 128.
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+__device__ __forceinline__ float load_src(const void* p, int dtype, size_t i) {
+  return dtype == PKV_BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
+                           : __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+
+__device__ __forceinline__ int quant_code(float x, float s, float z) {
+  if (s == 0.f) return -128;
+  float u = rintf(__fdiv_rn(__fsub_rn(x, z), s));
+  u = fminf(fmaxf(u, 0.f), 255.f);
+  return (int)u - 128;
+}
+
+__device__ __forceinline__ bool row_window(const AppendParams& p, int b, int& pos, int& n) {
+  pos = p.positions[b];
+  n = p.new_lens ? p.new_lens[b] : p.t_new;
+  if (n > p.t_new || n < 0 || pos < 0 || (long long)pos + n > (long long)p.max_pages * p.page_size) {
+    flag_status(p.dev_status, PKV_DEV_BAD_POSITION);
+    return false;
+  }
+  return n > 0;
+}
+
+__device__ __forceinline__ int page_of(const AppendParams& p, int b, int lp) {
+  const int phys = p.block_table[(size_t)b * p.max_pages + lp];
+  if (phys < 0 || phys >= p.num_pages) {
+    flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+    return -1;
+  }
+  return phys;
+}
+
+// fp16/bf16 cache: copy (with conversion when the source dtype differs).
+// grid (t_new, batch); each thread moves 8 elements.
+__global__ void append_copy_kernel(const AppendParams p) {
+  const int t = blockIdx.x, b = blockIdx.y;
+  int pos, n;
+  if (!row_window(p, b, pos, n) || t >= n) return;
+  const int tp = pos + t;
+  const int phys = page_of(p, b, tp / p.page_size);
+  if (phys < 0) return;
+  const int slot = tp % p.page_size;
+  const int D = p.head_dim, H = p.num_kv_heads;
+  const int per_head = D / 8;
+  for (int idx = threadIdx.x; idx < 2 * H * per_head; idx += blockDim.x) {
+    const int kv = idx / (H * per_head);
+    const int rem = idx - kv * H * per_head;
+    const int g = rem / per_head, e8 = rem - g * per_head;
+    const size_t src = (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
+    const size_t dst = (((size_t)phys * H + g) * p.page_size + slot) * D + e8 * 8;
+    const void* sp = kv ? p.v_new : p.k_new;
+    uint16_t* dp = reinterpret_cast<uint16_t*>(kv ? p.v_pages : p.k_pages);
+    if (p.src_dtype == p.kv_dtype) {
+      *reinterpret_cast<uint4*>(dp + dst) = *reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint16_t*>(sp) + src);
+    } else {
+      for (int e = 0; e < 8; ++e) {
+        const float x = load_src(sp, p.src_dtype, src + e);
+        dp[dst + e] = p.kv_dtype == PKV_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                                             : __half_as_ushort(__float2half_rn(x));
+      }
+    }
+  }
+}
+
+// Per-token INT8: one warp per (row, token, kv head, K|V) quantises head_dim values.
+__global__ void append_per_token_kernel(const AppendParams p) {
+  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = p.num_kv_heads, D = p.head_dim;
+  const long long total = (long long)p.batch * p.t_new * H * 2;
+  if (wid >= total) return;
+  const int kv = (int)(wid & 1);
+  const int g = (int)((wid >> 1) % H);
+  const long long bt = (wid >> 1) / H;
+  const int t = (int)(bt % p.t_new), b = (int)(bt / p.t_new);
+  int pos, n;
+  if (!row_window(p, b, pos, n) || t >= n) return;
+  const int tp = pos + t;
+  const int phys = page_of(p, b, tp / p.page_size);
+  if (phys < 0) return;
+  const int slot = tp % p.page_size;
+  const void* sp = kv ? p.v_new : p.k_new;
+  const size_t src = (((size_t)b * p.t_new + t) * H + g) * D;
+  const int per = D / 32;  // 4 (D = 128) or 2 (D = 64)
+  float x[4];
+  float mn = INFINITY, mx = -INFINITY;
+  for (int e = 0; e < per; ++e) {
+    x[e] = load_src(sp, p.src_dtype, src + lane * per + e);
+    mn = fminf(mn, x[e]);
+    mx = fmaxf(mx, x[e]);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
+  const float z = mn;
+  const size_t row = ((size_t)phys * H + g) * p.page_size + slot;
+  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + lane * per;
+  uint32_t packed = 0;
+  for (int e = 0; e < per; ++e) packed |= (uint32_t)(uint8_t)(int8_t)quant_code(x[e], s, z) << (8 * e);
+  if (per == 4)
+    *reinterpret_cast<uint32_t*>(dst) = packed;
+  else
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+  if (lane == 0) {
+    p.kv_sz[row * 4 + kv * 2 + 0] = s;
+    p.kv_sz[row * 4 + kv * 2 + 1] = z;
+  }
+}
+
+__device__ __forceinline__ float* tail_row(const AppendParams& p, int b, int g, int kv, int parity) {
+  return p.tail + ((((size_t)b * p.num_kv_heads + g) * 2 + kv) * 2 + parity) * 64 * p.head_dim;
+}
+
+// Per-64-token-group INT8. grid (group slot, kv head * 2 + kv, row); one block
+// re-quantises one group that received tokens: its members are the kept
+// originals of earlier tokens of the open group (tail) plus the new tokens.
+// write_tail: also keep the new members of a group that stays open.
+__global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
+  __shared__ float vals[64 * 128];
+  __shared__ float red_mn[32], red_mx[32];
+  __shared__ int ok_s;
+  const int b = blockIdx.z, g = blockIdx.y >> 1, kv = blockIdx.y & 1;
+  const int D = p.head_dim, H = p.num_kv_heads;
+  int pos, n;
+  if (!row_window(p, b, pos, n)) return;
+  const int gi = pos / 64 + blockIdx.x;
+  if (gi > (pos + n - 1) / 64) return;
+  const int t0 = gi * 64;
+  const int t_end = min(t0 + 64, pos + n);
+  const int nm = t_end - t0;
+  if (threadIdx.x == 0) ok_s = page_of(p, b, t0 / p.page_size);
+  __syncthreads();
+  const int phys = ok_s;
+  if (phys < 0) return;
+  const void* sp = kv ? p.v_new : p.k_new;
+  const float* tl = tail_row(p, b, g, kv, gi & 1);
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = threadIdx.x; i < nm * D; i += blockDim.x) {
+    const int tt = i / D, e = i - tt * D;
+    const int tok = t0 + tt;
+    float x;
+    if (tok < pos)
+      x = tl[(size_t)tt * D + e];
+    else
+      x = load_src(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
+    vals[i] = x;
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  if (lane == 0) {
+    red_mn[warp] = mn;
+    red_mx[warp] = mx;
+  }
+  __syncthreads();
+  mn = red_mn[0];
+  mx = red_mx[0];
+  for (int w = 1; w < nwarps; ++w) {
+    mn = fminf(mn, red_mn[w]);
+    mx = fmaxf(mx, red_mx[w]);
+  }
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
+  const float z = mn;
+  const int off0 = t0 % p.page_size;
+  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) +
+                (((size_t)phys * H + g) * p.page_size + off0) * D;
+  for (int i = threadIdx.x; i < nm * D; i += blockDim.x) dst[i] = (int8_t)quant_code(vals[i], s, z);
+  if (threadIdx.x == 0) {
+    float* szp = p.kv_sz + (((size_t)phys * H + g) * (p.page_size / 64) + off0 / 64) * 4;
+    szp[kv * 2 + 0] = s;
+    szp[kv * 2 + 1] = z;
+  }
+  if (write_tail && nm < 64) {
+    float* tw = tail_row(p, b, g, kv, gi & 1);
+    for (int i = threadIdx.x; i < nm * D; i += blockDim.x) {
+      const int tt = i / D;
+      if (t0 + tt >= pos) tw[i] = vals[i];
+    }
+  }
+}
+
+// Keeps the new members of each row's open group (appends longer than one
+// group, run after the quantise kernel so no block reads a tail row another
+// block rewrites). grid (kv head * 2 + kv, row).
+__global__ void append_tail_kernel(const AppendParams p) {
+  const int b = blockIdx.y, g = blockIdx.x >> 1, kv = blockIdx.x & 1;
+  const int D = p.head_dim, H = p.num_kv_heads;
+  int pos, n;
+  if (!row_window(p, b, pos, n)) return;
+  const int end = pos + n;
+  if (end % 64 == 0) return;
+  const int gi = (end - 1) / 64, t0 = gi * 64;
+  const int first = max(t0, pos);
+  const void* sp = kv ? p.v_new : p.k_new;
+  float* tw = tail_row(p, b, g, kv, gi & 1);
+  for (int i = threadIdx.x; i < (end - first) * D; i += blockDim.x) {
+    const int tt = i / D, e = i - tt * D;
+    const int tok = first + tt;
+    tw[(size_t)(tok - t0) * D + e] =
+        load_src(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
+  }
+}
+
+// Recompute the key bounding box of every page the append touched, over the
+// page's valid tokens, from the stored keys. grid (page slot, kv head, row),
+// one thread per channel.
+__global__ void append_meta_kernel(const AppendParams p) {
+  const int b = blockIdx.z, g = blockIdx.y, i = threadIdx.x;
+  const int D = p.head_dim, H = p.num_kv_heads, ps = p.page_size;
+  int pos, n;
+  if (!row_window(p, b, pos, n)) return;
+  const int lp = pos / ps + blockIdx.x;
+  if (lp > (pos + n - 1) / ps) return;
+  const int phys = page_of(p, b, lp);
+  if (phys < 0 || i >= D) return;
+  const int nv = min(ps, pos + n - lp * ps);
+  const size_t row0 = ((size_t)phys * H + g) * ps;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int s = 0; s < nv; ++s) {
+    float x;
+    if (p.kv_dtype == PKV_I8) {
+      const int code = reinterpret_cast<const int8_t*>(p.k_pages)[(row0 + s) * D + i];
+      const float* sz = p.quant == PKV_QUANT_PER_TOKEN
+                            ? p.kv_sz + (row0 + s) * 4
+                            : p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + s / 64) * 4;
+      x = __fadd_rn(__fmul_rn((float)(code + 128), sz[0]), sz[1]);
+    } else {
+      x = load_src(p.k_pages, p.kv_dtype, (row0 + s) * D + i);
+    }
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D;
+  meta[i] = mn;
+  meta[D + i] = mx;
+}
+
+}  // namespace
+
+pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
+  const int H = p.num_kv_heads;
+  if (p.kv_dtype != PKV_I8) {
+    append_copy_kernel<<<dim3(p.t_new, p.batch), 256, 0, st>>>(p);
+  } else if (p.quant == PKV_QUANT_PER_TOKEN) {
+    const long long warps = (long long)p.batch * p.t_new * H * 2;
+    const long long blocks = (warps * 32 + 255) / 256;
+    append_per_token_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+  } else {
+    const int groups = (p.t_new + 63) / 64 + 1;
+    const int inline_tail = p.t_new <= 64;
+    append_per_group_kernel<<<dim3(groups, H * 2, p.batch), 256, 0, st>>>(p, inline_tail);
+    if (!inline_tail) append_tail_kernel<<<dim3(H * 2, p.batch), 256, 0, st>>>(p);
+  }
+  if (p.page_meta) {
+    const int pages = (p.t_new + p.page_size - 1) / p.page_size + 1;
+    append_meta_kernel<<<dim3(pages, H, p.batch), p.head_dim, 0, st>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

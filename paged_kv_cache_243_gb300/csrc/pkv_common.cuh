@@ -1,0 +1,135 @@
+// Shared device helpers of the paged KV-cache kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Tokens per staged chunk: every page size is a multiple of it, so a chunk of
+// one (page, kv head) is one contiguous run of 16 * head_dim elements.
+constexpr int kChunk = 16;
+
+enum KvKind : int { KV_F16 = 0, KV_BF16 = 1, KV_I8T = 2, KV_I8G = 3 };
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+// Two 16-bit values of a 32-bit word as floats (exact widening).
+template <int KV>
+__device__ __forceinline__ void unpack2(uint32_t w, float& a, float& b) {
+  if (KV == KV_BF16) {
+    a = bf16_lo(w);
+    b = bf16_hi(w);
+  } else {
+    a = f16_lo(w);
+    b = f16_hi(w);
+  }
+}
+
+// INT8 codes c (stored with a -128 bias) as u = c + 128 in [0, 255], exactly:
+// flipping the sign bit of the byte gives u; placing u in the low mantissa
+// byte of 2^23 and subtracting 2^23 gives float(u).
+__device__ __forceinline__ float u8_as_float(uint32_t wflip, int i) {
+  return __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i)) - 8388608.0f;
+}
+
+__device__ __forceinline__ float load_q_elem(const void* q, int dtype, size_t idx) {
+  if (dtype == PKV_F16) return __half2float(reinterpret_cast<const __half*>(q)[idx]);
+  if (dtype == PKV_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[idx]);
+  return reinterpret_cast<const float*>(q)[idx];
+}
+
+__device__ __forceinline__ void store_out_elem(void* out, int dtype, size_t idx, float v) {
+  if (dtype == PKV_F16)
+    reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+  else if (dtype == PKV_BF16)
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(out)[idx] = v;
+}
+
+__device__ __forceinline__ void flag_status(int32_t* st, int bit) {
+  if (st) atomicOr(st, bit);
+}
+
+// ------------------------------------------------------------ mbarrier / TMA
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^31 cycles (about a second) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace pkv

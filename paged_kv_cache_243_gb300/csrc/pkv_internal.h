@@ -1,0 +1,51 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+struct AppendParams {
+  void* k_pages;
+  void* v_pages;
+  float* kv_sz;
+  float* tail;
+  float* page_meta;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* block_table;
+  const int32_t* positions;
+  const int32_t* new_lens;
+  int32_t* dev_status;
+  int num_pages, page_size, num_kv_heads, head_dim;
+  int kv_dtype, quant, src_dtype;
+  int batch, t_new, max_pages;
+};
+
+struct TopkParams {
+  const float* page_meta;
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t* sel_pages;
+  int32_t* sel_count;
+  float* scores_out;
+  int32_t* dev_status;
+  int num_pages, page_size, num_kv_heads, head_dim;
+  int num_q_heads, group, batch, max_pages, top_k, q_dtype;
+};
+
+pkv_status launch_append(const AppendParams& p, cudaStream_t st);
+pkv_status launch_topk(const TopkParams& p, cudaStream_t st);
+
+// Attention kernels, one getter per KV kind (each in its own translation unit).
+const void* attn_kernel_f16(int D, int GE);
+const void* attn_kernel_bf16(int D, int GE);
+const void* attn_kernel_i8t(int D, int GE);
+const void* attn_kernel_i8g(int D, int GE);
+
+// Bytes of one shared-memory stage (a 16-token chunk of K and V plus its INT8
+// scales), by KV kind and head_dim.
+int attn_stage_bytes(int kv_kind, int D);
+
+}  // namespace pkv

@@ -1,0 +1,224 @@
+// page_score_topk: score every page of a sequence against one query head with
+// the direction-aware bounding box, then keep the top-K pages [TinyServe page,
+// section 2.1 (metadata, score) and section 3.1 phases 1-2].
+//
+// One block per (sequence, query head). Phase 1: each warp scores pages
+// (lane-parallel over channels, butterfly sum), keeping the fp32 scores in
+// shared memory. Phase 2: an exact radix select (four 8-bit passes over an
+// order-preserving integer image of the scores) finds the K-th largest score
+// T; pages above T are kept, and of those equal to T the lowest page indices
+// fill the remaining places. Phase 3: a block-wide scan in page order writes
+// the kept pages in ascending order.
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+
+// Larger float -> larger unsigned key; NaN is treated as -inf.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) f = -INFINITY;
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Exclusive scan of one int per thread over the block; returns the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  int pre = 0, tot = 0;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    const int t = warp_tot[w];
+    if (w < warp) pre += t;
+    tot += t;
+  }
+  __syncthreads();
+  total = tot;
+  return pre + x - v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint32_t keys[];  // [max pages of a sequence]
+  __shared__ int hist[256];
+  __shared__ int warp_tot[kTopkWarps];
+  __shared__ int sel_digit, sel_remaining;
+
+  const int bh = blockIdx.x;
+  const int b = bh / p.num_q_heads, h = bh - b * p.num_q_heads;
+  const int g = h / p.group;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ps = p.page_size;
+  int L = p.seq_lens[b];
+  if (L < 0) L = 0;
+  int P = (L + ps - 1) / ps;
+  if (P > p.max_pages) P = p.max_pages;
+  const int K = min(p.top_k, P);
+
+  // ---- phase 1: scores
+  constexpr int PL = D / 32;  // channels per lane
+  float qv[PL];
+  bool qpos[PL];
+#pragma unroll
+  for (int e = 0; e < PL; ++e) {
+    qv[e] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h) * D + lane * PL + e);
+    qpos[e] = qv[e] >= 0.f;
+  }
+  constexpr int UNROLL = 4;
+  for (int base = warp * UNROLL; base < P; base += kTopkWarps * UNROLL) {
+    float part[UNROLL];
+    int phys[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const int pg = base + k;
+      phys[k] = pg < P ? p.block_table[(size_t)b * p.max_pages + pg] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const int pg = base + k;
+      part[k] = 0.f;
+      if (pg < P && phys[k] >= 0 && phys[k] < p.num_pages) {
+        const float* mrow = p.page_meta + (((size_t)phys[k] * p.num_kv_heads + g) * 2) * D + lane * PL;
+        float mn[PL], mx[PL];
+        if constexpr (PL == 4) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
+          const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
+          mn[0] = a.x; mn[1] = a.y; mn[2] = a.z; mn[3] = a.w;
+          mx[0] = c.x; mx[1] = c.y; mx[2] = c.z; mx[3] = c.w;
+        } else {
+          const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
+          const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
+          mn[0] = a.x; mn[1] = a.y;
+          mx[0] = c.x; mx[1] = c.y;
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) s = fmaf(qv[e], qpos[e] ? mx[e] : mn[e], s);
+        part[k] = s;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part[k] += __shfl_xor_sync(0xffffffffu, part[k], off);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const int pg = base + k;
+        if (pg >= P) break;
+        float s = part[k];
+        if (phys[k] < 0 || phys[k] >= p.num_pages) {
+          flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+          s = -INFINITY;
+        }
+        keys[pg] = __float_as_uint(s);
+        if (p.scores_out) p.scores_out[((size_t)b * p.num_q_heads + h) * p.max_pages + pg] = s;
+      }
+    }
+  }
+  if (p.scores_out) {
+    for (int pg = P + tid; pg < p.max_pages; pg += kTopkThreads)
+      p.scores_out[((size_t)b * p.num_q_heads + h) * p.max_pages + pg] = -INFINITY;
+  }
+  __syncthreads();
+
+  int32_t* sel = p.sel_pages + ((size_t)b * p.num_q_heads + h) * p.top_k;
+  if (tid == 0) p.sel_count[(size_t)b * p.num_q_heads + h] = K;
+  for (int i = K + tid; i < p.top_k; i += kTopkThreads) sel[i] = -1;
+  if (K == 0) return;
+  if (K == P) {
+    for (int i = tid; i < P; i += kTopkThreads) sel[i] = i;
+    return;
+  }
+
+  for (int i = tid; i < P; i += kTopkThreads) keys[i] = order_key(__uint_as_float(keys[i]));
+  __syncthreads();
+
+  // ---- phase 2: radix select of the K-th largest key
+  uint32_t prefix = 0, mask = 0;
+  int remaining = K;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < P; i += kTopkThreads) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int cum = 0, dgt = 255;
+      for (; dgt > 0; --dgt) {
+        if (cum + hist[dgt] >= remaining) break;
+        cum += hist[dgt];
+      }
+      sel_digit = dgt;
+      sel_remaining = remaining - cum;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sel_digit << shift;
+    mask |= 255u << shift;
+    remaining = sel_remaining;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  const int need_eq = remaining;  // how many pages scoring exactly T are kept
+
+  // ---- phase 3: ordered compaction
+  const int per = (P + kTopkThreads - 1) / kTopkThreads;
+  const int i0 = min(P, tid * per), i1 = min(P, i0 + per);
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += keys[i] == T;
+  int tot;
+  int eq_before = block_excl_scan(n_eq, warp_tot, tot);
+  int n_sel = 0;
+  {
+    int e = eq_before;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      if (k > T) ++n_sel;
+      else if (k == T) { if (e < need_eq) ++n_sel; ++e; }
+    }
+  }
+  int out = block_excl_scan(n_sel, warp_tot, tot);
+  {
+    int e = eq_before;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      bool take = false;
+      if (k > T) take = true;
+      else if (k == T) { take = e < need_eq; ++e; }
+      if (take) sel[out++] = i;
+    }
+  }
+}
+
+}  // namespace
+
+pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
+  const size_t smem = (size_t)p.max_pages * 4;
+  const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&score_topk_kernel<128>)
+                                     : reinterpret_cast<const void*>(&score_topk_kernel<64>);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  const unsigned grid = (unsigned)(p.batch * p.num_q_heads);
+  if (p.head_dim == 128)
+    score_topk_kernel<128><<<grid, kTopkThreads, smem, st>>>(p);
+  else
+    score_topk_kernel<64><<<grid, kTopkThreads, smem, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

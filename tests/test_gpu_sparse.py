@@ -1,0 +1,150 @@
+"""Query-aware sparse mode on the GPU: page bounding boxes, scores, top-K and
+attention over the selected pages, against the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import TOL, gather, load_workload, max_abs_err, oracle_bbox_keys, oracle_dense, queries_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def check_meta(ld):
+    meta = ld.cache.page_meta.cpu().numpy()      # [pages][Hkv][2][d]
+    w = ld.w
+    for b in range(w.batch):
+        L = int(ld.lens[b])
+        if L == 0:
+            continue
+        mn, mx = oracle.page_bounding_boxes(oracle_bbox_keys(w, ld.seqs[b]), w.page_size)
+        P = mn.shape[0]
+        got = meta[ld.bt[b][:P]]
+        assert np.array_equal(got[:, :, 0].view(np.uint32), mn.view(np.uint32))
+        assert np.array_equal(got[:, :, 1].view(np.uint32), mx.view(np.uint32))
+
+
+def check_selection(ld, qf, top_k, sel, cnt, scores):
+    """Scores within fp32 tolerance; kept pages bit-exact unless the oracle's K-th and
+    (K+1)-th scores tie within 1e-4 relative. Returns the page lists to attend over."""
+    w = ld.w
+    meta_sel = {}
+    for b in range(w.batch):
+        L = int(ld.lens[b])
+        P = -(-L // w.page_size)
+        mn, mx = oracle.page_bounding_boxes(oracle_bbox_keys(w, ld.seqs[b]), w.page_size)
+        r = oracle.page_scores(qf[b], mn, mx, w.group)
+        for h in range(w.num_q_heads):
+            K = min(top_k, P)
+            assert cnt[b, h] == K
+            slack = 1e-5 * (np.abs(qf[b, h])[None, :] * np.maximum(np.abs(mn[:, h // w.group]),
+                                                                 np.abs(mx[:, h // w.group]))).sum(1) + 1e-6
+            assert (np.abs(scores[b, h, :P] - r[h]) <= slack).all()
+            assert np.isneginf(scores[b, h, P:]).all()
+            want = oracle.select_top_k(r[h], K)
+            got = sel[b, h, :K]
+            assert (sel[b, h, K:] == -1).all()
+            assert (np.diff(got) > 0).all()
+            if not np.array_equal(got, want):
+                srt = np.sort(r[h])[::-1]
+                kth, nxt = srt[K - 1], srt[K]
+                assert abs(kth - nxt) <= 1e-4 * max(abs(kth), abs(nxt)), (b, h)
+                assert (r[h][got] >= nxt - slack[got]).all()
+            meta_sel[(b, h)] = got
+    return meta_sel
+
+
+def oracle_sparse(ld, qf, selected, units):
+    w = ld.w
+    res = {}
+    for b, h in units:
+        sd = ld.seqs[b]
+        o = oracle.sparse_decode_attention(qf[b, h:h + 1], sd.k[:, h // w.group:h // w.group + 1],
+                                           sd.v[:, h // w.group:h // w.group + 1], w.sm_scale,
+                                           [selected[(b, h)]], w.page_size)
+        res[(b, h)] = o[0]
+    return res
+
+
+def run_sparse(ld, q, top_k):
+    sel, cnt, scores = ld.cache.score_topk(q, ld.bt_dev, ld.lens_dev, top_k, want_scores=True,
+                                           dev_status=ld.status)
+    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=ld.w.sm_scale, sel=sel, sel_count=cnt,
+                             dev_status=ld.status)
+    torch.cuda.synchronize()
+    return sel.cpu().numpy(), cnt.cpu().numpy(), scores.cpu().numpy(), out.cpu().numpy()
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,ps,top_k", [(64, 4, 4, 16, 5), (128, 8, 2, 32, 3), (64, 8, 4, 64, 2)])
+def test_small_sparse_all_outputs(d, Hq, Hkv, ps, top_k):
+    w = synth.Workload(name="sp", seed=900 + d + ps, batch=4, layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_dim=d, page_size=ps, dtype="f16", quant="none", seq_len=None,
+                       seq_len_range=(1, 500), page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([500, 1, 37, 160], dtype=np.int32), with_meta=True)
+    check_meta(ld)
+    q, qf = queries_dev(w)
+    sel, cnt, scores, out = run_sparse(ld, q, top_k)
+    chosen = check_selection(ld, qf, top_k, sel, cnt, scores)
+    ref = oracle_sparse(ld, qf, chosen, list(chosen))
+    assert max_abs_err(out, ref) <= TOL["f16"]
+    assert int(ld.status.item()) == 0
+
+
+def test_w5_full_size_30pct_and_all_pages():
+    w = synth.WORKLOADS["w5_sparse_f16"]
+    ld = load_workload(w, with_meta=True)
+    check_meta(ld)
+    q, qf = queries_dev(w)
+    P = w.seq_len // w.page_size
+    K = oracle.top_k_count(w.top_k_ratio, P)
+    assert K == 308
+    sel, cnt, scores, out = run_sparse(ld, q, K)
+    chosen = check_selection(ld, qf, K, sel, cnt, scores)
+    rng = np.random.default_rng(5)
+    units = sorted({(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, 24), rng.integers(0, 16, 24))})
+    assert max_abs_err(out, oracle_sparse(ld, qf, chosen, units)) <= TOL["f16"]
+    # top-K = all pages reproduces dense attention
+    sel2, cnt2, scores2, out_all = run_sparse(ld, q, P)
+    assert (cnt2 == P).all() and (sel2 == np.arange(P)[None, None, :]).all()
+    dense = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale).cpu().numpy()
+    assert np.abs(out_all - dense).max() <= 1e-5
+    assert max_abs_err(out_all, oracle_dense(ld, qf, units)) <= TOL["f16"]
+    assert int(ld.status.item()) == 0
+
+
+def test_int8_per_token_boxes_and_sparse():
+    w = synth.Workload(name="sp8", seed=950, batch=3, layers=1, num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, page_size=16, dtype="f16", quant="per_token", seq_len=None,
+                       seq_len_range=(1, 300), outlier_channels=4, outlier_scale=15.0, page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([300, 45, 160], dtype=np.int32), with_meta=True)
+    check_meta(ld)
+    q, qf = queries_dev(w)
+    sel, cnt, scores, out = run_sparse(ld, q, 4)
+    chosen = check_selection(ld, qf, 4, sel, cnt, scores)
+    from helpers import oracle_kv
+    for (b, h), pages in chosen.items():
+        k, v = oracle_kv(ld, b)
+        o = oracle.sparse_decode_attention(qf[b, h:h + 1], k[:, h // 4:h // 4 + 1], v[:, h // 4:h // 4 + 1],
+                                           w.sm_scale, [pages], w.page_size)[0]
+        assert np.abs(out[b, h] - o).max() <= TOL["int8"]
+    assert int(ld.status.item()) == 0
+
+
+def test_bad_selected_page_is_reported():
+    from paged_kv_cache_243_gb300 import binding as B
+    w = dataclasses.replace(synth.WORKLOADS["w1_tiny_f16"], batch=1, seq_len=64)
+    ld = load_workload(w)
+    q, qf = queries_dev(w)
+    sel = torch.tensor([[[0, 9]] * 4], dtype=torch.int32, device="cuda")     # page 9 >= 4 pages
+    cnt = torch.full((1, 4), 2, dtype=torch.int32, device="cuda")
+    ld.status.zero_()
+    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sel=sel, sel_count=cnt, dev_status=ld.status)
+    torch.cuda.synchronize()
+    assert int(ld.status.item()) & B.DEV_BAD_SELECTED
+    out = out.cpu().numpy()
+    for h in range(4):
+        o = oracle.decode_attention_tokens(qf[0, h], ld.seqs[0].k[:16, h], ld.seqs[0].v[:16, h], w.sm_scale)
+        assert np.abs(out[0, h] - o).max() <= TOL["f16"]
