@@ -56,6 +56,7 @@ typedef enum {
 #define PKV_DEV_BAD_SELECTED 2  /* selected logical page outside the sequence */
 #define PKV_DEV_BAD_POSITION 4  /* append slot beyond the block table / bad length */
 #define PKV_DEV_TIMEOUT 8       /* a bounded wait inside a kernel gave up */
+#define PKV_DEV_BAD_CONFIG 16   /* launch parameters a kernel refuses to run with */
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2, PKV_I8 = 3 } pkv_dtype;
 
@@ -190,12 +191,14 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *                 (split-K over the whole batch's pages, each block taking an
  *                 equal share); 0 = one full wave of the device.
  *   workspace   : >= pkv_attention_workspace_bytes(...) bytes, 256-byte
- *                 aligned. Its first part holds per-sequence-head arrival
- *                 counters that must be ZERO before the first call; every call
- *                 leaves them zero again when it completes. Zero it once
- *                 (cudaMemsetAsync) after allocating it.
- * Partial results of each block (running max, sum, accumulator) are merged in
- * the same launch by the last block to finish each (sequence, kv head).
+ *                 aligned, any contents (it holds the per-block partial states
+ *                 of one call; no initialisation is needed).
+ * Two launches: the attention kernel, and (when num_splits != 1) a combine
+ * kernel that merges, for each (sequence, kv head) shared by several blocks,
+ * the blocks' partial (running max, sum, accumulator) states. Both are
+ * launched with programmatic stream serialization, and every kernel of this
+ * library waits for the preceding kernel on the stream before its first
+ * global memory access, so stream order is kept.
  * A sequence with no tokens (or no selected pages) yields zeros.
  * Device errors: PKV_DEV_BAD_PAGE, PKV_DEV_BAD_SELECTED (chunk skipped),
  * PKV_DEV_TIMEOUT.

@@ -18,7 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 F16, BF16, F32, I8 = 0, 1, 2, 3
 QUANT_NONE, QUANT_PER_TOKEN, QUANT_PER_GROUP64 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_PAGES, ERR_CUDA, ERR_WORKSPACE = range(6)
-DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_BAD_CONFIG = 1, 2, 4, 8, 16
 
 EXPORTED = [
     "pkv_status_string", "pkv_abi_version", "pkv_kv_append", "pkv_page_score_topk",

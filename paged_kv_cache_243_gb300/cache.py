@@ -132,10 +132,11 @@ class PagedKVCache:
 
     # --------------------------------------------------------------- attention
     def workspace(self, batch: int, num_q_heads: int, sparse: bool, num_splits: int) -> torch.Tensor:
+        """Zero-filled workspace of at least the size the library asks for (kept and reused)."""
         key = (batch, num_q_heads, bool(sparse), num_splits)
+        n = B.attention_workspace_bytes(self._desc, batch, num_q_heads, sparse, num_splits)
         ws = self._ws.get(key)
-        if ws is None:
-            n = B.attention_workspace_bytes(self._desc, batch, num_q_heads, sparse, num_splits)
+        if ws is None or ws.numel() < n:
             ws = torch.zeros(n, dtype=torch.uint8, device=self.device)
             self._ws[key] = ws
         return ws

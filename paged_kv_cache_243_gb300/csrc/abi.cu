@@ -119,6 +119,15 @@ int kv_kind(const pkv_cache* c) {
   return c->quant == PKV_QUANT_PER_TOKEN ? KV_I8T : KV_I8G;
 }
 
+const void* attn_combine(int D, int ge) {
+#define PKV_COMB(d, g) \
+  if (D == d && ge == g) return reinterpret_cast<const void*>(&attn_combine_kernel<d, g>);
+  PKV_COMB(64, 1) PKV_COMB(64, 2) PKV_COMB(64, 4) PKV_COMB(64, 8)
+  PKV_COMB(128, 1) PKV_COMB(128, 2) PKV_COMB(128, 4) PKV_COMB(128, 8)
+#undef PKV_COMB
+  return nullptr;
+}
+
 const void* attn_kernel(int kind, int D, int ge) {
   switch (kind) {
     case KV_F16: return attn_kernel_f16(D, ge);
@@ -132,7 +141,7 @@ struct AttnPlan {
   const void* fn = nullptr;
   int ge = 1, units = 0, stages = 0, ctas = 0;
   size_t smem = 0;
-  size_t off_m = 0, off_l = 0, off_acc = 0, ws_bytes = 0;
+  size_t off_wrec = 0, off_crec = 0, ws_bytes = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -153,18 +162,24 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   DeviceInfo di;
   st = device_info(di);
   if (st != PKV_OK) return st;
+  // The stage count is a multiple of the consumer-warp count: consumer warp w
+  // takes chunks w, w + 4, ..., so every stage is then read by one warp only and
+  // that warp waits on the stage's phases strictly in order. (A parity wait on a
+  // phase two ahead of the barrier's current phase would pass at once.)
   const int stage = attn_stage_bytes(kind, c->head_dim);
   const int ring_kb = env_int("PKV_ATTN_RING_KB", 64);
   int stages = (ring_kb * 1024) / stage;
-  stages = stages < 2 ? 2 : (stages > 32 ? 32 : stages);
   const int forced = env_int("PKV_ATTN_STAGES", 0);
-  if (forced >= 2 && forced <= 64) stages = forced;
+  if (forced > 0) stages = forced;
+  stages = stages / kConsumerWarps * kConsumerWarps;
+  stages = stages < kConsumerWarps ? kConsumerWarps : (stages > 32 ? 32 : stages);
   size_t smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
-  while (smem > (size_t)di.max_smem_optin && stages > 2) {
-    --stages;
+  while (smem > (size_t)di.max_smem_optin && stages > kConsumerWarps) {
+    stages -= kConsumerWarps;
     smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
   }
   if (smem > (size_t)di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
+  if (stages % kConsumerWarps != 0) return PKV_ERR_UNSUPPORTED;
   pl.stages = stages;
   pl.smem = smem;
   if (num_splits > 0) {
@@ -177,14 +192,13 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     if (cap > 0 && cap < nb) nb = cap;
     pl.ctas = di.sms * nb;
   }
-  const size_t slots = (size_t)(pl.ctas + pl.units) * kConsumerWarps;
-  size_t off = align256((size_t)pl.units * 4);
-  pl.off_m = off;
-  off = align256(off + slots * pl.ge * 4);
-  pl.off_l = off;
-  off = align256(off + slots * pl.ge * 4);
-  pl.off_acc = off;
-  off = align256(off + slots * pl.ge * c->head_dim * 4);
+  const size_t rs = (size_t)rec_floats(pl.ge, c->head_dim);
+  const size_t cslots = (size_t)(pl.ctas + pl.units);
+  size_t off = align256((size_t)(pl.units + 1) * 4);        // unit chunk prefix
+  pl.off_wrec = off;
+  off = align256(off + cslots * kConsumerWarps * rs * 4);    // warp records
+  pl.off_crec = off;
+  off = align256(off + cslots * rs * 4);                     // block records
   pl.ws_bytes = off;
   return PKV_OK;
 }
@@ -255,10 +269,9 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.sel_pages = sel_pages;
   p.sel_count = sel_count;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.ws_counter = reinterpret_cast<int32_t*>(ws);
-  p.ws_m = reinterpret_cast<float*>(ws + pl.off_m);
-  p.ws_l = reinterpret_cast<float*>(ws + pl.off_l);
-  p.ws_acc = reinterpret_cast<float*>(ws + pl.off_acc);
+  p.ws_prefix = reinterpret_cast<int32_t*>(ws);
+  p.ws_wrec = reinterpret_cast<float*>(ws + pl.off_wrec);
+  p.ws_crec = reinterpret_cast<float*>(ws + pl.off_crec);
   p.dev_status = dev_status;
   p.num_pages = cache->num_pages;
   p.page_size = cache->page_size;
@@ -276,8 +289,12 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.out_dtype = out_dtype;
   p.q_scale = sm_scale * 1.4426950408889634f;
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), args, pl.smem,
-                                   static_cast<cudaStream_t>(stream));
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);
+  if (e == cudaSuccess && pl.ctas > 1) {
+    const void* comb = attn_combine(cache->head_dim, pl.ge);
+    e = launch_pdl(comb, dim3(pl.units), dim3(128), 0, cs, args);
+  }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

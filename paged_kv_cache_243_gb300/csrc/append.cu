@@ -47,40 +47,60 @@ __device__ __forceinline__ int page_of(const AppendParams& p, int b, int lp) {
 }
 
 // fp16/bf16 cache: copy (with conversion when the source dtype differs).
-// grid (t_new, batch); each thread moves 8 elements.
+// grid (t_new, batch); each thread moves 8 elements per pass. The source rows
+// are loaded before the block-table lookup so the two latencies overlap.
 __global__ void append_copy_kernel(const AppendParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x, b = blockIdx.y;
+  const int D = p.head_dim, H = p.num_kv_heads;
+  const int per_head = D / 8;
+  const int total = 2 * H * per_head;
+  constexpr int kMaxPer = 4;  // 16-byte vectors per thread held across the lookup
+  uint4 vals[kMaxPer];
+  int n_mine = 0;
+  for (int idx = threadIdx.x; idx < total && n_mine < kMaxPer; idx += blockDim.x, ++n_mine) {
+    const int kv = idx / (H * per_head);
+    const int rem = idx - kv * H * per_head;
+    const int g = rem / per_head, e8 = rem - g * per_head;
+    const size_t src = (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
+    vals[n_mine] = *reinterpret_cast<const uint4*>(
+        reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src);
+  }
   int pos, n;
   if (!row_window(p, b, pos, n) || t >= n) return;
   const int tp = pos + t;
   const int phys = page_of(p, b, tp / p.page_size);
   if (phys < 0) return;
   const int slot = tp % p.page_size;
-  const int D = p.head_dim, H = p.num_kv_heads;
-  const int per_head = D / 8;
-  for (int idx = threadIdx.x; idx < 2 * H * per_head; idx += blockDim.x) {
+  int i = 0;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x, ++i) {
     const int kv = idx / (H * per_head);
     const int rem = idx - kv * H * per_head;
     const int g = rem / per_head, e8 = rem - g * per_head;
     const size_t src = (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
     const size_t dst = (((size_t)phys * H + g) * p.page_size + slot) * D + e8 * 8;
-    const void* sp = kv ? p.v_new : p.k_new;
     uint16_t* dp = reinterpret_cast<uint16_t*>(kv ? p.v_pages : p.k_pages);
-    if (p.src_dtype == p.kv_dtype) {
-      *reinterpret_cast<uint4*>(dp + dst) = *reinterpret_cast<const uint4*>(
-          reinterpret_cast<const uint16_t*>(sp) + src);
-    } else {
+    uint4 v = i < kMaxPer ? vals[i]
+                          : *reinterpret_cast<const uint4*>(
+                                reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src);
+    if (p.src_dtype != p.kv_dtype) {
+      uint16_t* h = reinterpret_cast<uint16_t*>(&v);
       for (int e = 0; e < 8; ++e) {
-        const float x = load_src(sp, p.src_dtype, src + e);
-        dp[dst + e] = p.kv_dtype == PKV_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
-                                             : __half_as_ushort(__float2half_rn(x));
+        const float x = p.src_dtype == PKV_BF16 ? __bfloat162float(__ushort_as_bfloat16(h[e]))
+                                                : __half2float(__ushort_as_half(h[e]));
+        h[e] = p.kv_dtype == PKV_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                                      : __half_as_ushort(__float2half_rn(x));
       }
     }
+    *reinterpret_cast<uint4*>(dp + dst) = v;
   }
 }
 
 // Per-token INT8: one warp per (row, token, kv head, K|V) quantises head_dim values.
 __global__ void append_per_token_kernel(const AppendParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.num_kv_heads, D = p.head_dim;
@@ -135,6 +155,8 @@ __device__ __forceinline__ float* tail_row(const AppendParams& p, int b, int g, 
 // originals of earlier tokens of the open group (tail) plus the new tokens.
 // write_tail: also keep the new members of a group that stays open.
 __global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float vals[64 * 128];
   __shared__ float red_mn[32], red_mx[32];
   __shared__ int ok_s;
@@ -206,6 +228,8 @@ __global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
 // group, run after the quantise kernel so no block reads a tail row another
 // block rewrites). grid (kv head * 2 + kv, row).
 __global__ void append_tail_kernel(const AppendParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.y, g = blockIdx.x >> 1, kv = blockIdx.x & 1;
   const int D = p.head_dim, H = p.num_kv_heads;
   int pos, n;
@@ -228,6 +252,8 @@ __global__ void append_tail_kernel(const AppendParams p) {
 // page's valid tokens, from the stored keys. grid (page slot, kv head, row),
 // one thread per channel.
 __global__ void append_meta_kernel(const AppendParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.z, g = blockIdx.y, i = threadIdx.x;
   const int D = p.head_dim, H = p.num_kv_heads, ps = p.page_size;
   int pos, n;
@@ -262,23 +288,33 @@ __global__ void append_meta_kernel(const AppendParams p) {
 
 pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
   const int H = p.num_kv_heads;
+  AppendParams pc = p;
+  void* args1[] = {&pc};
+  cudaError_t e = cudaSuccess;
   if (p.kv_dtype != PKV_I8) {
-    append_copy_kernel<<<dim3(p.t_new, p.batch), 256, 0, st>>>(p);
+    e = launch_pdl(reinterpret_cast<const void*>(&append_copy_kernel), dim3(p.t_new, p.batch), dim3(256), 0,
+                   st, args1);
   } else if (p.quant == PKV_QUANT_PER_TOKEN) {
     const long long warps = (long long)p.batch * p.t_new * H * 2;
     const long long blocks = (warps * 32 + 255) / 256;
-    append_per_token_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    e = launch_pdl(reinterpret_cast<const void*>(&append_per_token_kernel), dim3((unsigned)blocks), dim3(256),
+                   0, st, args1);
   } else {
     const int groups = (p.t_new + 63) / 64 + 1;
-    const int inline_tail = p.t_new <= 64;
-    append_per_group_kernel<<<dim3(groups, H * 2, p.batch), 256, 0, st>>>(p, inline_tail);
-    if (!inline_tail) append_tail_kernel<<<dim3(H * 2, p.batch), 256, 0, st>>>(p);
+    int inline_tail = p.t_new <= 64;
+    void* args2[] = {&pc, &inline_tail};
+    e = launch_pdl(reinterpret_cast<const void*>(&append_per_group_kernel), dim3(groups, H * 2, p.batch),
+                   dim3(256), 0, st, args2);
+    if (e == cudaSuccess && !inline_tail)
+      e = launch_pdl(reinterpret_cast<const void*>(&append_tail_kernel), dim3(H * 2, p.batch), dim3(256), 0,
+                     st, args1);
   }
-  if (p.page_meta) {
+  if (e == cudaSuccess && p.page_meta) {
     const int pages = (p.t_new + p.page_size - 1) / p.page_size + 1;
-    append_meta_kernel<<<dim3(pages, H, p.batch), p.head_dim, 0, st>>>(p);
+    e = launch_pdl(reinterpret_cast<const void*>(&append_meta_kernel), dim3(pages, H, p.batch),
+                   dim3(p.head_dim), 0, st, args1);
   }
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -46,6 +46,9 @@ namespace pkv {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+// Small shared scratch: [0] [1] merge masks, [4, 4 + 2 * 8) per-head M and L of
+// the cross-block merge, [8, 8 + warps) scan totals (used before streaming).
+constexpr int kMiscInts = 32;
 
 struct AttnParams {
   const uint8_t* k_pages;
@@ -57,10 +60,9 @@ struct AttnParams {
   const int32_t* seq_lens;
   const int32_t* sel_pages;  // NULL: dense
   const int32_t* sel_count;
-  float* ws_m;
-  float* ws_l;
-  float* ws_acc;
-  int32_t* ws_counter;
+  float* ws_wrec;     // per-warp partial records, slot ((block + unit) * 4 + warp)
+  float* ws_crec;     // per-block partial records, slot (block + unit)
+  int32_t* ws_prefix; // [num_units + 1] chunk prefix, written by block 0 for the combine
   int32_t* dev_status;
   int num_pages, page_size, num_kv_heads, num_q_heads, group;
   int batch, max_pages, sel_stride;
@@ -96,6 +98,11 @@ struct AttnSmem {
   static constexpr int PBUF = kChunk * GE + 8;     // floats per warp: p[16][GE], alpha[GE]
 };
 
+// Partial-state record of one (block or warp, unit): m[GE], l[GE] (padded to a
+// multiple of 4 floats), then acc[GE][D]. All in the log2 domain.
+__host__ __device__ constexpr int rec_hdr(int ge) { return (2 * ge + 3) / 4 * 4; }
+__host__ __device__ constexpr int rec_floats(int ge, int d) { return rec_hdr(ge) + ge * d; }
+
 __host__ __device__ inline size_t attn_smem_bytes(int stage_bytes, int stages, int ge, int units,
                                                   int batch) {
   size_t s = (size_t)stage_bytes * stages;
@@ -103,7 +110,7 @@ __host__ __device__ inline size_t attn_smem_bytes(int stage_bytes, int stages, i
   s += (size_t)stages * 16;                       // full + empty mbarriers
   s += (size_t)kConsumerWarps * (kChunk * ge + 8) * 4;
   s += 32 * sizeof(ChunkInfo);
-  s += 16 * 4;                                    // misc
+  s += kMiscInts * 4;                              // misc
   s += (size_t)(units + 1) * 4 + (size_t)batch * 4;
   return (s + 15) / 16 * 16;
 }
@@ -115,65 +122,54 @@ __device__ __forceinline__ int qk_dim(int j, int e) {
   return AttnGeom<D, KV>::QD * j + e;
 }
 
-// Load this lane's D/8 channels of token row `row` (score layout), as floats
-// (INT8: u = code + 128).
+// Load this lane's D/8 channels of token row `row` (score layout) as packed
+// fp32 pairs (INT8: u = code + 128).
 template <int D, int KV>
-__device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, float (&kf)[D / 8]) {
+__device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, uint64_t (&k2)[D / 16]) {
   if constexpr (KV == KV_F16 || KV == KV_BF16) {
     if constexpr (D == 128) {
-      uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
-      uint4 b = *reinterpret_cast<const uint4*>(row + (j + 8) * 16);
-      unpack2<KV>(a.x, kf[0], kf[1]);
-      unpack2<KV>(a.y, kf[2], kf[3]);
-      unpack2<KV>(a.z, kf[4], kf[5]);
-      unpack2<KV>(a.w, kf[6], kf[7]);
-      unpack2<KV>(b.x, kf[8], kf[9]);
-      unpack2<KV>(b.y, kf[10], kf[11]);
-      unpack2<KV>(b.z, kf[12], kf[13]);
-      unpack2<KV>(b.w, kf[14], kf[15]);
+      const uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
+      const uint4 b = *reinterpret_cast<const uint4*>(row + (j + 8) * 16);
+      k2[0] = widen2<KV>(a.x); k2[1] = widen2<KV>(a.y); k2[2] = widen2<KV>(a.z); k2[3] = widen2<KV>(a.w);
+      k2[4] = widen2<KV>(b.x); k2[5] = widen2<KV>(b.y); k2[6] = widen2<KV>(b.z); k2[7] = widen2<KV>(b.w);
     } else {
-      uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
-      unpack2<KV>(a.x, kf[0], kf[1]);
-      unpack2<KV>(a.y, kf[2], kf[3]);
-      unpack2<KV>(a.z, kf[4], kf[5]);
-      unpack2<KV>(a.w, kf[6], kf[7]);
+      const uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
+      k2[0] = widen2<KV>(a.x); k2[1] = widen2<KV>(a.y); k2[2] = widen2<KV>(a.z); k2[3] = widen2<KV>(a.w);
     }
   } else {
     if constexpr (D == 128) {
-      uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
-      uint32_t w[4] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u, a.z ^ 0x80808080u, a.w ^ 0x80808080u};
+      const uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
+      const uint32_t w[4] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u, a.z ^ 0x80808080u, a.w ^ 0x80808080u};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) kf[i] = u8_as_float(w[i >> 2], i & 3);
+      for (int i = 0; i < 8; ++i) k2[i] = u8pair(w[i >> 1], (i & 1) * 2);
     } else {
-      uint2 a = *reinterpret_cast<const uint2*>(row + j * 8);
-      uint32_t w[2] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u};
+      const uint2 a = *reinterpret_cast<const uint2*>(row + j * 8);
+      const uint32_t w[2] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) kf[i] = u8_as_float(w[i >> 2], i & 3);
+      for (int i = 0; i < 4; ++i) k2[i] = u8pair(w[i >> 1], (i & 1) * 2);
     }
   }
 }
 
-// Load this lane's D/32 channels of token row `row` (value layout).
+// Load this lane's D/32 channels of token row `row` (value layout) as packed pairs.
 template <int D, int KV>
-__device__ __forceinline__ void load_v_slice(const uint8_t* row, int lane, float (&vf)[D / 32]) {
+__device__ __forceinline__ void load_v_slice(const uint8_t* row, int lane, uint64_t (&v2)[D / 64]) {
   if constexpr (KV == KV_F16 || KV == KV_BF16) {
     if constexpr (D == 128) {
-      uint2 a = *reinterpret_cast<const uint2*>(row + lane * 8);
-      unpack2<KV>(a.x, vf[0], vf[1]);
-      unpack2<KV>(a.y, vf[2], vf[3]);
+      const uint2 a = *reinterpret_cast<const uint2*>(row + lane * 8);
+      v2[0] = widen2<KV>(a.x);
+      v2[1] = widen2<KV>(a.y);
     } else {
-      uint32_t a = *reinterpret_cast<const uint32_t*>(row + lane * 4);
-      unpack2<KV>(a, vf[0], vf[1]);
+      v2[0] = widen2<KV>(*reinterpret_cast<const uint32_t*>(row + lane * 4));
     }
   } else {
     if constexpr (D == 128) {
-      uint32_t a = *reinterpret_cast<const uint32_t*>(row + lane * 4) ^ 0x80808080u;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vf[i] = u8_as_float(a, i);
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(row + lane * 4) ^ 0x80808080u;
+      v2[0] = u8pair(a, 0);
+      v2[1] = u8pair(a, 2);
     } else {
-      uint32_t a = (uint32_t)(*reinterpret_cast<const uint16_t*>(row + lane * 2)) ^ 0x8080u;
-      vf[0] = u8_as_float(a, 0);
-      vf[1] = u8_as_float(a, 1);
+      const uint32_t a = (uint32_t)(*reinterpret_cast<const uint16_t*>(row + lane * 2)) ^ 0x8080u;
+      v2[0] = u8pair(a, 0);
     }
   }
 }
@@ -257,14 +253,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
   float* pbuf_all = reinterpret_cast<float*>(empty + S);
   ChunkInfo* info = reinterpret_cast<ChunkInfo*>(pbuf_all + NW * PBUF);
   int* misc = reinterpret_cast<int*>(info + 32);
-  int* prefix = misc + 16;
+  int* prefix = misc + kMiscInts;
   int* lens = prefix + p.num_units + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.num_units;
+  if (S <= 0 || S % NW != 0 || S > 32) {  // the host never launches this; refuse rather than race
+    if (tid == 0) flag_status(p.dev_status, PKV_DEV_BAD_CONFIG);
+    return;
+  }
   const int ps = p.page_size;
   const bool sparse = p.sel_pages != nullptr;
 
+  pdl_wait();
+  pdl_launch_dependents();
   // ---- sequence lengths (clamped to the block table) and unit chunk counts
   for (int b = tid; b < p.batch; b += kAttnThreads) {
     int L = p.seq_lens[b];
@@ -328,6 +330,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
   }
   __syncthreads();
 
+  if (blockIdx.x == 0)
+    for (int u = tid; u <= U; u += kAttnThreads) p.ws_prefix[u] = prefix[u];
   const long long W = prefix[U];
   const long long N = p.num_ctas;
   const int c = blockIdx.x;
@@ -350,56 +354,70 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
 
   if (warp == NW) {
     // ================================================================ producer
+    // Lane l resolves chunk base + l of each batch of 32. The table entries of
+    // batch k + 1 are loaded before lane 0 issues the copies of batch k, so
+    // their latency overlaps the streaming of batch k.
     const uint64_t pol = policy_evict_first();
+    const int cpp = ps / kChunk;
+    // raw lookup of chunk x: unit, chunk-in-unit, and the loaded table entries
+    struct Raw {
+      int u, k, sp, phys;
+    };
+    auto fetch = [&](int x, Raw& r) {   // issues the global loads
+      r.u = -1; r.k = 0; r.sp = 0; r.phys = -1;
+      if (x >= hi) return;
+      r.u = find_unit(prefix, U, x);
+      r.k = x - prefix[r.u];
+      const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
+      if (!sparse) {
+        const int lp = (r.k * kChunk) / ps;
+        if (r.k * kChunk < lens[b]) r.phys = p.block_table[(size_t)b * p.max_pages + lp];
+      } else {
+        r.sp = p.sel_pages[(size_t)(b * p.num_q_heads + hu) * p.sel_stride + r.k / cpp];
+      }
+    };
+    auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
+      ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
+      ci.nvalid = 0; ci.valid = 0; ci.pad = 0;
+      if (r.u < 0) return;
+      const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
+      const int L = lens[b];
+      int t0, g, phys = r.phys;
+      if (!sparse) {
+        t0 = r.k * kChunk;
+        g = hu;
+      } else {
+        g = hu / p.group;
+        if (r.sp < 0 || (long long)r.sp * ps >= L) {
+          flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
+          return;
+        }
+        t0 = r.sp * ps + (r.k % cpp) * kChunk;
+        if (t0 < L) phys = p.block_table[(size_t)b * p.max_pages + t0 / ps];
+      }
+      const int nv = min(kChunk, L - t0);
+      if (nv <= 0) return;
+      if (phys < 0 || phys >= p.num_pages) {
+        flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+        return;
+      }
+      const int off = t0 % ps;
+      const size_t row0 = ((size_t)phys * p.num_kv_heads + g) * ps + off;
+      ci.k = p.k_pages + row0 * Geo::ROW;
+      ci.v = p.v_pages + row0 * Geo::ROW;
+      if constexpr (KV == KV_I8T) ci.sz = p.kv_sz + row0 * 4;
+      if constexpr (KV == KV_I8G)
+        ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
+      ci.nvalid = nv;
+      ci.valid = 1;
+    };
     int n = 0;
     bool abort = false;
+    Raw cur;
+    fetch(lo + lane, cur);
     for (int base = lo; base < hi && !abort; base += 32) {
-      const int x = base + lane;
       ChunkInfo ci;
-      ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = 0; ci.nvalid = 0; ci.valid = 0; ci.pad = 0;
-      if (x < hi) {
-        const int u = find_unit(prefix, U, x);
-        const int k = x - prefix[u];
-        const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-        const int L = lens[b];
-        int t0, g;
-        bool ok = true;
-        if (!sparse) {
-          t0 = k * kChunk;
-          g = hu;
-        } else {
-          const int cpp = ps / kChunk;
-          const int sp = p.sel_pages[(size_t)(b * p.num_q_heads + hu) * p.sel_stride + k / cpp];
-          g = hu / p.group;
-          if (sp < 0 || (long long)sp * ps >= L) {
-            flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
-            ok = false;
-            t0 = 0;
-          } else {
-            t0 = sp * ps + (k % cpp) * kChunk;
-          }
-        }
-        ci.u = u;
-        if (ok) {
-          const int nv = min(kChunk, L - t0);
-          if (nv > 0) {
-            const int lp = t0 / ps, off = t0 - lp * ps;
-            const int phys = p.block_table[(size_t)b * p.max_pages + lp];
-            if (phys < 0 || phys >= p.num_pages) {
-              flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
-            } else {
-              const size_t row0 = ((size_t)phys * p.num_kv_heads + g) * ps + off;
-              ci.k = p.k_pages + row0 * Geo::ROW;
-              ci.v = p.v_pages + row0 * Geo::ROW;
-              if constexpr (KV == KV_I8T) ci.sz = p.kv_sz + row0 * 4;
-              if constexpr (KV == KV_I8G)
-                ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
-              ci.nvalid = nv;
-              ci.valid = 1;
-            }
-          }
-        }
-      }
+      resolve(cur, ci);
       info[lane] = ci;
       __syncwarp();
       const int cnt = min(32, hi - base);
@@ -426,7 +444,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
         }
       }
       abort = __shfl_sync(0xffffffffu, abort ? 1 : 0, 0) != 0;
+      n = __shfl_sync(0xffffffffu, n, 0);
       __syncwarp();
+      // the next batch's table loads overlap the streaming of the stages just issued
+      fetch(base + 32 + lane, cur);
     }
     // Let every issued copy land before this warp (and so the block) can exit.
     if (lane == 0) {
@@ -446,38 +467,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
   const int my_head = j / DUP;  // head this lane holds after the score reduction
   float* pb = pbuf_all + warp * PBUF;
 
-  float q[GE][QD];
+  constexpr int QD2 = QD / 2, PD2 = PD / 2;
+  uint64_t q2[GE][QD2];  // q * sm_scale * log2(e), packed pairs (score layout)
   float qsum = 0.f;
-  float acc[GE][PD];
+  uint64_t acc2[GE][PD2];
   float m_h = -INFINITY, l_h = 0.f, zs = 0.f;
   int u_cur = -1, next_unit = ua;
 
-  auto slot_of = [&](int u) { return (size_t)(c + u) * NW + warp; };
+  constexpr int WRS = rec_floats(GE, D), WHDR = rec_hdr(GE);
+  auto rec_of = [&](int u) { return p.ws_wrec + ((size_t)(c + u) * NW + warp) * WRS; };
 
   auto write_empty = [&](int u) {
     if (lane < GE) {
-      const size_t sl = slot_of(u) * GE + lane;
-      p.ws_m[sl] = -INFINITY;
-      p.ws_l[sl] = 0.f;
+      float* rec = rec_of(u);
+      rec[lane] = -INFINITY;
+      rec[GE + lane] = 0.f;
     }
   };
 
   auto flush = [&](int u) {
-    const size_t sl = slot_of(u);
+    float* rec = rec_of(u);
 #pragma unroll
     for (int h = 0; h < GE; ++h) {
       const float zh = __shfl_sync(0xffffffffu, zs, h * DUP);
-      float* dst = p.ws_acc + (sl * GE + h) * D + lane * PD;
+      float* dst = rec + WHDR + h * D + lane * PD;
+      float a0, a1;
+      unpack2f(acc2[h][0], a0, a1);
       if constexpr (PD == 4) {
-        *reinterpret_cast<float4*>(dst) =
-            make_float4(acc[h][0] + zh, acc[h][1] + zh, acc[h][2] + zh, acc[h][3] + zh);
+        float a2, a3;
+        unpack2f(acc2[h][1], a2, a3);
+        *reinterpret_cast<float4*>(dst) = make_float4(a0 + zh, a1 + zh, a2 + zh, a3 + zh);
       } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(acc[h][0] + zh, acc[h][1] + zh);
+        *reinterpret_cast<float2*>(dst) = make_float2(a0 + zh, a1 + zh);
       }
     }
     if (r == 0 && (j % DUP) == 0) {
-      p.ws_m[sl * GE + my_head] = m_h;
-      p.ws_l[sl * GE + my_head] = l_h;
+      rec[my_head] = m_h;
+      rec[GE + my_head] = l_h;
     }
   };
 
@@ -489,10 +515,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     for (int h = 0; h < GE; ++h) {
       float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < QD; ++e) {
-        const size_t idx = ((size_t)b * p.num_q_heads + qh0 + h) * D + qk_dim<D, KV>(j, e);
-        q[h][e] = load_q_elem(p.q, p.q_dtype, idx) * p.q_scale;
-        s += q[h][e];
+      for (int e = 0; e < QD2; ++e) {
+        const size_t idx = ((size_t)b * p.num_q_heads + qh0 + h) * D;
+        const float x0 = load_q_elem(p.q, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e)) * p.q_scale;
+        const float x1 = load_q_elem(p.q, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e + 1)) * p.q_scale;
+        q2[h][e] = pack2f(x0, x1);
+        s += x0 + x1;
       }
       part[h] = s;
     }
@@ -500,13 +528,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
 #pragma unroll
     for (int h = 0; h < GE; ++h)
 #pragma unroll
-      for (int e = 0; e < PD; ++e) acc[h][e] = 0.f;
+      for (int e = 0; e < PD2; ++e) acc2[h][e] = 0ull;
     m_h = -INFINITY;
     l_h = 0.f;
     zs = 0.f;
   };
 
   bool abort = false;
+  // S is a multiple of NW (checked by the host), so stage s is only ever read by
+  // warp s % NW, which waits on its phases 0, 1, 2, ... in order.
   for (int n = warp; lo + n < hi; n += NW) {
     const int s = n % S, use = n / S;
     if (!mbar_wait_bounded(smem_u32(&full[s]), use & 1)) {
@@ -537,15 +567,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int t = 4 * it + r;
-        float kf[QD];
-        load_k_slice<D, KV>(st + t * Geo::ROW, j, kf);
+        uint64_t k2[QD2];
+        load_k_slice<D, KV>(st + t * Geo::ROW, j, k2);
         float part[GE];
 #pragma unroll
         for (int h = 0; h < GE; ++h) {
-          float a = 0.f;
+          uint64_t a = ffma2(q2[h][0], k2[0], 0ull);
 #pragma unroll
-          for (int e = 0; e < QD; ++e) a = fmaf(q[h][e], kf[e], a);
-          part[h] = a;
+          for (int e = 1; e < QD2; ++e) a = ffma2(q2[h][e], k2[e], a);
+          part[h] = hsum2(a);
         }
         float sv = reduce_scatter8<GE>(part, j);
         if constexpr (KV == KV_I8T) sv = fmaf(sz[t * 4 + 0], sv, sz[t * 4 + 1] * qsum);
@@ -599,33 +629,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
 #pragma unroll
       for (int h = 0; h < GE; ++h) {
         const float al = pb[kChunk * GE + h];
+        const uint64_t al2 = pack2f(al, al);
 #pragma unroll
-        for (int e = 0; e < PD; ++e) acc[h][e] *= al;
+        for (int e = 0; e < PD2; ++e) acc2[h][e] = fmul2(acc2[h][e], al2);
       }
       const uint8_t* vrow = st + KB;
+      auto pv_token = [&](int t) {
+        uint64_t v2[PD2];
+        load_v_slice<D, KV>(vrow + t * Geo::ROW, lane, v2);
+#pragma unroll
+        for (int h = 0; h < GE; ++h) {
+          const float pv = pb[t * GE + h];
+          const uint64_t pv2 = pack2f(pv, pv);
+#pragma unroll
+          for (int e = 0; e < PD2; ++e) acc2[h][e] = ffma2(pv2, v2[e], acc2[h][e]);
+        }
+      };
       if (nvalid == kChunk) {
 #pragma unroll
-        for (int t = 0; t < kChunk; ++t) {
-          float vf[PD];
-          load_v_slice<D, KV>(vrow + t * Geo::ROW, lane, vf);
-#pragma unroll
-          for (int h = 0; h < GE; ++h) {
-            const float pv = pb[t * GE + h];
-#pragma unroll
-            for (int e = 0; e < PD; ++e) acc[h][e] = fmaf(pv, vf[e], acc[h][e]);
-          }
-        }
+        for (int t = 0; t < kChunk; ++t) pv_token(t);
       } else {
-        for (int t = 0; t < nvalid; ++t) {
-          float vf[PD];
-          load_v_slice<D, KV>(vrow + t * Geo::ROW, lane, vf);
-#pragma unroll
-          for (int h = 0; h < GE; ++h) {
-            const float pv = pb[t * GE + h];
-#pragma unroll
-            for (int e = 0; e < PD; ++e) acc[h][e] = fmaf(pv, vf[e], acc[h][e]);
-          }
-        }
+        for (int t = 0; t < nvalid; ++t) pv_token(t);
       }
     }
     __syncwarp();
@@ -639,61 +663,135 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     for (int v = next_unit; v <= ub; ++v) write_empty(v);
   }
 
-  // ---- merge: the last block to finish a unit combines its partials
-  __threadfence();
+  // ---- in-block merge. Every unit this block touched gets one block record
+  // from its 4 warp records; a unit that lies entirely inside this block is
+  // final here and goes to the output. Units shared with other blocks are
+  // finished by attn_combine_kernel, the next launch on the stream.
+  constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
+  constexpr int OUTS = GE * D;                           // outputs of one unit
+  constexpr int OPT = (OUTS + NW * 32 - 1) / (NW * 32);  // outputs per thread
   named_bar_sync(1, NW * 32);
   for (int u = ua; u <= ub; ++u) {
-    const int s0 = prefix[u], s1 = prefix[u + 1];
-    const int c_first = cta_of(s0, W, N), c_last = cta_of(s1 - 1, W, N);
-    if (tid == 0) {
-      int expected = 0;
-      for (int cc = c_first; cc <= c_last; ++cc)
-        if (cta_lo(cc, W, N) < cta_lo(cc + 1, W, N)) ++expected;
-      int last = 1;
-      if (expected > 1) last = atomicAdd(&p.ws_counter[u], 1) == expected - 1;
-      misc[0] = last;
-      misc[1] = expected;
-    }
-    named_bar_sync(1, NW * 32);
-    if (misc[0]) {
-      __threadfence();
-      const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-      const int qh0 = sparse ? hu : hu * p.group;
-      for (int h = warp; h < GE; h += NW) {
-        float M = -INFINITY;
-        for (int cc = c_first; cc <= c_last; ++cc) {
-          if (cta_lo(cc, W, N) >= cta_lo(cc + 1, W, N)) continue;
-          if (lane < NW) M = fmaxf(M, __ldcg(&p.ws_m[((size_t)(cc + u) * NW + lane) * GE + h]));
+    if (prefix[u] == prefix[u + 1]) continue;
+    const bool alone = cta_of(prefix[u], W, N) == cta_of(prefix[u + 1] - 1, W, N);
+    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
+    const int qh0 = sparse ? hu : hu * p.group;
+    const float* wr = p.ws_wrec + (size_t)(c + u) * NW * RS;
+    float* cr = p.ws_crec + (size_t)(c + u) * RS;
+#pragma unroll
+    for (int k = 0; k < OPT; ++k) {
+      const int o = tid + k * NW * 32;
+      if (o < OUTS) {
+        const int h = o / D, ch = o - h * D;
+        float mw[NW], lw[NW], aw[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          mw[w] = wr[w * RS + h];
+          lw[w] = wr[w * RS + GE + h];
+          aw[w] = wr[w * RS + HDR + o];
         }
+        float M = mw[0];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float Ls = 0.f;
-        float o[PD];
-#pragma unroll
-        for (int e = 0; e < PD; ++e) o[e] = 0.f;
+        for (int w = 1; w < NW; ++w) M = fmaxf(M, mw[w]);
+        float L = 0.f, A = 0.f;
         if (M != -INFINITY) {
-          for (int cc = c_first; cc <= c_last; ++cc) {
-            if (cta_lo(cc, W, N) >= cta_lo(cc + 1, W, N)) continue;
-            for (int w = 0; w < NW; ++w) {
-              const size_t sl = ((size_t)(cc + u) * NW + w) * GE + h;
-              const float ms = __ldcg(&p.ws_m[sl]);
-              if (ms == -INFINITY) continue;
-              const float f = exp2f(ms - M);
-              Ls = fmaf(f, __ldcg(&p.ws_l[sl]), Ls);
-              const float* src = p.ws_acc + sl * D + lane * PD;
 #pragma unroll
-              for (int e = 0; e < PD; ++e) o[e] = fmaf(f, __ldcg(src + e), o[e]);
-            }
+          for (int w = 0; w < NW; ++w) {
+            const float f = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
+            L = fmaf(f, lw[w], L);
+            A = f > 0.f ? fmaf(f, aw[w], A) : A;
           }
         }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        const size_t ob = ((size_t)b * p.num_q_heads + qh0 + h) * D + lane * PD;
-#pragma unroll
-        for (int e = 0; e < PD; ++e) store_out_elem(p.out, p.out_dtype, ob + e, o[e] * inv);
+        if (alone) {
+          store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o,
+                         L > 0.f ? A / L : 0.f);
+        } else {
+          if (ch == 0) {
+            cr[h] = M;
+            cr[GE + h] = L;
+          }
+          cr[HDR + o] = A;
+        }
       }
-      if (tid == 0 && misc[1] > 1) p.ws_counter[u] = 0;
     }
-    named_bar_sync(1, NW * 32);
+  }
+}
+
+// Cross-block merge of the units that several blocks shared: one block per
+// unit, over the block records [m[G], l[G], acc[G][D]] of the covering blocks,
+//   M = max m_c,  out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
+// (the log2-domain partial states of the attention kernel).
+template <int D, int GE>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
+  constexpr int OUTS = GE * D, OPT = (OUTS + 127) / 128;
+  __shared__ float ML[2 * 8];
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int U = p.num_units;
+  const long long W = __ldcg(p.ws_prefix + U), N = p.num_ctas;
+  const int s0 = __ldcg(p.ws_prefix + u), s1 = __ldcg(p.ws_prefix + u + 1);
+  if (s0 == s1) return;
+  const int c_first = cta_of(s0, W, N), c_last = cta_of(s1 - 1, W, N);
+  if (c_first == c_last) return;                 // finished by the attention kernel
+  const bool sparse = p.sel_pages != nullptr;
+  const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
+  const int qh0 = sparse ? hu : hu * p.group;
+  // pass A: per head (warp h % 4), M and L over the covering blocks
+  for (int h = warp; h < GE; h += 4) {
+    float Mx = -INFINITY, Lx = 0.f;
+    for (int cc = c_first + lane; cc <= c_last; cc += 32) {
+      if (cta_lo(cc, W, N) >= cta_lo(cc + 1, W, N)) continue;
+      const float* rr = p.ws_crec + (size_t)(cc + u) * RS;
+      const float mc = __ldcg(rr + h), lc = __ldcg(rr + GE + h);
+      if (mc == -INFINITY) continue;
+      const float Mn = fmaxf(Mx, mc);
+      Lx = Lx * exp2f(Mx - Mn) + lc * exp2f(mc - Mn);
+      Mx = Mn;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, Mx, off);
+      const float Lo = __shfl_xor_sync(0xffffffffu, Lx, off);
+      const float Mn = fmaxf(Mx, Mo);
+      Lx = (Mn == -INFINITY) ? 0.f : Lx * exp2f(Mx - Mn) + Lo * exp2f(Mo - Mn);
+      Mx = Mn;
+    }
+    if (lane == 0) {
+      ML[h] = Mx;
+      ML[GE + h] = Lx;
+    }
+  }
+  __syncthreads();
+  // pass B: this thread's outputs, covering blocks in batches of 8
+#pragma unroll
+  for (int k = 0; k < OPT; ++k) {
+    const int o = tid + k * 128;
+    if (o >= OUTS) break;
+    const int h = o / D;
+    const float M = ML[h], L = ML[GE + h];
+    float A = 0.f;
+    if (M != -INFINITY) {
+      for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+        float mc[8], ac[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int cc = cc0 + i;
+          const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
+          const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
+          mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
+          ac[i] = __ldcg(rr + HDR + o);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float f = mc[i] == -INFINITY ? 0.f : exp2f(mc[i] - M);
+          A = f > 0.f ? fmaf(f, ac[i], A) : A;
+        }
+      }
+    }
+    store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o,
+                   L > 0.f ? A / L : 0.f);
   }
 }
 

@@ -64,6 +64,53 @@ __device__ __forceinline__ void flag_status(int32_t* st, int bit) {
   if (st) atomicOr(st, bit);
 }
 
+// ------------------------------------------------- packed fp32 pairs (f32x2)
+// Two fp32 values in one 64-bit register pair; the .f32x2 forms of fma / add /
+// sub / mul issue both lanes in one instruction (sm_100 and later).
+__device__ __forceinline__ uint64_t pack2f(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2f(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float hsum2(uint64_t r) {
+  float a, b;
+  unpack2f(r, a, b);
+  return a + b;
+}
+
+// Two 16-bit values of a 32-bit word as a packed fp32 pair (exact widening).
+template <int KV>
+__device__ __forceinline__ uint64_t widen2(uint32_t w) {
+  float a, b;
+  unpack2<KV>(w, a, b);
+  return pack2f(a, b);
+}
+
+// Bytes i, i+1 of a sign-flipped INT8 word as the pair (u_i, u_i+1), u = code + 128.
+__device__ __forceinline__ uint64_t u8pair(uint32_t wflip, int i) {
+  const float a = __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i));
+  const float b = __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i + 1));
+  return fsub2(pack2f(a, b), pack2f(8388608.0f, 8388608.0f));
+}
+
 // ------------------------------------------------------------ mbarrier / TMA
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -126,6 +173,32 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch. pdl_wait: wait until the preceding kernel on
+// the stream has completed and its memory is visible (a no-op when this kernel
+// was launched without the attribute); every kernel here calls it before its
+// first global access. pdl_launch_dependents: let the next kernel start
+// launching (its own pdl_wait still holds it until this grid completes).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization allowed.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
   __shared__ int hist[256];
   __shared__ int warp_tot[kTopkWarps];
   __shared__ int sel_digit, sel_remaining;
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int bh = blockIdx.x;
   const int b = bh / p.num_q_heads, h = bh - b * p.num_q_heads;
@@ -214,10 +216,9 @@ pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
       return PKV_ERR_CUDA;
   }
   const unsigned grid = (unsigned)(p.batch * p.num_q_heads);
-  if (p.head_dim == 128)
-    score_topk_kernel<128><<<grid, kTopkThreads, smem, st>>>(p);
-  else
-    score_topk_kernel<64><<<grid, kTopkThreads, smem, st>>>(p);
+  TopkParams pc = p;
+  void* args[] = {&pc};
+  if (launch_pdl(fn, dim3(grid), dim3(kTopkThreads), smem, st, args) != cudaSuccess) return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -57,6 +57,20 @@ def test_split_count_invariance():
         assert np.abs(o - outs[0]).max() <= 1e-5
 
 
+@pytest.mark.parametrize("stages,per_sm", [("3", "1"), ("4", "1"), ("5", "2"), ("12", "0"), ("32", "0")])
+def test_ring_depth_and_blocks_per_sm(monkeypatch, stages, per_sm):
+    # the stage count is rounded to a multiple of the consumer warps, so every
+    # ring slot has a single reader; results must not depend on these knobs
+    monkeypatch.setenv("PKV_ATTN_STAGES", stages)
+    monkeypatch.setenv("PKV_ATTN_CTAS_PER_SM", per_sm)
+    w = dataclasses.replace(synth.WORKLOADS["w2_llama7b_bf16"], batch=2, layers=1)
+    ld = load_workload(w, lens=np.array([700, 333], dtype=np.int32))
+    q, qf = queries_dev(w)
+    out = run_attention(ld, q).cpu().numpy()
+    assert max_abs_err(out, oracle_dense(ld, qf)) <= TOL["bf16"]
+    assert int(ld.status.item()) == 0
+
+
 @pytest.mark.parametrize("d,Hq,Hkv,ps,dt", [
     (64, 4, 4, 16, "f16"), (64, 8, 4, 32, "bf16"), (64, 16, 4, 16, "f16"), (64, 16, 2, 64, "f16"),
     (128, 8, 8, 16, "bf16"), (128, 8, 4, 48, "f16"), (128, 16, 4, 16, "bf16"), (128, 16, 2, 32, "f16"),
