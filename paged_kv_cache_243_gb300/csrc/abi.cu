@@ -128,17 +128,26 @@ const void* attn_combine(int D, int ge) {
   return nullptr;
 }
 
-const void* attn_kernel(int kind, int D, int ge) {
+const void* attn_kernel(int kind, int D, int ge, bool mma) {
   switch (kind) {
-    case KV_F16: return attn_kernel_f16(D, ge);
-    case KV_BF16: return attn_kernel_bf16(D, ge);
-    case KV_I8T: return attn_kernel_i8t(D, ge);
-    default: return attn_kernel_i8g(D, ge);
+    case KV_F16: return attn_kernel_f16(D, ge, mma);
+    case KV_BF16: return attn_kernel_bf16(D, ge, mma);
+    case KV_I8T: return attn_kernel_i8t(D, ge, mma);
+    default: return attn_kernel_i8g(D, ge, mma);
   }
+}
+
+// The tensor-core variant serves dense query-head groups (G >= 2) when q has
+// the dtype of the products' operands: fp16 for fp16 and INT8 caches (codes
+// enter as exact fp16 integers), bf16 for bf16 caches.
+bool use_mma(int kind, int ge, int q_dtype) {
+  if (ge < 2 || env_int("PKV_ATTN_MMA", 1) == 0) return false;
+  return kind == KV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16;
 }
 
 struct AttnPlan {
   const void* fn = nullptr;
+  bool mma = false;
   int ge = 1, units = 0, stages = 0, ctas = 0;
   size_t smem = 0;
   size_t off_wrec = 0, off_crec = 0, ws_bytes = 0;
@@ -146,8 +155,9 @@ struct AttnPlan {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// q_dtype < 0: size the workspace for whichever kernel variant a call may use.
 pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads, bool sparse,
-                          int32_t num_splits, AttnPlan& pl) {
+                          int32_t num_splits, int q_dtype, AttnPlan& pl) {
   pkv_status st = check_cache(c, false);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -157,7 +167,8 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   if (pl.ge != 1 && pl.ge != 2 && pl.ge != 4 && pl.ge != 8) return PKV_ERR_UNSUPPORTED;
   pl.units = batch * (sparse ? num_q_heads : c->num_kv_heads);
   const int kind = kv_kind(c);
-  pl.fn = attn_kernel(kind, c->head_dim, pl.ge);
+  pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, q_dtype);
+  pl.fn = attn_kernel(kind, c->head_dim, pl.ge, pl.mma);
   if (!pl.fn) return PKV_ERR_UNSUPPORTED;
   DeviceInfo di;
   st = device_info(di);
@@ -188,6 +199,11 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     int nb = 0;
     st = prepare_kernel(pl.fn, kAttnThreads, smem, nb);
     if (st != PKV_OK) return st;
+    if (q_dtype < 0 && pl.ge >= 2) {   // the tensor-core variant may fit more blocks
+      int nb2 = 0;
+      const void* f2 = attn_kernel(kind, c->head_dim, pl.ge, true);
+      if (f2 && prepare_kernel(f2, kAttnThreads, smem, nb2) == PKV_OK && nb2 > nb) nb = nb2;
+    }
     const int cap = env_int("PKV_ATTN_CTAS_PER_SM", 0);
     if (cap > 0 && cap < nb) nb = cap;
     pl.ctas = di.sms * nb;
@@ -227,7 +243,7 @@ int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
 size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                      int32_t sparse, int32_t num_splits) {
   AttnPlan pl;
-  if (plan_attention(cache, batch, num_q_heads, sparse != 0, num_splits, pl) != PKV_OK) return 0;
+  if (plan_attention(cache, batch, num_q_heads, sparse != 0, num_splits, -1, pl) != PKV_OK) return 0;
   return pl.ws_bytes;
 }
 
@@ -250,7 +266,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   if (sparse && (!sel_count || sel_stride <= 0)) return PKV_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !(sm_scale < 1e30f)) return PKV_ERR_INVALID_ARG;
   AttnPlan pl;
-  st = plan_attention(cache, batch, num_q_heads, sparse, num_splits, pl);
+  st = plan_attention(cache, batch, num_q_heads, sparse, num_splits, q_dtype, pl);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < pl.ws_bytes)
     return PKV_ERR_WORKSPACE;

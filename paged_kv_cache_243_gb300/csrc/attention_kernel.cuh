@@ -95,7 +95,8 @@ struct AttnGeom {
 
 template <int GE>
 struct AttnSmem {
-  static constexpr int PBUF = kChunk * GE + 8;     // floats per warp: p[16][GE], alpha[GE]
+  // floats per warp: p[16][GE] and alpha[GE] (CUDA-core path), or p[8][16] (tensor-core path)
+  static constexpr int PBUF = kChunk * 8 + 8;
 };
 
 // Partial-state record of one (block or warp, unit): m[GE], l[GE] (padded to a
@@ -108,7 +109,7 @@ __host__ __device__ inline size_t attn_smem_bytes(int stage_bytes, int stages, i
   size_t s = (size_t)stage_bytes * stages;
   s += (size_t)stages * 16;                       // hdr int4 per stage
   s += (size_t)stages * 16;                       // full + empty mbarriers
-  s += (size_t)kConsumerWarps * (kChunk * ge + 8) * 4;
+  s += (size_t)kConsumerWarps * (kChunk * 8 + 8) * 4;
   s += 32 * sizeof(ChunkInfo);
   s += kMiscInts * 4;                              // misc
   s += (size_t)(units + 1) * 4 + (size_t)batch * 4;
@@ -221,6 +222,65 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[GE], int j) {
   }
 }
 
+// ------------------------------------------------------------ tensor-core path
+// Warp-level mma.sync m16n8k16 with fp32 accumulation, for query-head groups
+// (G >= 2): q.K^T as [16 tokens] x [8 heads] and P.V as [16 channels] x [8 heads]
+// per 16-token chunk. INT8 codes enter as exact fp16 integers u = c + 128.
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Two bytes of a sign-flipped INT8 word (selected by sel: 0x4140 -> bytes 0, 1;
+// 0x4342 -> bytes 2, 3) as the fp16 pair (u0, u1): 0x64xx is the fp16 value
+// 1024 + xx, and subtracting 1024 is exact.
+__device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t wflip, uint32_t sel) {
+  const uint32_t h = __byte_perm(wflip, 0x64646464u, sel);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64006400u));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// fp32 pair -> (hi, lo) 16-bit pairs with hi + lo = x to ~2^-22 (fp16) / 2^-16 (bf16).
+template <bool BF16>
+__device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  } else {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+}
+
+__device__ __forceinline__ float h2lo_f(uint32_t w, bool bf) {
+  return bf ? __uint_as_float(w << 16) : __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float h2hi_f(uint32_t w, bool bf) {
+  return bf ? __uint_as_float(w & 0xffff0000u) : __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
 __device__ __forceinline__ int find_unit(const int* prefix, int num_units, int x) {
   int lo = 0, hi = num_units - 1;
   while (lo < hi) {
@@ -236,7 +296,7 @@ __device__ __forceinline__ int cta_of(long long x, long long W, long long N) {
   return (int)(((x + 1) * N - 1) / W);
 }
 
-template <int D, int GE, int KV>
+template <int D, int GE, int KV, bool MMA>
 __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const AttnParams p) {
   using Geo = AttnGeom<D, KV>;
   constexpr int QD = Geo::QD, PD = Geo::PD, KB = Geo::KB, SZB = Geo::SZB, STAGE = Geo::STAGE;
@@ -411,44 +471,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
       ci.nvalid = nv;
       ci.valid = 1;
     };
-    int n = 0;
+    // Copies are issued by up to S lanes at once (one per ring stage): a single
+    // issuing thread serialises the bulk-copy instructions and cannot keep the
+    // ring full. Lane l owns chunk nbase + l of the batch; it waits for its
+    // stage's previous use, which is always the phase just before its own.
+    int nbase = 0;
     bool abort = false;
     Raw cur;
     fetch(lo + lane, cur);
     for (int base = lo; base < hi && !abort; base += 32) {
-      ChunkInfo ci;
-      resolve(cur, ci);
-      info[lane] = ci;
-      __syncwarp();
+      ChunkInfo e;
+      resolve(cur, e);
       const int cnt = min(32, hi - base);
-      if (lane == 0) {
-        for (int i = 0; i < cnt; ++i, ++n) {
+      bool my_abort = false;
+      for (int k0 = 0; k0 < cnt; k0 += S) {
+        if (lane >= k0 && lane < min(cnt, k0 + S)) {
+          const int n = nbase + lane;
           const int s = n % S, use = n / S;
           if (use > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (use - 1) & 1)) {
             flag_status(p.dev_status, PKV_DEV_TIMEOUT);
-            abort = true;
-            break;
-          }
-          const ChunkInfo e = info[i];
-          hdr[s] = make_int4(e.u, e.nvalid, e.valid, 0);
-          const uint32_t fb = smem_u32(&full[s]);
-          if (e.valid) {
-            uint8_t* st = ring + (size_t)s * STAGE;
-            mbar_arrive_expect_tx(fb, 2 * KB + SZB);
-            bulk_g2s(smem_u32(st), e.k, KB, fb, pol);
-            bulk_g2s(smem_u32(st + KB), e.v, KB, fb, pol);
-            if constexpr (SZB > 0) bulk_g2s(smem_u32(st + 2 * KB), e.sz, SZB, fb, pol);
+            my_abort = true;
           } else {
-            mbar_arrive(fb);
+            hdr[s] = make_int4(e.u, e.nvalid, e.valid, 0);
+            const uint32_t fb = smem_u32(&full[s]);
+            if (e.valid) {
+              uint8_t* st = ring + (size_t)s * STAGE;
+              mbar_arrive_expect_tx(fb, 2 * KB + SZB);
+              bulk_g2s(smem_u32(st), e.k, KB, fb, pol);
+              bulk_g2s(smem_u32(st + KB), e.v, KB, fb, pol);
+              if constexpr (SZB > 0) bulk_g2s(smem_u32(st + 2 * KB), e.sz, SZB, fb, pol);
+            } else {
+              mbar_arrive(fb);
+            }
           }
         }
+        __syncwarp();
+        if (__any_sync(0xffffffffu, my_abort)) break;
       }
-      abort = __shfl_sync(0xffffffffu, abort ? 1 : 0, 0) != 0;
-      n = __shfl_sync(0xffffffffu, n, 0);
-      __syncwarp();
+      abort = __any_sync(0xffffffffu, my_abort);
+      nbase += cnt;
       // the next batch's table loads overlap the streaming of the stages just issued
       fetch(base + 32 + lane, cur);
     }
+    const int n = nbase;
     // Let every issued copy land before this warp (and so the block) can exit.
     if (lane == 0) {
       const int first = n > S ? n - S : 0;
@@ -462,6 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     return;
   }
 
+  if constexpr (!MMA) {
   // ================================================================== consumers
   const int r = lane >> 3, j = lane & 7;
   const int my_head = j / DUP;  // head this lane holds after the score reduction
@@ -663,6 +729,296 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     for (int v = next_unit; v <= ub; ++v) write_empty(v);
   }
 
+  } else {
+  // ============================================== consumers, tensor-core path
+  // Thread (g = lane / 4, t = lane % 4). Scores: C fragment of the [16 tok] x
+  // [8 head] product, i.e. tokens g and g + 8, heads 2t and 2t + 1. The channel
+  // axis is permuted so that thread t reads whole 16-byte blocks t, t + 4, ...
+  // of a row. Values: O^T [16 channels] x [8 heads] per m-tile; thread (g, t)
+  // owns channels [g D/8, (g + 1) D/8) of every output head 2t, 2t + 1, and
+  // tokens 4t .. 4t + 3 of the chunk enter the product's k slots.
+  constexpr bool BF = (KV == KV_BF16);
+  constexpr int ESZ = Geo::ESZ;
+  constexpr int E = 16 / ESZ;                 // channels per 16-byte block
+  constexpr int NB = (D / 4) / E;             // 16-byte blocks per thread per row
+  constexpr int KS = D / 16;                  // k-steps of q.K^T
+  constexpr int MT = D / 16;                  // m-tiles of P.V
+  constexpr int DPT = D / 8;                  // channels per thread group in P.V
+  const int g = lane >> 2, t = lane & 3;
+  float* pb = pbuf_all + warp * PBUF;
+  auto chan = [&](int i) { return (t + 4 * (i / E)) * E + (i % E); };
+
+  uint32_t qb[KS][2];
+  float qs[2];
+  float acc[MT][4];
+  float m2[2], l2[2], zs2[2];
+  int u_cur = -1, next_unit = ua;
+  constexpr int WRS = rec_floats(GE, D), WHDR = rec_hdr(GE);
+  auto rec_of = [&](int u) { return p.ws_wrec + ((size_t)(c + u) * NW + warp) * WRS; };
+  auto write_empty = [&](int u) {
+    if (lane < GE) {
+      float* rec = rec_of(u);
+      rec[lane] = -INFINITY;
+      rec[GE + lane] = 0.f;
+    }
+  };
+  auto flush = [&](int u) {
+    float* rec = rec_of(u);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int h = 2 * t + jj;
+      if (h < GE) {
+        float* dst = rec + WHDR + h * D + g * DPT;
+#pragma unroll
+        for (int mt = 0; mt < MT; mt += 2) {
+          *reinterpret_cast<float4*>(dst + 2 * mt) =
+              make_float4(acc[mt][jj] + zs2[jj], acc[mt][2 + jj] + zs2[jj], acc[mt + 1][jj] + zs2[jj],
+                          acc[mt + 1][2 + jj] + zs2[jj]);
+        }
+        if (g == 0) {
+          rec[h] = m2[jj];
+          rec[GE + h] = l2[jj];
+        }
+      }
+    }
+  };
+  auto start_unit = [&](int u) {
+    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
+    const int qh0 = hu * p.group;   // dense only on this path
+    float part = 0.f;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const uint16_t*>(p.q) + ((size_t)b * p.num_q_heads + qh0 + (g < GE ? g : 0)) * D);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int ch = chan(4 * kk);
+      uint32_t w0 = 0u, w1 = 0u;
+      if (g < GE) {
+        w0 = qrow[ch / 2];
+        w1 = qrow[ch / 2 + 1];
+      }
+      qb[kk][0] = w0;
+      qb[kk][1] = w1;
+      part += h2lo_f(w0, BF) + h2hi_f(w0, BF) + h2lo_f(w1, BF) + h2hi_f(w1, BF);
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);     // q sum of head g
+    qs[0] = __shfl_sync(0xffffffffu, part, (2 * t) * 4);
+    qs[1] = __shfl_sync(0xffffffffu, part, (2 * t + 1) * 4);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+    m2[0] = m2[1] = -INFINITY;
+    l2[0] = l2[1] = 0.f;
+    zs2[0] = zs2[1] = 0.f;
+  };
+
+  bool abort = false;
+  for (int n = warp; lo + n < hi; n += NW) {
+    const int s = n % S, use = n / S;
+    if (!mbar_wait_bounded(smem_u32(&full[s]), use & 1)) {
+      flag_status(p.dev_status, PKV_DEV_TIMEOUT);
+      abort = true;
+      break;
+    }
+    const int4 h4 = hdr[s];
+    const uint8_t* st = ring + (size_t)s * STAGE;
+    if (h4.x != u_cur) {
+      if (u_cur >= 0) {
+        flush(u_cur);
+        next_unit = u_cur + 1;
+      }
+      for (int v = next_unit; v < h4.x; ++v) write_empty(v);
+      u_cur = h4.x;
+      start_unit(u_cur);
+    }
+    if (h4.z) {
+      const int nvalid = h4.y;
+      const float* sz = reinterpret_cast<const float*>(st + 2 * KB);
+      // ---- q.K^T on the tensor cores
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint4 k0[NB], k1[NB];
+#pragma unroll
+        for (int m = 0; m < NB; ++m) {
+          k0[m] = *reinterpret_cast<const uint4*>(st + g * Geo::ROW + (t + 4 * m) * 16);
+          k1[m] = *reinterpret_cast<const uint4*>(st + (g + 8) * Geo::ROW + (t + 4 * m) * 16);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int m = (4 * kk) / E;
+          const int wi = ((4 * kk) % E) * ESZ / 4;
+          uint32_t a0, a1, a2, a3;
+          if constexpr (ESZ == 1) {
+            const uint32_t w0 = word_of(k0[m], wi) ^ 0x80808080u;
+            const uint32_t w1 = word_of(k1[m], wi) ^ 0x80808080u;
+            a0 = u8x2_to_h2(w0, 0x4140u);
+            a2 = u8x2_to_h2(w0, 0x4342u);
+            a1 = u8x2_to_h2(w1, 0x4140u);
+            a3 = u8x2_to_h2(w1, 0x4342u);
+          } else {
+            a0 = word_of(k0[m], wi);
+            a2 = word_of(k0[m], wi + 1);
+            a1 = word_of(k1[m], wi);
+            a3 = word_of(k1[m], wi + 1);
+          }
+          mma16816<BF>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+      }
+      // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
+      float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
+      if constexpr (KV == KV_I8T) {
+        const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
+        const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
+        sc[0] = fmaf(z0.x, sc[0], z0.y * qs[0]);
+        sc[1] = fmaf(z0.x, sc[1], z0.y * qs[1]);
+        sc[2] = fmaf(z1.x, sc[2], z1.y * qs[0]);
+        sc[3] = fmaf(z1.x, sc[3], z1.y * qs[1]);
+        vs0 = z0.z; vz0 = z0.w; vs1 = z1.z; vz1 = z1.w;
+      } else if constexpr (KV == KV_I8G) {
+        const float4 z = *reinterpret_cast<const float4*>(sz);
+        sc[0] = fmaf(z.x, sc[0], z.y * qs[0]);
+        sc[1] = fmaf(z.x, sc[1], z.y * qs[1]);
+        sc[2] = fmaf(z.x, sc[2], z.y * qs[0]);
+        sc[3] = fmaf(z.x, sc[3], z.y * qs[1]);
+        vs0 = vs1 = z.z; vz0 = vz1 = z.w;
+      }
+      const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[e] *= p.q_scale;
+      if (!ok0) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+      if (!ok1) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+      // ---- online softmax per head 2t + jj
+      float al[2], pw[4];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float cm = fmaxf(sc[jj], sc[2 + jj]);
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+        const float mn = fmaxf(m2[jj], cm);
+        al[jj] = exp2f(m2[jj] - mn);
+        const float p0 = exp2f(sc[jj] - mn), p1 = exp2f(sc[2 + jj] - mn);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l2[jj] = fmaf(l2[jj], al[jj], ps);
+        if constexpr (KV == KV_I8T) {
+          float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
+          pz += __shfl_xor_sync(0xffffffffu, pz, 4);
+          pz += __shfl_xor_sync(0xffffffffu, pz, 8);
+          pz += __shfl_xor_sync(0xffffffffu, pz, 16);
+          zs2[jj] = fmaf(zs2[jj], al[jj], pz);
+          pw[jj] = ok0 ? p0 * vs0 : 0.f;
+          pw[2 + jj] = ok1 ? p1 * vs1 : 0.f;
+        } else if constexpr (KV == KV_I8G) {
+          zs2[jj] = fmaf(zs2[jj], al[jj], vz0 * ps);
+          pw[jj] = p0 * vs0;
+          pw[2 + jj] = p1 * vs1;
+        } else {
+          pw[jj] = p0;
+          pw[2 + jj] = p1;
+        }
+        m2[jj] = mn;
+      }
+      // P' to [head][token] in shared memory, then as the B operand of P.V
+      pb[(2 * t) * kChunk + g] = pw[0];
+      pb[(2 * t + 1) * kChunk + g] = pw[1];
+      pb[(2 * t) * kChunk + g + 8] = pw[2];
+      pb[(2 * t + 1) * kChunk + g + 8] = pw[3];
+      __syncwarp();
+      float4 pv4 = *reinterpret_cast<const float4*>(pb + g * kChunk + 4 * t);   // head g, tokens 4t..4t+3
+      __syncwarp();
+      if (g >= GE) pv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      uint32_t bh0, bl0, bh1, bl1;
+      split_hi_lo<BF>(pv4.x, pv4.y, bh0, bl0);
+      split_hi_lo<BF>(pv4.z, pv4.w, bh1, bl1);
+      // ---- P.V on the tensor cores
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][0] *= al[0];
+        acc[mt][2] *= al[0];
+        acc[mt][1] *= al[1];
+        acc[mt][3] *= al[1];
+      }
+      const uint8_t* vrow = st + KB;
+      if constexpr (ESZ == 1) {
+        // int8: dims [g DPT, (g+1) DPT) of tokens 4t .. 4t+3 (DPT bytes per row)
+        uint32_t rw[4][DPT / 4];
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) {
+          const uint8_t* src = vrow + (4 * t + jr) * Geo::ROW + g * DPT;
+          if constexpr (DPT == 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src);
+            rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
+            rw[jr][2] = v.z ^ 0x80808080u; rw[jr][3] = v.w ^ 0x80808080u;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
+          }
+        }
+        if (nvalid < kChunk) {   // masked tokens: their codes may be stale; make them 0
+#pragma unroll
+          for (int jr = 0; jr < 4; ++jr)
+            if (4 * t + jr >= nvalid)
+#pragma unroll
+              for (int i = 0; i < DPT / 4; ++i) rw[jr][i] = 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int wi = mt / 2;
+          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+          const uint32_t t01 = __byte_perm(rw[0][wi], rw[1][wi], sel);
+          const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
+          const uint32_t a0 = u8x2_to_h2(t01, 0x4140u), a1 = u8x2_to_h2(t01, 0x4342u);
+          const uint32_t a2 = u8x2_to_h2(t23, 0x4140u), a3 = u8x2_to_h2(t23, 0x4342u);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+        }
+      } else {
+        // fp16 / bf16: dims [g DPT, (g+1) DPT) of tokens 4t .. 4t+3 (2 DPT bytes per row)
+        uint32_t rw[4][DPT / 2];
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) {
+          const uint8_t* src = vrow + (4 * t + jr) * Geo::ROW + g * DPT * 2;
+#pragma unroll
+          for (int q4 = 0; q4 < DPT / 8; ++q4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
+            rw[jr][4 * q4 + 0] = v.x; rw[jr][4 * q4 + 1] = v.y;
+            rw[jr][4 * q4 + 2] = v.z; rw[jr][4 * q4 + 3] = v.w;
+          }
+        }
+        if (nvalid < kChunk) {   // masked tokens may hold NaN; weight 0 would not clear it
+#pragma unroll
+          for (int jr = 0; jr < 4; ++jr)
+            if (4 * t + jr >= nvalid)
+#pragma unroll
+              for (int i = 0; i < DPT / 2; ++i) rw[jr][i] = 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t a0 = __byte_perm(rw[0][mt], rw[1][mt], 0x5410u);
+          const uint32_t a1 = __byte_perm(rw[0][mt], rw[1][mt], 0x7632u);
+          const uint32_t a2 = __byte_perm(rw[2][mt], rw[3][mt], 0x5410u);
+          const uint32_t a3 = __byte_perm(rw[2][mt], rw[3][mt], 0x7632u);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+  }
+  if (!abort) {
+    if (u_cur >= 0) {
+      flush(u_cur);
+      next_unit = u_cur + 1;
+    }
+    for (int v = next_unit; v <= ub; ++v) write_empty(v);
+  }
+  }
+
   // ---- in-block merge. Every unit this block touched gets one block record
   // from its 4 warp records; a unit that lies entirely inside this block is
   // final here and goes to the output. Units shared with other blocks are
@@ -678,7 +1034,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     const int qh0 = sparse ? hu : hu * p.group;
     const float* wr = p.ws_wrec + (size_t)(c + u) * NW * RS;
     float* cr = p.ws_crec + (size_t)(c + u) * RS;
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < OPT; ++k) {
       const int o = tid + k * NW * 32;
       if (o < OUTS) {
@@ -727,8 +1083,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
   pdl_launch_dependents();
   constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
   constexpr int OUTS = GE * D, OPT = (OUTS + 127) / 128;
-  __shared__ float ML[2 * 8];
-  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.x, tid = threadIdx.x;
   const int U = p.num_units;
   const long long W = __ldcg(p.ws_prefix + U), N = p.num_ctas;
   const int s0 = __ldcg(p.ws_prefix + u), s1 = __ldcg(p.ws_prefix + u + 1);
@@ -738,56 +1093,33 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
   const bool sparse = p.sel_pages != nullptr;
   const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
   const int qh0 = sparse ? hu : hu * p.group;
-  // pass A: per head (warp h % 4), M and L over the covering blocks
-  for (int h = warp; h < GE; h += 4) {
-    float Mx = -INFINITY, Lx = 0.f;
-    for (int cc = c_first + lane; cc <= c_last; cc += 32) {
-      if (cta_lo(cc, W, N) >= cta_lo(cc + 1, W, N)) continue;
-      const float* rr = p.ws_crec + (size_t)(cc + u) * RS;
-      const float mc = __ldcg(rr + h), lc = __ldcg(rr + GE + h);
-      if (mc == -INFINITY) continue;
-      const float Mn = fmaxf(Mx, mc);
-      Lx = Lx * exp2f(Mx - Mn) + lc * exp2f(mc - Mn);
-      Mx = Mn;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float Mo = __shfl_xor_sync(0xffffffffu, Mx, off);
-      const float Lo = __shfl_xor_sync(0xffffffffu, Lx, off);
-      const float Mn = fmaxf(Mx, Mo);
-      Lx = (Mn == -INFINITY) ? 0.f : Lx * exp2f(Mx - Mn) + Lo * exp2f(Mo - Mn);
-      Mx = Mn;
-    }
-    if (lane == 0) {
-      ML[h] = Mx;
-      ML[GE + h] = Lx;
-    }
-  }
-  __syncthreads();
-  // pass B: this thread's outputs, covering blocks in batches of 8
+  // One pass: each thread folds the covering blocks' (m, l, acc) of its own
+  // output online; the loads of 8 records are issued together.
 #pragma unroll
   for (int k = 0; k < OPT; ++k) {
     const int o = tid + k * 128;
     if (o >= OUTS) break;
     const int h = o / D;
-    const float M = ML[h], L = ML[GE + h];
-    float A = 0.f;
-    if (M != -INFINITY) {
-      for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
-        float mc[8], ac[8];
+    float M = -INFINITY, L = 0.f, A = 0.f;
+    for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+      float mc[8], lc[8], ac[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int cc = cc0 + i;
-          const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
-          const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
-          mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
-          ac[i] = __ldcg(rr + HDR + o);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const int cc = cc0 + i;
+        const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
+        const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
+        mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
+        lc[i] = __ldcg(rr + GE + h);
+        ac[i] = __ldcg(rr + HDR + o);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float f = mc[i] == -INFINITY ? 0.f : exp2f(mc[i] - M);
-          A = f > 0.f ? fmaf(f, ac[i], A) : A;
-        }
+      for (int i = 0; i < 8; ++i) {
+        if (mc[i] == -INFINITY) continue;
+        const float Mn = fmaxf(M, mc[i]);
+        const float sc = exp2f(M - Mn), f = exp2f(mc[i] - Mn);
+        L = fmaf(L, sc, f * lc[i]);
+        A = fmaf(A, sc, f * ac[i]);
+        M = Mn;
       }
     }
     store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o,

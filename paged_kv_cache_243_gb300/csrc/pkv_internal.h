@@ -39,10 +39,11 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st);
 pkv_status launch_topk(const TopkParams& p, cudaStream_t st);
 
 // Attention kernels, one getter per KV kind (each in its own translation unit).
-const void* attn_kernel_f16(int D, int GE);
-const void* attn_kernel_bf16(int D, int GE);
-const void* attn_kernel_i8t(int D, int GE);
-const void* attn_kernel_i8g(int D, int GE);
+// mma: the tensor-core variant (query-head groups of 2, 4 or 8).
+const void* attn_kernel_f16(int D, int GE, bool mma);
+const void* attn_kernel_bf16(int D, int GE, bool mma);
+const void* attn_kernel_i8t(int D, int GE, bool mma);
+const void* attn_kernel_i8g(int D, int GE, bool mma);
 
 // Bytes of one shared-memory stage (a 16-token chunk of K and V plus its INT8
 // scales), by KV kind and head_dim.

@@ -71,11 +71,14 @@ def test_ring_depth_and_blocks_per_sm(monkeypatch, stages, per_sm):
     assert int(ld.status.item()) == 0
 
 
+@pytest.mark.parametrize("mma", ["1", "0"])
 @pytest.mark.parametrize("d,Hq,Hkv,ps,dt", [
     (64, 4, 4, 16, "f16"), (64, 8, 4, 32, "bf16"), (64, 16, 4, 16, "f16"), (64, 16, 2, 64, "f16"),
     (128, 8, 8, 16, "bf16"), (128, 8, 4, 48, "f16"), (128, 16, 4, 16, "bf16"), (128, 16, 2, 32, "f16"),
+    (128, 32, 4, 16, "bf16"),
 ])
-def test_shapes_ragged_lengths(d, Hq, Hkv, ps, dt):
+def test_shapes_ragged_lengths(monkeypatch, d, Hq, Hkv, ps, dt, mma):
+    monkeypatch.setenv("PKV_ATTN_MMA", mma)
     w = synth.Workload(name="t", seed=77 + d + Hq + ps, batch=5, layers=1, num_q_heads=Hq,
                        num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt, quant="none",
                        seq_len=None, seq_len_range=(1, 300))

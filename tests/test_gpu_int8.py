@@ -54,8 +54,11 @@ def small_int8(quant, seed, d=128, Hq=8, Hkv=2, ps=None, batch=4, outliers=4):
                           seq_len_range=(1, 400), outlier_channels=outliers, outlier_scale=15.0)
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (64, 16, 2), (128, 8, 8)])
-def test_per_token_small_all_outputs(d, Hq, Hkv):
+@pytest.mark.parametrize("mma", ["1", "0"])
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (64, 16, 2), (128, 8, 8), (128, 16, 8)])
+def test_per_token_small_all_outputs(monkeypatch, d, Hq, Hkv, mma):
+    # mma = 1: query-head groups use the tensor-core kernel; 0: the CUDA-core one
+    monkeypatch.setenv("PKV_ATTN_MMA", mma)
     w = small_int8("per_token", 300 + d + Hq, d, Hq, Hkv)
     ld = load_workload(w, lens=np.array([1, 400, 17, 250], dtype=np.int32))
     check_per_token_codes(ld)
@@ -67,8 +70,10 @@ def test_per_token_small_all_outputs(d, Hq, Hkv):
     assert int(ld.status.item()) == 0
 
 
-@pytest.mark.parametrize("d,Hq,Hkv,ps", [(128, 8, 2, 128), (64, 8, 4, 64), (128, 32, 8, 256)])
-def test_per_group_small_all_outputs(d, Hq, Hkv, ps):
+@pytest.mark.parametrize("mma", ["1", "0"])
+@pytest.mark.parametrize("d,Hq,Hkv,ps", [(128, 8, 2, 128), (64, 8, 4, 64), (128, 32, 8, 256), (64, 16, 2, 64)])
+def test_per_group_small_all_outputs(monkeypatch, d, Hq, Hkv, ps, mma):
+    monkeypatch.setenv("PKV_ATTN_MMA", mma)
     w = small_int8("per_group64", 400 + d + ps, d, Hq, Hkv, ps)
     ld = load_workload(w, lens=np.array([1, 400, 64, 129], dtype=np.int32))
     check_per_group_codes(ld)
