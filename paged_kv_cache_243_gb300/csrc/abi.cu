@@ -55,8 +55,11 @@ pkv_status device_info(DeviceInfo& di) {
   return PKV_OK;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per (device, kernel, size)
-// and return how many of its blocks fit on one SM.
+// Make sure a kernel may launch with `smem` bytes of dynamic shared memory and
+// return how many of its blocks fit on one SM at that size. The shared-memory
+// limit is one value per (device, kernel); it is only ever raised, so a launch
+// prepared earlier with a larger size stays valid after a smaller request.
+// Occupancy is kept per (device, kernel, size).
 pkv_status prepare_kernel(const void* fn, int threads, size_t smem, int& blocks_per_sm) {
   static std::mutex mu;
   struct Key {
@@ -70,23 +73,29 @@ pkv_status prepare_kernel(const void* fn, int threads, size_t smem, int& blocks_
       return std::hash<const void*>()(k.fn) ^ (k.smem * 1315423911u) ^ (size_t)k.dev;
     }
   };
-  static std::unordered_map<Key, int, Hash> cache;
+  static std::unordered_map<Key, int, Hash> occupancy;   // (dev, fn, smem) -> blocks per SM
+  static std::unordered_map<Key, size_t, Hash> limit;    // (dev, fn, 0) -> smem limit set
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  Key key{dev, fn, smem};
   std::lock_guard<std::mutex> lk(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) {
+  const Key fkey{dev, fn, 0};
+  auto lim = limit.find(fkey);
+  if (lim == limit.end() || lim->second < smem) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    limit[fkey] = smem;
+  }
+  const Key key{dev, fn, smem};
+  auto it = occupancy.find(key);
+  if (it != occupancy.end()) {
     blocks_per_sm = it->second;
     return PKV_OK;
   }
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return PKV_ERR_CUDA;
   int nb = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (nb < 1) return PKV_ERR_UNSUPPORTED;
-  cache[key] = nb;
+  occupancy[key] = nb;
   blocks_per_sm = nb;
   return PKV_OK;
 }

@@ -212,7 +212,9 @@ pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
   const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&score_topk_kernel<128>)
                                      : reinterpret_cast<const void*>(&score_topk_kernel<64>);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    // always the one maximum (16384 pages), never a per-call size, so a
+    // concurrent or later launch with more pages is never left below its need
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
   const unsigned grid = (unsigned)(p.batch * p.num_q_heads);

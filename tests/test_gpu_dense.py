@@ -57,6 +57,23 @@ def test_split_count_invariance():
         assert np.abs(o - outs[0]).max() <= 1e-5
 
 
+def test_alternating_batch_sizes_on_one_kernel():
+    # the kernel's shared-memory size grows with the batch (per-sequence unit
+    # table); a smaller call in between must not leave a larger one unlaunchable
+    w = dataclasses.replace(synth.WORKLOADS["w2_llama7b_bf16"], batch=8, layers=1)
+    ld = load_workload(w, lens=np.array([300, 17, 64, 129, 1, 250, 33, 90], dtype=np.int32))
+    q, qf = queries_dev(w)
+    ref = oracle_dense(ld, qf)
+    for rows in (8, 1, 8, 3, 8):
+        out = ld.cache.attention(q[:rows].contiguous(), ld.bt_dev[:rows].contiguous(),
+                                 ld.lens_dev[:rows].contiguous(), sm_scale=w.sm_scale,
+                                 dev_status=ld.status)
+        torch.cuda.synchronize()
+        sub = {k: v for k, v in ref.items() if k[0] < rows}
+        assert max_abs_err(out.cpu().numpy(), sub) <= TOL["bf16"], rows
+    assert int(ld.status.item()) == 0
+
+
 @pytest.mark.parametrize("stages,per_sm", [("3", "1"), ("4", "1"), ("5", "2"), ("12", "0"), ("32", "0")])
 def test_ring_depth_and_blocks_per_sm(monkeypatch, stages, per_sm):
     # the stage count is rounded to a multiple of the consumer warps, so every
