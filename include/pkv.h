@@ -214,6 +214,34 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       int32_t* dev_status, void* stream);
 
 /*
+ * paged_decode_attention_noalloc — the same computation and arguments as
+ * pkv_paged_decode_attention, minus the workspace, for callers that cannot
+ * allocate device memory: a program that reserves all device memory at start-up
+ * and allows no later cudaMalloc (which can stall every stream on the device),
+ * or a plugin that only receives its input and output buffers. The pages have
+ * no counterpart; this is a packaging choice of the library.
+ *   Scratch: a fixed 8 MiB array inside the library's device image, present on
+ *   every GPU that loads the library until the process exits. A call whose
+ *   workspace (pkv_attention_workspace_bytes) exceeds 8 MiB returns
+ *   PKV_ERR_WORKSPACE and launches nothing.
+ *   Set-up: the first call with a given device current looks up the array's
+ *   device address (cudaGetSymbolAddress); make that first call before any
+ *   stream capture on that device.
+ *   Sharing: every call uses the same array, and its contents are whatever the
+ *   last call left (nothing needs to start at zero). Calls that may run at the
+ *   same time on the GPU (other streams, other host threads) race: issue them
+ *   one after another on one stream.
+ *   Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t batch,
+                                              int32_t num_q_heads, const void* q, pkv_dtype q_dtype,
+                                              float sm_scale, const int32_t* block_table,
+                                              int32_t max_pages, const int32_t* seq_lens,
+                                              const int32_t* sel_pages, const int32_t* sel_count,
+                                              int32_t sel_stride, void* out, pkv_dtype out_dtype,
+                                              int32_t num_splits, int32_t* dev_status, void* stream);
+
+/*
  * Host page allocator [HBM-layout page, section 三 allocate_blocks /
  * free_sequence]: a free list of physical page ids; a sequence needs
  * ceil(tokens / page_size) pages; an allocation that cannot be met fails

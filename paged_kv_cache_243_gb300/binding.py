@@ -23,6 +23,7 @@ DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_BAD_CONFIG = 
 EXPORTED = [
     "pkv_status_string", "pkv_abi_version", "pkv_kv_append", "pkv_page_score_topk",
     "pkv_attention_workspace_bytes", "pkv_paged_decode_attention",
+    "pkv_paged_decode_attention_noalloc",
     "pkv_alloc_create", "pkv_alloc_destroy", "pkv_alloc_reserve", "pkv_alloc_free",
     "pkv_alloc_num_free", "pkv_alloc_seq_pages", "pkv_alloc_check",
 ]
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp, vp,
                                                i32, vp, c_int, i32, vp, c_size_t, vp, vp]),
+        "pkv_paged_decode_attention_noalloc": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp,
+                                                       vp, i32, vp, c_int, i32, vp, vp]),
         "pkv_alloc_create": (c_int, [i32, POINTER(c_void_p)]),
         "pkv_alloc_destroy": (None, [vp]),
         "pkv_alloc_reserve": (c_int, [vp, i64, i32, i32, vp, i32]),
@@ -136,6 +139,19 @@ def paged_decode_attention(cache: PkvCache, batch: int, num_q_heads: int, q: int
                                             out_dtype, num_splits, workspace, workspace_bytes,
                                             dev_status or None, stream or None),
            "paged_decode_attention")
+
+
+def paged_decode_attention_noalloc(cache: PkvCache, batch: int, num_q_heads: int, q: int,
+                                   q_dtype: int, sm_scale: float, block_table: int, max_pages: int,
+                                   seq_lens: int, sel_pages: int, sel_count: int, sel_stride: int,
+                                   out: int, out_dtype: int, num_splits: int, dev_status: int,
+                                   stream: int) -> None:
+    """paged_decode_attention with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check(lib().pkv_paged_decode_attention_noalloc(
+        ctypes.byref(cache), batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages,
+        seq_lens, sel_pages or None, sel_count or None, sel_stride, out, out_dtype, num_splits,
+        dev_status or None, stream or None), "paged_decode_attention_noalloc")
 
 
 def alloc_create(num_pages: int) -> int:
