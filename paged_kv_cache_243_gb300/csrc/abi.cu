@@ -318,7 +318,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);
   if (e == cudaSuccess && pl.ctas > 1) {
     const void* comb = attn_combine(cache->head_dim, pl.ge);
-    e = launch_pdl(comb, dim3(pl.units), dim3(128), 0, cs, args);
+    e = launch_pdl(comb, dim3(pl.units, (pl.ge * cache->head_dim + 127) / 128), dim3(128), 0, cs, args);
   }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -296,8 +296,10 @@ __device__ __forceinline__ int cta_of(long long x, long long W, long long N) {
   return (int)(((x + 1) * N - 1) / W);
 }
 
+// The tensor-core variant is held to 3 resident blocks per SM (<= 136 registers)
+// so that 12 consumer warps hide its per-chunk latency.
 template <int D, int GE, int KV, bool MMA>
-__global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_kernel(const AttnParams p) {
   using Geo = AttnGeom<D, KV>;
   constexpr int QD = Geo::QD, PD = Geo::PD, KB = Geo::KB, SZB = Geo::SZB, STAGE = Geo::STAGE;
   constexpr int PBUF = AttnSmem<GE>::PBUF;
@@ -1034,7 +1036,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_attention_kernel(const 
     const int qh0 = sparse ? hu : hu * p.group;
     const float* wr = p.ws_wrec + (size_t)(c + u) * NW * RS;
     float* cr = p.ws_crec + (size_t)(c + u) * RS;
-#pragma unroll 1
+#pragma unroll
     for (int k = 0; k < OPT; ++k) {
       const int o = tid + k * NW * 32;
       if (o < OUTS) {
@@ -1082,7 +1084,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
   pdl_wait();
   pdl_launch_dependents();
   constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
-  constexpr int OUTS = GE * D, OPT = (OUTS + 127) / 128;
+  constexpr int OUTS = GE * D;
   const int u = blockIdx.x, tid = threadIdx.x;
   const int U = p.num_units;
   const long long W = __ldcg(p.ws_prefix + U), N = p.num_ctas;
@@ -1094,37 +1096,34 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
   const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
   const int qh0 = sparse ? hu : hu * p.group;
   // One pass: each thread folds the covering blocks' (m, l, acc) of its own
-  // output online; the loads of 8 records are issued together.
+  // output online; the loads of 16 records are issued together. Block
+  // (unit, y) takes outputs [128 y, 128 y + 128) of the unit.
+  const int o = blockIdx.y * 128 + tid;
+  if (o >= OUTS) return;
+  const int h = o / D;
+  float M = -INFINITY, L = 0.f, A = 0.f;
+  for (int cc0 = c_first; cc0 <= c_last; cc0 += 16) {
+    float mc[16], lc[16], ac[16];
 #pragma unroll
-  for (int k = 0; k < OPT; ++k) {
-    const int o = tid + k * 128;
-    if (o >= OUTS) break;
-    const int h = o / D;
-    float M = -INFINITY, L = 0.f, A = 0.f;
-    for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
-      float mc[8], lc[8], ac[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int cc = cc0 + i;
-        const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
-        const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
-        mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
-        lc[i] = __ldcg(rr + GE + h);
-        ac[i] = __ldcg(rr + HDR + o);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (mc[i] == -INFINITY) continue;
-        const float Mn = fmaxf(M, mc[i]);
-        const float sc = exp2f(M - Mn), f = exp2f(mc[i] - Mn);
-        L = fmaf(L, sc, f * lc[i]);
-        A = fmaf(A, sc, f * ac[i]);
-        M = Mn;
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int cc = cc0 + i;
+      const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
+      const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
+      mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
+      lc[i] = __ldcg(rr + GE + h);
+      ac[i] = __ldcg(rr + HDR + o);
     }
-    store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o,
-                   L > 0.f ? A / L : 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (mc[i] == -INFINITY) continue;
+      const float Mn = fmaxf(M, mc[i]);
+      const float sc = exp2f(M - Mn), f = exp2f(mc[i] - Mn);
+      L = fmaf(L, sc, f * lc[i]);
+      A = fmaf(A, sc, f * ac[i]);
+      M = Mn;
+    }
   }
+  store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o, L > 0.f ? A / L : 0.f);
 }
 
 }  // namespace pkv

@@ -76,15 +76,21 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
     qv[e] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h) * D + lane * PL + e);
     qpos[e] = qv[e] >= 0.f;
   }
-  constexpr int UNROLL = 4;
+  // The row's block-table entries are staged (coalesced) in the key array first;
+  // each page's entry is read before its score overwrites that slot.
+  for (int pg = tid; pg < P; pg += kTopkThreads)
+    keys[pg] = (uint32_t)p.block_table[(size_t)b * p.max_pages + pg];
+  __syncthreads();
+  constexpr int UNROLL = 16;   // pages in flight per warp (box loads issued before use)
   for (int base = warp * UNROLL; base < P; base += kTopkWarps * UNROLL) {
     float part[UNROLL];
     int phys[UNROLL];
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       const int pg = base + k;
-      phys[k] = pg < P ? p.block_table[(size_t)b * p.max_pages + pg] : -1;
+      phys[k] = pg < P ? (int)keys[pg] : -1;
     }
+    __syncwarp();
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       const int pg = base + k;
@@ -158,14 +164,36 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
       if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-      int cum = 0, dgt = 255;
-      for (; dgt > 0; --dgt) {
-        if (cum + hist[dgt] >= remaining) break;
-        cum += hist[dgt];
+    if (warp == 0) {
+      // lane l holds digits 255 - 8l .. 248 - 8l (descending); a scan over the
+      // lanes finds the digit where the running count first reaches `remaining`
+      int c8[8], lsum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c8[i] = hist[255 - 8 * lane - i];
+        lsum += c8[i];
       }
-      sel_digit = dgt;
-      sel_remaining = remaining - cum;
+      int incl = lsum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int excl = incl - lsum;
+      const unsigned mine = __ballot_sync(0xffffffffu, excl < remaining && remaining <= incl);
+      if (lane == __ffs(mine) - 1) {
+        int cum = excl, dgt = 248 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + c8[i] >= remaining) {
+            dgt = 255 - 8 * lane - i;
+            break;
+          }
+          cum += c8[i];
+        }
+        sel_digit = dgt;
+        sel_remaining = remaining - cum;
+      }
     }
     __syncthreads();
     prefix |= (uint32_t)sel_digit << shift;
