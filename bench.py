@@ -42,6 +42,8 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "w2_llama7b_bf16"
+# attention launches overlap the kernel before them (see Replica._layer)
+EARLY_START = True
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -298,9 +300,14 @@ class Replica:
             c.score_topk(self.qs[i], self.bts[i], self.len_list[s], self.top_k, dev_status=self.status,
                          sel=self.sel[i], count=self.cnt[i], stream=stream)
         if attention:
+            # early start: after this step's append, the kernel before the
+            # attention writes only the new token's rows (fresh_rows = 1); after
+            # another layer's attention it writes nothing the call reads (0).
+            # Scoring writes the page lists, so sparse calls wait (-1).
+            fresh = -1 if (sparse or not EARLY_START) else (1 if append else 0)
             c.attention(self.qs[i], self.bts[i], self.len_list[s], sm_scale=self.w.sm_scale,
                         sel=self.sel[i] if sparse else None, sel_count=self.cnt[i] if sparse else None,
-                        out=self.outs[i], dev_status=self.status, stream=stream)
+                        out=self.outs[i], dev_status=self.status, stream=stream, fresh_rows=fresh)
 
     def capture(self, append=True, attention=True, sparse=False):
         """CUDA graph of one replay: every decode step of the workload over all layers."""
@@ -629,6 +636,7 @@ def run_ours(args) -> None:
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peaks["source"],
                          "kernel": "paged_attention_kernel (one launch per layer)",
+                         "early_start": EARLY_START,
                          "algorithmic_bytes_per_launch": int(att_bytes),
                          "avg_launch_us": round(ms_att * 1e3, 3)},
             "clocks": clocks,
@@ -688,7 +696,11 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-early-start", action="store_true",
+                    help="attention waits for the preceding kernel before any read (fresh_rows = -1)")
     args = ap.parse_args(argv)
+    global EARLY_START
+    EARLY_START = not args.no_early_start
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef enum {
   PKV_OK = 0,
@@ -190,15 +190,34 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *   num_splits  : number of cooperating thread blocks that share the work
  *                 (split-K over the whole batch's pages, each block taking an
  *                 equal share); 0 = one full wave of the device.
+ *   fresh_rows  : -1, or a promise that lets the call start before the
+ *                 kernel launched just before it on `stream` has finished:
+ *                 that kernel writes nothing this call reads except the K/V
+ *                 rows (and scales) that a pkv_kv_append of the last
+ *                 fresh_rows tokens of each sequence writes, i.e. positions
+ *                 >= seq_lens[b] - fresh_rows (per-group INT8: from the
+ *                 start of the 64-token group holding that position, which
+ *                 the append re-quantises). Typical use: the call right after
+ *                 this step's pkv_kv_append (fresh_rows = its t_new), or
+ *                 right after another attention call (fresh_rows = 0). The
+ *                 call then reads q, the tables, the lengths and all older
+ *                 rows at once, and waits for that kernel before copying a
+ *                 chunk with fresh rows and before its first write to out or
+ *                 the workspace (so both may be shared with that kernel);
+ *                 only dev_status flags can be raised before the wait. A
+ *                 false promise gives wrong results, not a fault. -1 (no
+ *                 promise) waits before the first global access.
  *   workspace   : >= pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                 aligned, any contents (it holds the per-block partial states
  *                 of one call; no initialisation is needed).
  * Two launches: the attention kernel, and (when num_splits != 1) a combine
  * kernel that merges, for each (sequence, kv head) shared by several blocks,
  * the blocks' partial (running max, sum, accumulator) states. Both are
- * launched with programmatic stream serialization, and every kernel of this
+ * launched with programmatic stream serialization. Every kernel of this
  * library waits for the preceding kernel on the stream before its first
- * global memory access, so stream order is kept.
+ * global memory access (the attention kernel with fresh_rows >= 0: before
+ * its first access to anything outside the promise above), and lets its own
+ * dependents start only after that wait, so stream order is kept.
  * A sequence with no tokens (or no selected pages) yields zeros.
  * Device errors: PKV_DEV_BAD_PAGE, PKV_DEV_BAD_SELECTED (chunk skipped),
  * PKV_DEV_TIMEOUT.
@@ -210,12 +229,12 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       const int32_t* sel_pages, const int32_t* sel_count,
                                       int32_t sel_stride,
                                       void* out, pkv_dtype out_dtype, int32_t num_splits,
-                                      void* workspace, size_t workspace_bytes,
+                                      int32_t fresh_rows, void* workspace, size_t workspace_bytes,
                                       int32_t* dev_status, void* stream);
 
 /*
  * paged_decode_attention_noalloc — the same computation and arguments as
- * pkv_paged_decode_attention, minus the workspace, for callers that cannot
+ * pkv_paged_decode_attention with fresh_rows = -1, minus the workspace, for callers that cannot
  * allocate device memory: a program that reserves all device memory at start-up
  * and allows no later cudaMalloc (which can stall every stream on the device),
  * or a plugin that only receives its input and output buffers. The pages have

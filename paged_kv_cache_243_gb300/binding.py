@@ -70,7 +70,7 @@ def lib() -> ctypes.CDLL:
         "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, vp, vp, vp, vp, vp]),
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp, vp,
-                                               i32, vp, c_int, i32, vp, c_size_t, vp, vp]),
+                                               i32, vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
         "pkv_paged_decode_attention_noalloc": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp,
                                                        vp, i32, vp, c_int, i32, vp, vp]),
         "pkv_alloc_create": (c_int, [i32, POINTER(c_void_p)]),
@@ -132,12 +132,14 @@ def paged_decode_attention(cache: PkvCache, batch: int, num_q_heads: int, q: int
                            sm_scale: float, block_table: int, max_pages: int, seq_lens: int,
                            sel_pages: int, sel_count: int, sel_stride: int, out: int,
                            out_dtype: int, num_splits: int, workspace: int, workspace_bytes: int,
-                           dev_status: int, stream: int) -> None:
+                           dev_status: int, stream: int, fresh_rows: int = -1) -> None:
+    """fresh_rows comes last here (keyword, default -1: no early start) and
+    goes to its place after num_splits in the C call."""
     _check(lib().pkv_paged_decode_attention(ctypes.byref(cache), batch, num_q_heads, q, q_dtype,
                                             sm_scale, block_table, max_pages, seq_lens,
                                             sel_pages or None, sel_count or None, sel_stride, out,
-                                            out_dtype, num_splits, workspace, workspace_bytes,
-                                            dev_status or None, stream or None),
+                                            out_dtype, num_splits, fresh_rows, workspace,
+                                            workspace_bytes, dev_status or None, stream or None),
            "paged_decode_attention")
 
 

@@ -146,8 +146,14 @@ class PagedKVCache:
                   sel_count: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   out_dtype: torch.dtype = torch.float32, num_splits: int = 0,
                   dev_status: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-        """Decode attention for q [B][Hq][d]; dense, or over sel[b][h][:sel_count[b][h]] pages."""
+                  stream: Optional[torch.cuda.Stream] = None, fresh_rows: int = -1) -> torch.Tensor:
+        """Decode attention for q [B][Hq][d]; dense, or over sel[b][h][:sel_count[b][h]] pages.
+
+        fresh_rows >= 0 lets the call start while the kernel launched just before
+        it on the stream still runs, on the promise that, of this call's inputs,
+        that kernel writes only the K/V rows of the last fresh_rows tokens of each
+        sequence (e.g. the kv_append of this step, fresh_rows = its token count;
+        0 after another attention call)."""
         _need(q, "q", device=self.device)
         _need(block_table, "block_table", torch.int32, self.device)
         _need(seq_lens, "seq_lens", torch.int32, self.device)
@@ -162,7 +168,8 @@ class PagedKVCache:
             self._desc, Bsz, Hq, q.data_ptr(), pkv_dtype(q), float(sm_scale),
             block_table.data_ptr(), block_table.shape[1], seq_lens.data_ptr(), _ptr(sel),
             _ptr(sel_count), sel.shape[2] if sparse else 0, out.data_ptr(), pkv_dtype(out),
-            num_splits, ws.data_ptr(), ws.numel(), _ptr(dev_status), _stream(stream))
+            num_splits, ws.data_ptr(), ws.numel(), _ptr(dev_status), _stream(stream),
+            fresh_rows=fresh_rows)
         return out
 
 

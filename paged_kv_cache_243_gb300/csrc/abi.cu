@@ -261,8 +261,9 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       const int32_t* block_table, int32_t max_pages,
                                       const int32_t* seq_lens, const int32_t* sel_pages,
                                       const int32_t* sel_count, int32_t sel_stride, void* out,
-                                      pkv_dtype out_dtype, int32_t num_splits, void* workspace,
-                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                                      pkv_dtype out_dtype, int32_t num_splits, int32_t fresh_rows,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
   pkv_status st = check_cache(cache, true);
   if (st != PKV_OK) return st;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
@@ -274,6 +275,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   const bool sparse = sel_pages != nullptr;
   if (sparse && (!sel_count || sel_stride <= 0)) return PKV_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !(sm_scale < 1e30f)) return PKV_ERR_INVALID_ARG;
+  if (fresh_rows < -1) return PKV_ERR_INVALID_ARG;
   AttnPlan pl;
   st = plan_attention(cache, batch, num_q_heads, sparse, num_splits, q_dtype, pl);
   if (st != PKV_OK) return st;
@@ -313,6 +315,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.q_dtype = q_dtype;
   p.out_dtype = out_dtype;
   p.q_scale = sm_scale * 1.4426950408889634f;
+  p.fresh_rows = fresh_rows;
   void* args[] = {&p};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);

@@ -70,6 +70,12 @@ struct AttnParams {
   int num_ctas, stages;
   int q_dtype, out_dtype;
   float q_scale;  // sm_scale * log2(e): scores live in the log2 domain
+  // < 0: wait for the preceding kernel before reading anything. >= 0: that
+  // kernel writes, of this launch's inputs, only K/V rows (and scales) at
+  // positions >= seq_len - fresh_rows (for per-group INT8: from the start of
+  // the 64-token group holding that position), so everything else is read
+  // while it still runs; see the early-start notes in the kernel.
+  int fresh_rows;
 };
 
 struct ChunkInfo {
@@ -79,7 +85,7 @@ struct ChunkInfo {
   int u;
   int nvalid;
   int valid;
-  int pad;
+  int fresh;  // overlaps rows the preceding kernel may still be writing
 };
 
 template <int D, int KV>
@@ -327,8 +333,19 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   const int ps = p.page_size;
   const bool sparse = p.sel_pages != nullptr;
 
-  pdl_wait();
-  pdl_launch_dependents();
+  // Early start (fresh_rows >= 0). The launch may begin while the preceding
+  // kernel on the stream still runs. Reads of the lengths, tables, q and of
+  // all K/V rows that kernel does not write go ahead at once; griddepcontrol
+  // .wait comes before the producer copies a chunk holding fresh rows, before
+  // any thread's first global write (the preceding kernel may still read the
+  // output or the workspace), and in every block before it exits, so this
+  // grid never completes, or lets its dependents start, before the preceding
+  // one has completed.
+  const bool early = p.fresh_rows >= 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   // ---- sequence lengths (clamped to the block table) and unit chunk counts
   for (int b = tid; b < p.batch; b += kAttnThreads) {
     int L = p.seq_lens[b];
@@ -392,8 +409,6 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   }
   __syncthreads();
 
-  if (blockIdx.x == 0)
-    for (int u = tid; u <= U; u += kAttnThreads) p.ws_prefix[u] = prefix[u];
   const long long W = prefix[U];
   const long long N = p.num_ctas;
   const int c = blockIdx.x;
@@ -402,17 +417,27 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   const int ua = lo < hi ? find_unit(prefix, U, lo) : 0;
   const int ub = lo < hi ? find_unit(prefix, U, hi - 1) : -1;
 
+  // the unit prefix for the combine: block 0 writes it here when it has no
+  // chunks, else in its merge phase (after its wait in early mode)
+  if (blockIdx.x == 0 && lo >= hi) {
+    if (early) pdl_wait();
+    for (int u = tid; u <= U; u += kAttnThreads) p.ws_prefix[u] = prefix[u];
+  }
   // ---- units without any chunk produce zeros (block u mod N writes them)
   if (warp < NW) {
     for (int u = c; u < U; u += (int)N) {
       if (prefix[u] != prefix[u + 1]) continue;
+      if (early) pdl_wait();
       const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
       const int qh0 = sparse ? hu : hu * p.group;
       for (int i = tid; i < GE * D; i += NW * 32)
         store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + i, 0.f);
     }
   }
-  if (lo >= hi) return;
+  if (lo >= hi) {
+    if (early) pdl_wait();   // the block must not complete before the preceding grid
+    return;
+  }
 
   if (warp == NW) {
     // ================================================================ producer
@@ -440,7 +465,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     };
     auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
       ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
-      ci.nvalid = 0; ci.valid = 0; ci.pad = 0;
+      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0;
       if (r.u < 0) return;
       const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
       const int L = lens[b];
@@ -472,6 +497,11 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
       ci.nvalid = nv;
       ci.valid = 1;
+      if (early) {
+        int bnd = L - p.fresh_rows;   // first row the preceding kernel may write
+        if constexpr (KV == KV_I8G) bnd = bnd <= 0 ? 0 : bnd / 64 * 64;
+        ci.fresh = t0 + nv > bnd;
+      }
     };
     // Copies are issued by up to S lanes at once (one per ring stage): a single
     // issuing thread serialises the bulk-copy instructions and cannot keep the
@@ -479,6 +509,12 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     // stage's previous use, which is always the phase just before its own.
     int nbase = 0;
     bool abort = false;
+    bool waited = !early;    // warp-uniform
+    auto wait_prior = [&]() {
+      pdl_wait();
+      pdl_launch_dependents();
+      waited = true;
+    };
     Raw cur;
     fetch(lo + lane, cur);
     for (int base = lo; base < hi && !abort; base += 32) {
@@ -487,7 +523,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       const int cnt = min(32, hi - base);
       bool my_abort = false;
       for (int k0 = 0; k0 < cnt; k0 += S) {
-        if (lane >= k0 && lane < min(cnt, k0 + S)) {
+        const bool mine = lane >= k0 && lane < min(cnt, k0 + S);
+        if (!waited && __any_sync(0xffffffffu, mine && e.fresh)) wait_prior();
+        if (mine) {
           const int n = nbase + lane;
           const int s = n % S, use = n / S;
           if (use > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (use - 1) & 1)) {
@@ -514,7 +552,11 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       nbase += cnt;
       // the next batch's table loads overlap the streaming of the stages just issued
       fetch(base + 32 + lane, cur);
+      // early start: by the end of the first batch the preceding kernel is
+      // normally done; waiting here costs nothing and lets dependents launch
+      if (!waited) wait_prior();
     }
+    if (!waited) wait_prior();
     const int n = nbase;
     // Let every issued copy land before this warp (and so the block) can exit.
     if (lane == 0) {
@@ -546,6 +588,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   auto rec_of = [&](int u) { return p.ws_wrec + ((size_t)(c + u) * NW + warp) * WRS; };
 
   auto write_empty = [&](int u) {
+    if (early) pdl_wait();
     if (lane < GE) {
       float* rec = rec_of(u);
       rec[lane] = -INFINITY;
@@ -554,6 +597,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   };
 
   auto flush = [&](int u) {
+    if (early) pdl_wait();
     float* rec = rec_of(u);
 #pragma unroll
     for (int h = 0; h < GE; ++h) {
@@ -758,6 +802,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   constexpr int WRS = rec_floats(GE, D), WHDR = rec_hdr(GE);
   auto rec_of = [&](int u) { return p.ws_wrec + ((size_t)(c + u) * NW + warp) * WRS; };
   auto write_empty = [&](int u) {
+    if (early) pdl_wait();
     if (lane < GE) {
       float* rec = rec_of(u);
       rec[lane] = -INFINITY;
@@ -765,6 +810,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     }
   };
   auto flush = [&](int u) {
+    if (early) pdl_wait();
     float* rec = rec_of(u);
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
@@ -1029,6 +1075,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   constexpr int OUTS = GE * D;                           // outputs of one unit
   constexpr int OPT = (OUTS + NW * 32 - 1) / (NW * 32);  // outputs per thread
   named_bar_sync(1, NW * 32);
+  if (early) pdl_wait();
+  if (blockIdx.x == 0)
+    for (int u = tid; u <= U; u += NW * 32) p.ws_prefix[u] = prefix[u];
   for (int u = ua; u <= ub; ++u) {
     if (prefix[u] == prefix[u + 1]) continue;
     const bool alone = cta_of(prefix[u], W, N) == cta_of(prefix[u + 1] - 1, W, N);

@@ -66,7 +66,7 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t ba
   // The workspace needs no initial contents, so nothing is cleared here.
   return pkv_paged_decode_attention(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table,
                                     max_pages, seq_lens, sel_pages, sel_count, sel_stride, out,
-                                    out_dtype, num_splits, scratch, pkv::kNoallocScratchBytes,
+                                    out_dtype, num_splits, -1, scratch, pkv::kNoallocScratchBytes,
                                     dev_status, stream);
 }
 

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(B):
 
 
 def test_status_strings_and_version(B):
-    assert B.abi_version() == 1
+    assert B.abi_version() == 2
     assert B.status_string(B.OK) == "ok"
     assert B.status_string(B.ERR_OUT_OF_PAGES) == "out of pages"
 
@@ -71,6 +71,10 @@ def test_argument_checks_before_cuda(B):
     with pytest.raises(B.PkvError) as e:   # misaligned out
         B.paged_decode_attention(good, 1, 2, 0x4000, B.F16, 0.125, 0x5000, 4, 0x6000, 0, 0, 0,
                                  0x7004, B.F32, 0, 0x8000, 1 << 20, 0, 0)
+    assert e.value.status == B.ERR_INVALID_ARG
+    with pytest.raises(B.PkvError) as e:   # fresh_rows below -1
+        B.paged_decode_attention(good, 1, 2, 0x4000, B.F16, 0.125, 0x5000, 4, 0x6000, 0, 0, 0,
+                                 0x7000, B.F32, 0, 0x8000, 1 << 20, 0, 0, fresh_rows=-2)
     assert e.value.status == B.ERR_INVALID_ARG
     with pytest.raises(B.PkvError) as e:   # sparse without counts
         B.paged_decode_attention(good, 1, 2, 0x4000, B.F16, 0.125, 0x5000, 4, 0x6000, 0x9000, 0, 4,

@@ -1,0 +1,99 @@
+"""Early start of the attention kernel (fresh_rows >= 0): the launch overlaps
+the kernel before it on the stream and reads everything but the rows that
+kernel writes before waiting for it. Results must equal the oracle's for
+appends of one and several tokens, across 64-token group boundaries of
+per-group INT8 caches, and for back-to-back calls sharing output and
+workspace."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import TOL, bits_to_torch, load_workload, oracle_dense, queries_dev
+from oracle.quant import per_group_dequant, per_token_dequant
+
+pytestmark = pytest.mark.gpu
+
+
+def _restored(w, k):
+    """K or V as attention sees it after quantising every token at once."""
+    if w.quant == "none":
+        return k.astype(np.float64)
+    if w.quant == "per_token":
+        return per_token_dequant(*oracle.quantize_per_token(k))
+    return per_group_dequant(*oracle.quantize_per_group(k))
+
+
+CASES = [
+    # name, dtype, quant, d, Hq, Hkv, page
+    ("bf16", "bf16", "none", 128, 8, 2, 16),
+    ("f16-mha", "f16", "none", 64, 4, 4, 32),
+    ("i8-token", "f16", "per_token", 128, 8, 2, 16),
+    ("i8-group", "f16", "per_group64", 128, 16, 4, 64),
+]
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+@pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps", CASES)
+def test_append_then_attention_overlapped(name, dt, quant, d, Hq, Hkv, ps, splits):
+    w = synth.Workload(name="early-" + name, seed=610 + d + Hq + ps, batch=3, layers=1,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt,
+                       quant=quant, seq_len=None, seq_len_range=(1, 300),
+                       outlier_channels=4 if quant != "none" else 0, outlier_scale=15.0)
+    lens = np.array([61, 190, 1], dtype=np.int32)
+    steps = [1, 1, 3, 1, 70, 1, 2]               # tokens appended per sequence each step
+    ld = load_workload(w, lens=lens, extra_pages=-(-sum(steps) // ps) + 1)
+    K = [s.k for s in ld.seqs]
+    V = [s.v for s in ld.seqs]
+    cur = lens.copy()
+    tok = 0
+    for i, t_new in enumerate(steps):
+        toks = [[synth.append_tokens(w, b, tok + j) for j in range(t_new)] for b in range(w.batch)]
+        tok += t_new
+        kb = np.stack([np.concatenate([t.k_bits for t in row]) for row in toks])
+        vb = np.stack([np.concatenate([t.v_bits for t in row]) for row in toks])
+        ld.cache.append(bits_to_torch(kb, dt).cuda(), bits_to_torch(vb, dt).cuda(), ld.bt_dev,
+                        torch.from_numpy(cur.copy()).cuda(), dev_status=ld.status)
+        for b in range(w.batch):
+            K[b] = np.concatenate([K[b]] + [t.k for t in toks[b]])
+            V[b] = np.concatenate([V[b]] + [t.v for t in toks[b]])
+        cur = cur + t_new
+        q, qf = queries_dev(w, step=i)
+        out = ld.cache.attention(q, ld.bt_dev, torch.from_numpy(cur.copy()).cuda(), sm_scale=w.sm_scale,
+                                 num_splits=splits, dev_status=ld.status, fresh_rows=t_new)
+        out = out.cpu().numpy()
+        for b in range(w.batch):
+            kd, vd = _restored(w, K[b]), _restored(w, V[b])
+            for h in range(Hq):
+                g = h // w.group
+                o = oracle.decode_attention_tokens(qf[b, h], kd[:, g], vd[:, g], w.sm_scale)
+                tol = TOL["int8"] if quant != "none" else TOL[dt]
+                assert np.abs(out[b, h] - o).max() <= tol, (i, b, h)
+    assert int(ld.status.item()) == 0
+
+
+def test_back_to_back_calls_share_output_and_workspace():
+    # each call may start while the previous call's combine still writes the
+    # same output buffer and reads the same workspace
+    w = synth.Workload(name="early-b2b", seed=640, batch=4, layers=1, num_q_heads=16, num_kv_heads=4,
+                       head_dim=128, page_size=16, dtype="bf16", quant="none", seq_len=None,
+                       seq_len_range=(1, 600))
+    ld = load_workload(w, lens=np.array([600, 33, 257, 1], dtype=np.int32))
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    outs = [torch.empty_like(out) for _ in range(4)]
+    qs = [queries_dev(w, step=i) for i in range(4)]
+    for i, (q, _) in enumerate(qs):            # distinct outputs, one workspace
+        ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, out=outs[i],
+                           dev_status=ld.status, fresh_rows=0)
+    for q, _ in qs:                            # one output written four times
+        ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, out=out,
+                           dev_status=ld.status, fresh_rows=0)
+    torch.cuda.synchronize()
+    for i, (_, qf) in enumerate(qs):
+        ref = oracle_dense(ld, qf)
+        got = outs[i].cpu().numpy()
+        assert max(float(np.abs(got[b, h] - o).max()) for (b, h), o in ref.items()) <= TOL["bf16"]
+    last = out.cpu().numpy()
+    assert np.array_equal(last, outs[3].cpu().numpy())
+    assert int(ld.status.item()) == 0
