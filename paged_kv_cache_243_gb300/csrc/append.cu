@@ -58,14 +58,21 @@ __global__ void append_copy_kernel(const AppendParams p) {
   const int total = 2 * H * per_head;
   constexpr int kMaxPer = 4;  // 16-byte vectors per thread held across the lookup
   uint4 vals[kMaxPer];
-  int n_mine = 0;
-  for (int idx = threadIdx.x; idx < total && n_mine < kMaxPer; idx += blockDim.x, ++n_mine) {
-    const int kv = idx / (H * per_head);
+  auto src_of = [&](int idx, int& kv, int& g, int& e8) {
+    kv = idx / (H * per_head);
     const int rem = idx - kv * H * per_head;
-    const int g = rem / per_head, e8 = rem - g * per_head;
-    const size_t src = (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
-    vals[n_mine] = *reinterpret_cast<const uint4*>(
-        reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src);
+    g = rem / per_head;
+    e8 = rem - g * per_head;
+    return (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
+  };
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int idx = threadIdx.x + k * blockDim.x;
+    if (idx < total) {
+      int kv, g, e8;
+      const size_t src = src_of(idx, kv, g, e8);
+      vals[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src);
+    }
   }
   int pos, n;
   if (!row_window(p, b, pos, n) || t >= n) return;
@@ -73,19 +80,14 @@ __global__ void append_copy_kernel(const AppendParams p) {
   const int phys = page_of(p, b, tp / p.page_size);
   if (phys < 0) return;
   const int slot = tp % p.page_size;
-  int i = 0;
-  for (int idx = threadIdx.x; idx < total; idx += blockDim.x, ++i) {
-    const int kv = idx / (H * per_head);
-    const int rem = idx - kv * H * per_head;
-    const int g = rem / per_head, e8 = rem - g * per_head;
-    const size_t src = (((size_t)b * p.t_new + t) * H + g) * D + e8 * 8;
+  auto put = [&](int idx, uint4 v) {
+    int kv, g, e8;
+    src_of(idx, kv, g, e8);
     const size_t dst = (((size_t)phys * H + g) * p.page_size + slot) * D + e8 * 8;
     uint16_t* dp = reinterpret_cast<uint16_t*>(kv ? p.v_pages : p.k_pages);
-    uint4 v = i < kMaxPer ? vals[i]
-                          : *reinterpret_cast<const uint4*>(
-                                reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src);
     if (p.src_dtype != p.kv_dtype) {
       uint16_t* h = reinterpret_cast<uint16_t*>(&v);
+#pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float x = p.src_dtype == PKV_BF16 ? __bfloat162float(__ushort_as_bfloat16(h[e]))
                                                 : __half2float(__ushort_as_half(h[e]));
@@ -94,6 +96,16 @@ __global__ void append_copy_kernel(const AppendParams p) {
       }
     }
     *reinterpret_cast<uint4*>(dp + dst) = v;
+  };
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int idx = threadIdx.x + k * blockDim.x;
+    if (idx < total) put(idx, vals[k]);
+  }
+  for (int idx = threadIdx.x + kMaxPer * blockDim.x; idx < total; idx += blockDim.x) {
+    int kv, g, e8;
+    const size_t src = src_of(idx, kv, g, e8);
+    put(idx, *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new) + src));
   }
 }
 
@@ -121,10 +133,13 @@ __global__ void append_per_token_kernel(const AppendParams p) {
   const int per = D / 32;  // 4 (D = 128) or 2 (D = 64)
   float x[4];
   float mn = INFINITY, mx = -INFINITY;
-  for (int e = 0; e < per; ++e) {
-    x[e] = load_src(sp, p.src_dtype, src + lane * per + e);
-    mn = fminf(mn, x[e]);
-    mx = fmaxf(mx, x[e]);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (e < per) {
+      x[e] = load_src(sp, p.src_dtype, src + lane * per + e);
+      mn = fminf(mn, x[e]);
+      mx = fmaxf(mx, x[e]);
+    }
   }
   for (int off = 16; off > 0; off >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
@@ -135,7 +150,9 @@ __global__ void append_per_token_kernel(const AppendParams p) {
   const size_t row = ((size_t)phys * H + g) * p.page_size + slot;
   int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + lane * per;
   uint32_t packed = 0;
-  for (int e = 0; e < per; ++e) packed |= (uint32_t)(uint8_t)(int8_t)quant_code(x[e], s, z) << (8 * e);
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (e < per) packed |= (uint32_t)(uint8_t)(int8_t)quant_code(x[e], s, z) << (8 * e);
   if (per == 4)
     *reinterpret_cast<uint32_t*>(dst) = packed;
   else
@@ -150,15 +167,38 @@ __device__ __forceinline__ float* tail_row(const AppendParams& p, int b, int g, 
   return p.tail + ((((size_t)b * p.num_kv_heads + g) * 2 + kv) * 2 + parity) * 64 * p.head_dim;
 }
 
+// Four consecutive source values (f16/bf16) widened to fp32; i is a multiple of 4.
+__device__ __forceinline__ float4 load_src4(const void* p, int dtype, size_t i) {
+  const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p) + i);
+  if (dtype == PKV_BF16)
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+  return make_float4(__half2float(__ushort_as_half((unsigned short)(w.x & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.x >> 16))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y >> 16))));
+}
+
+__device__ __forceinline__ uint32_t quant4(const float4& x, float s, float z) {
+  return (uint32_t)(uint8_t)(int8_t)quant_code(x.x, s, z) |
+         (uint32_t)(uint8_t)(int8_t)quant_code(x.y, s, z) << 8 |
+         (uint32_t)(uint8_t)(int8_t)quant_code(x.z, s, z) << 16 |
+         (uint32_t)(uint8_t)(int8_t)quant_code(x.w, s, z) << 24;
+}
+
 // Per-64-token-group INT8. grid (group slot, kv head * 2 + kv, row); one block
 // re-quantises one group that received tokens: its members are the kept
 // originals of earlier tokens of the open group (tail) plus the new tokens.
 // write_tail: also keep the new members of a group that stays open.
-__global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
+// Each thread holds up to kGroupVec4 float4s of the group in registers; all
+// of its loads (tail and new tokens) are issued before the first use, and
+// before the block-table lookup, so the block pays about one memory latency.
+constexpr int kGroupThreads = 256;
+constexpr int kGroupVec4 = 64 * 128 / 4 / kGroupThreads;   // head_dim <= 128
+__global__ void __launch_bounds__(kGroupThreads) append_per_group_kernel(const AppendParams p, int write_tail) {
   pdl_wait();
   pdl_launch_dependents();
-  __shared__ float vals[64 * 128];
-  __shared__ float red_mn[32], red_mx[32];
+  __shared__ float red_mn[kGroupThreads / 32], red_mx[kGroupThreads / 32];
   __shared__ int ok_s;
   const int b = blockIdx.z, g = blockIdx.y >> 1, kv = blockIdx.y & 1;
   const int D = p.head_dim, H = p.num_kv_heads;
@@ -168,39 +208,44 @@ __global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
   if (gi > (pos + n - 1) / 64) return;
   const int t0 = gi * 64;
   const int t_end = min(t0 + 64, pos + n);
-  const int nm = t_end - t0;
-  if (threadIdx.x == 0) ok_s = page_of(p, b, t0 / p.page_size);
-  __syncthreads();
-  const int phys = ok_s;
-  if (phys < 0) return;
+  const int nf = (t_end - t0) * D / 4;      // float4s of the group
   const void* sp = kv ? p.v_new : p.k_new;
   const float* tl = tail_row(p, b, g, kv, gi & 1);
+  float4 x[kGroupVec4];
+#pragma unroll
+  for (int k = 0; k < kGroupVec4; ++k) {
+    const int f = threadIdx.x + k * kGroupThreads;
+    if (f < nf) {
+      const int i = 4 * f, tt = i / D, e = i - tt * D, tok = t0 + tt;
+      x[k] = tok < pos ? *reinterpret_cast<const float4*>(tl + (size_t)tt * D + e)
+                       : load_src4(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
+    }
+  }
+  if (threadIdx.x == 0) ok_s = page_of(p, b, t0 / p.page_size);
   float mn = INFINITY, mx = -INFINITY;
-  for (int i = threadIdx.x; i < nm * D; i += blockDim.x) {
-    const int tt = i / D, e = i - tt * D;
-    const int tok = t0 + tt;
-    float x;
-    if (tok < pos)
-      x = tl[(size_t)tt * D + e];
-    else
-      x = load_src(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
-    vals[i] = x;
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
+#pragma unroll
+  for (int k = 0; k < kGroupVec4; ++k) {
+    if (threadIdx.x + k * kGroupThreads < nf) {
+      mn = fminf(fminf(mn, x[k].x), fminf(x[k].y, fminf(x[k].z, x[k].w)));
+      mx = fmaxf(fmaxf(mx, x[k].x), fmaxf(x[k].y, fmaxf(x[k].z, x[k].w)));
+    }
   }
   for (int off = 16; off > 0; off >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     red_mn[warp] = mn;
     red_mx[warp] = mx;
   }
   __syncthreads();
+  const int phys = ok_s;
+  if (phys < 0) return;
   mn = red_mn[0];
   mx = red_mx[0];
-  for (int w = 1; w < nwarps; ++w) {
+#pragma unroll
+  for (int w = 1; w < kGroupThreads / 32; ++w) {
     mn = fminf(mn, red_mn[w]);
     mx = fmaxf(mx, red_mx[w]);
   }
@@ -209,18 +254,21 @@ __global__ void append_per_group_kernel(const AppendParams p, int write_tail) {
   const int off0 = t0 % p.page_size;
   int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) +
                 (((size_t)phys * H + g) * p.page_size + off0) * D;
-  for (int i = threadIdx.x; i < nm * D; i += blockDim.x) dst[i] = (int8_t)quant_code(vals[i], s, z);
+  float* tw = tail_row(p, b, g, kv, gi & 1);
+  const bool keep = write_tail && t_end - t0 < 64;
+#pragma unroll
+  for (int k = 0; k < kGroupVec4; ++k) {
+    const int f = threadIdx.x + k * kGroupThreads;
+    if (f < nf) {
+      const int i = 4 * f;
+      *reinterpret_cast<uint32_t*>(dst + i) = quant4(x[k], s, z);
+      if (keep && t0 + i / D >= pos) *reinterpret_cast<float4*>(tw + i) = x[k];
+    }
+  }
   if (threadIdx.x == 0) {
     float* szp = p.kv_sz + (((size_t)phys * H + g) * (p.page_size / 64) + off0 / 64) * 4;
     szp[kv * 2 + 0] = s;
     szp[kv * 2 + 1] = z;
-  }
-  if (write_tail && nm < 64) {
-    float* tw = tail_row(p, b, g, kv, gi & 1);
-    for (int i = threadIdx.x; i < nm * D; i += blockDim.x) {
-      const int tt = i / D;
-      if (t0 + tt >= pos) tw[i] = vals[i];
-    }
   }
 }
 
@@ -265,19 +313,27 @@ __global__ void append_meta_kernel(const AppendParams p) {
   const int nv = min(ps, pos + n - lp * ps);
   const size_t row0 = ((size_t)phys * H + g) * ps;
   float mn = INFINITY, mx = -INFINITY;
-  for (int s = 0; s < nv; ++s) {
-    float x;
-    if (p.kv_dtype == PKV_I8) {
-      const int code = reinterpret_cast<const int8_t*>(p.k_pages)[(row0 + s) * D + i];
-      const float* sz = p.quant == PKV_QUANT_PER_TOKEN
-                            ? p.kv_sz + (row0 + s) * 4
-                            : p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + s / 64) * 4;
-      x = __fadd_rn(__fmul_rn((float)(code + 128), sz[0]), sz[1]);
-    } else {
-      x = load_src(p.k_pages, p.kv_dtype, (row0 + s) * D + i);
+  // 8 rows per pass, their loads issued together
+  for (int s0 = 0; s0 < nv; s0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s = min(s0 + k, nv - 1);     // a repeated row leaves min/max unchanged
+      if (p.kv_dtype == PKV_I8) {
+        const int code = reinterpret_cast<const int8_t*>(p.k_pages)[(row0 + s) * D + i];
+        const float* sz = p.quant == PKV_QUANT_PER_TOKEN
+                              ? p.kv_sz + (row0 + s) * 4
+                              : p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + s / 64) * 4;
+        x[k] = __fadd_rn(__fmul_rn((float)(code + 128), sz[0]), sz[1]);
+      } else {
+        x[k] = load_src(p.k_pages, p.kv_dtype, (row0 + s) * D + i);
+      }
     }
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      mn = fminf(mn, x[k]);
+      mx = fmaxf(mx, x[k]);
+    }
   }
   float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D;
   meta[i] = mn;
@@ -304,7 +360,7 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
     int inline_tail = p.t_new <= 64;
     void* args2[] = {&pc, &inline_tail};
     e = launch_pdl(reinterpret_cast<const void*>(&append_per_group_kernel), dim3(groups, H * 2, p.batch),
-                   dim3(256), 0, st, args2);
+                   dim3(kGroupThreads), 0, st, args2);
     if (e == cudaSuccess && !inline_tail)
       e = launch_pdl(reinterpret_cast<const void*>(&append_tail_kernel), dim3(H * 2, p.batch), dim3(256), 0,
                      st, args1);

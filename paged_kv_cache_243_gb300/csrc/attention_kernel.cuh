@@ -1150,13 +1150,17 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
   const int o = blockIdx.y * 128 + tid;
   if (o >= OUTS) return;
   const int h = o / D;
+  // With at least one chunk per block (W >= N) every covering block holds a
+  // record; otherwise blocks with empty ranges are skipped (64-bit divisions,
+  // too slow to do per record in the common case).
+  const bool dense_cover = W >= N;
   float M = -INFINITY, L = 0.f, A = 0.f;
   for (int cc0 = c_first; cc0 <= c_last; cc0 += 16) {
     float mc[16], lc[16], ac[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int cc = cc0 + i;
-      const bool ok = cc <= c_last && cta_lo(cc, W, N) < cta_lo(cc + 1, W, N);
+      const bool ok = cc <= c_last && (dense_cover || cta_lo(cc, W, N) < cta_lo(cc + 1, W, N));
       const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
       mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
       lc[i] = __ldcg(rr + GE + h);
