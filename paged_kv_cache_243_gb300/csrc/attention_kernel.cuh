@@ -258,6 +258,12 @@ __device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t wflip, uint32_t sel) {
   return r;
 }
 
+// The same pair left as 1024 + u (no subtraction): for the values of P.V,
+// where the 1024 offset is removed through the zero-point sum instead.
+__device__ __forceinline__ uint32_t u8x2_to_h2_biased(uint32_t wflip, uint32_t sel) {
+  return __byte_perm(wflip, 0x64646464u, sel);
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -812,6 +818,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   auto flush = [&](int u) {
     if (early) pdl_wait();
     float* rec = rec_of(u);
+    // l and the zero-point sum are kept per lane (tokens g, g + 8); sum the 8
+    // lanes of each head here instead of on every chunk
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l2[jj] += __shfl_xor_sync(0xffffffffu, l2[jj], off);
+        if constexpr (KV == KV_I8T || KV == KV_I8G) zs2[jj] += __shfl_xor_sync(0xffffffffu, zs2[jj], off);
+      }
+    }
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       const int h = 2 * t + jj;
@@ -883,8 +899,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     if (h4.z) {
       const int nvalid = h4.y;
       const float* sz = reinterpret_cast<const float*>(st + 2 * KB);
-      // ---- q.K^T on the tensor cores
+      // ---- q.K^T on the tensor cores (even and odd k-steps in two
+      // accumulators: two dependent MMA chains of half the length)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sco[4] = {0.f, 0.f, 0.f, 0.f};
       {
         uint4 k0[NB], k1[NB];
 #pragma unroll
@@ -910,8 +928,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
             a1 = word_of(k1[m], wi);
             a3 = word_of(k1[m], wi + 1);
           }
-          mma16816<BF>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          if (kk & 1)
+            mma16816<BF>(sco, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          else
+            mma16816<BF>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] += sco[e];
       }
       // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
       float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
@@ -922,14 +945,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         sc[1] = fmaf(z0.x, sc[1], z0.y * qs[1]);
         sc[2] = fmaf(z1.x, sc[2], z1.y * qs[0]);
         sc[3] = fmaf(z1.x, sc[3], z1.y * qs[1]);
-        vs0 = z0.z; vz0 = z0.w; vs1 = z1.z; vz1 = z1.w;
+        // V codes enter P.V as 1024 + u: vs (1024 + u) + (vz - 1024 vs) = vs u + vz
+        vs0 = z0.z; vz0 = fmaf(-1024.f, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(-1024.f, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
         const float4 z = *reinterpret_cast<const float4*>(sz);
         sc[0] = fmaf(z.x, sc[0], z.y * qs[0]);
         sc[1] = fmaf(z.x, sc[1], z.y * qs[1]);
         sc[2] = fmaf(z.x, sc[2], z.y * qs[0]);
         sc[3] = fmaf(z.x, sc[3], z.y * qs[1]);
-        vs0 = vs1 = z.z; vz0 = vz1 = z.w;
+        vs0 = vs1 = z.z;
+        vz0 = vz1 = fmaf(-1024.f, z.z, z.w);   // as for per-token scales
       }
       const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
 #pragma unroll
@@ -947,21 +972,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         const float mn = fmaxf(m2[jj], cm);
         al[jj] = exp2f(m2[jj] - mn);
         const float p0 = exp2f(sc[jj] - mn), p1 = exp2f(sc[2 + jj] - mn);
-        float ps = p0 + p1;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l2[jj] = fmaf(l2[jj], al[jj], ps);
+        // lane-local running sums (rescaled like the accumulator; the lanes
+        // of a head are summed at flush)
+        l2[jj] = fmaf(l2[jj], al[jj], p0 + p1);
         if constexpr (KV == KV_I8T) {
-          float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
-          pz += __shfl_xor_sync(0xffffffffu, pz, 4);
-          pz += __shfl_xor_sync(0xffffffffu, pz, 8);
-          pz += __shfl_xor_sync(0xffffffffu, pz, 16);
+          const float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
           zs2[jj] = fmaf(zs2[jj], al[jj], pz);
           pw[jj] = ok0 ? p0 * vs0 : 0.f;
           pw[2 + jj] = ok1 ? p1 * vs1 : 0.f;
         } else if constexpr (KV == KV_I8G) {
-          zs2[jj] = fmaf(zs2[jj], al[jj], vz0 * ps);
+          zs2[jj] = fmaf(zs2[jj], al[jj], vz0 * (p0 + p1));
           pw[jj] = p0 * vs0;
           pw[2 + jj] = p1 * vs1;
         } else {
@@ -982,13 +1002,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       uint32_t bh0, bl0, bh1, bl1;
       split_hi_lo<BF>(pv4.x, pv4.y, bh0, bl0);
       split_hi_lo<BF>(pv4.z, pv4.w, bh1, bl1);
-      // ---- P.V on the tensor cores
+      // ---- P.V on the tensor cores. The accumulator is rescaled only when
+      // the running max of some head of the warp grew on this chunk.
+      if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        acc[mt][0] *= al[0];
-        acc[mt][2] *= al[0];
-        acc[mt][1] *= al[1];
-        acc[mt][3] *= al[1];
+        for (int mt = 0; mt < MT; ++mt) {
+          acc[mt][0] *= al[0];
+          acc[mt][2] *= al[0];
+          acc[mt][1] *= al[1];
+          acc[mt][3] *= al[1];
+        }
       }
       const uint8_t* vrow = st + KB;
       if constexpr (ESZ == 1) {
@@ -1006,21 +1029,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
             rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
           }
         }
-        if (nvalid < kChunk) {   // masked tokens: their codes may be stale; make them 0
-#pragma unroll
-          for (int jr = 0; jr < 4; ++jr)
-            if (4 * t + jr >= nvalid)
-#pragma unroll
-              for (int i = 0; i < DPT / 4; ++i) rw[jr][i] = 0u;
-        }
+        // Masked tokens (stale codes) need no clearing: every code is a
+        // finite 1024 + u and their weights are exactly 0.
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int wi = mt / 2;
           const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
           const uint32_t t01 = __byte_perm(rw[0][wi], rw[1][wi], sel);
           const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
-          const uint32_t a0 = u8x2_to_h2(t01, 0x4140u), a1 = u8x2_to_h2(t01, 0x4342u);
-          const uint32_t a2 = u8x2_to_h2(t23, 0x4140u), a3 = u8x2_to_h2(t23, 0x4342u);
+          const uint32_t a0 = u8x2_to_h2_biased(t01, 0x4140u), a1 = u8x2_to_h2_biased(t01, 0x4342u);
+          const uint32_t a2 = u8x2_to_h2_biased(t23, 0x4140u), a3 = u8x2_to_h2_biased(t23, 0x4342u);
           mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
           mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
