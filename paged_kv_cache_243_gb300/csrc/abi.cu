@@ -159,7 +159,8 @@ struct AttnPlan {
   bool mma = false;
   int ge = 1, units = 0, stages = 0, ctas = 0;
   size_t smem = 0;
-  size_t off_wrec = 0, off_crec = 0, ws_bytes = 0;
+  size_t off_wrec = 0, ws_bytes = 0;
+  int comb_groups = 1;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -217,13 +218,33 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     if (cap > 0 && cap < nb) nb = cap;
     pl.ctas = di.sms * nb;
   }
+  // Combine layout: about 4 (blocks per unit + 1) records per unit; more
+  // record groups per block fold them in fewer dependent rounds, fewer give
+  // more outputs per block (fewer blocks). Cost ~ waves * (1 + rounds).
+  {
+    const int outs = pl.ge * c->head_dim;
+    const long long units = pl.units > 0 ? pl.units : 1;
+    const long long rbar = (long long)kConsumerWarps * ((pl.ctas + units - 1) / units + 1);
+    const long long slots = (long long)di.sms * 3;
+    long long best = -1;
+    for (int rg = 1; rg <= 8; rg *= 2) {
+      const int ob = kCombineThreads / rg;
+      if (ob > outs && rg < 8) continue;
+      const long long blocks = units * ((outs + ob - 1) / ob);
+      const long long waves = (blocks + slots - 1) / slots;
+      const long long rounds = (rbar + rg * 8 - 1) / (rg * 8);
+      const long long cost = waves * (1 + rounds);
+      if (best < 0 || cost < best) {
+        best = cost;
+        pl.comb_groups = rg;
+      }
+    }
+  }
   const size_t rs = (size_t)rec_floats(pl.ge, c->head_dim);
   const size_t cslots = (size_t)(pl.ctas + pl.units);
   size_t off = align256((size_t)(pl.units + 1) * 4);        // unit chunk prefix
   pl.off_wrec = off;
   off = align256(off + cslots * kConsumerWarps * rs * 4);    // warp records
-  pl.off_crec = off;
-  off = align256(off + cslots * rs * 4);                     // block records
   pl.ws_bytes = off;
   return PKV_OK;
 }
@@ -298,7 +319,6 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_prefix = reinterpret_cast<int32_t*>(ws);
   p.ws_wrec = reinterpret_cast<float*>(ws + pl.off_wrec);
-  p.ws_crec = reinterpret_cast<float*>(ws + pl.off_crec);
   p.dev_status = dev_status;
   p.num_pages = cache->num_pages;
   p.page_size = cache->page_size;
@@ -316,12 +336,15 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.out_dtype = out_dtype;
   p.q_scale = sm_scale * 1.4426950408889634f;
   p.fresh_rows = fresh_rows;
+  p.comb_groups = pl.comb_groups;
   void* args[] = {&p};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);
-  if (e == cudaSuccess && pl.ctas > 1) {
+  if (e == cudaSuccess) {
     const void* comb = attn_combine(cache->head_dim, pl.ge);
-    e = launch_pdl(comb, dim3(pl.units, (pl.ge * cache->head_dim + 127) / 128), dim3(128), 0, cs, args);
+    const int outs = pl.ge * cache->head_dim;
+    const int ob = kCombineThreads / p.comb_groups;
+    e = launch_pdl(comb, dim3(pl.units, (outs + ob - 1) / ob), dim3(kCombineThreads), 0, cs, args);
   }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

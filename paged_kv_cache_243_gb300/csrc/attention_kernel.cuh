@@ -61,7 +61,6 @@ struct AttnParams {
   const int32_t* sel_pages;  // NULL: dense
   const int32_t* sel_count;
   float* ws_wrec;     // per-warp partial records, slot ((block + unit) * 4 + warp)
-  float* ws_crec;     // per-block partial records, slot (block + unit)
   int32_t* ws_prefix; // [num_units + 1] chunk prefix, written by block 0 for the combine
   int32_t* dev_status;
   int num_pages, page_size, num_kv_heads, num_q_heads, group;
@@ -76,6 +75,7 @@ struct AttnParams {
   // the 64-token group holding that position), so everything else is read
   // while it still runs; see the early-start notes in the kernel.
   int fresh_rows;
+  int comb_groups;  // record groups of the combine kernel (1, 2, 4 or 8)
 };
 
 struct ChunkInfo {
@@ -1085,108 +1085,112 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   }
   }
 
-  // ---- in-block merge. Every unit this block touched gets one block record
-  // from its 4 warp records; a unit that lies entirely inside this block is
-  // final here and goes to the output. Units shared with other blocks are
-  // finished by attn_combine_kernel, the next launch on the stream.
-  constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
-  constexpr int OUTS = GE * D;                           // outputs of one unit
-  constexpr int OPT = (OUTS + NW * 32 - 1) / (NW * 32);  // outputs per thread
-  named_bar_sync(1, NW * 32);
-  if (early) pdl_wait();
-  if (blockIdx.x == 0)
+  // Block 0 publishes the unit prefix for the combine of sparse calls (dense
+  // calls recompute it there from the lengths).
+  if (blockIdx.x == 0) {
+    if (early) pdl_wait();
     for (int u = tid; u <= U; u += NW * 32) p.ws_prefix[u] = prefix[u];
-  for (int u = ua; u <= ub; ++u) {
-    if (prefix[u] == prefix[u + 1]) continue;
-    const bool alone = cta_of(prefix[u], W, N) == cta_of(prefix[u + 1] - 1, W, N);
-    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-    const int qh0 = sparse ? hu : hu * p.group;
-    const float* wr = p.ws_wrec + (size_t)(c + u) * NW * RS;
-    float* cr = p.ws_crec + (size_t)(c + u) * RS;
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int o = tid + k * NW * 32;
-      if (o < OUTS) {
-        const int h = o / D, ch = o - h * D;
-        float mw[NW], lw[NW], aw[NW];
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          mw[w] = wr[w * RS + h];
-          lw[w] = wr[w * RS + GE + h];
-          aw[w] = wr[w * RS + HDR + o];
-        }
-        float M = mw[0];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) M = fmaxf(M, mw[w]);
-        float L = 0.f, A = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            const float f = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
-            L = fmaf(f, lw[w], L);
-            A = f > 0.f ? fmaf(f, aw[w], A) : A;
-          }
-        }
-        if (alone) {
-          store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o,
-                         L > 0.f ? A / L : 0.f);
-        } else {
-          if (ch == 0) {
-            cr[h] = M;
-            cr[GE + h] = L;
-          }
-          cr[HDR + o] = A;
-        }
-      }
-    }
   }
 }
 
-// Cross-block merge of the units that several blocks shared: one block per
-// unit, over the block records [m[G], l[G], acc[G][D]] of the covering blocks,
-//   M = max m_c,  out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
-// (the log2-domain partial states of the attention kernel).
+// Merge of every unit's warp records: the 4 records (one per consumer warp,
+// some empty) of each block whose range overlaps the unit, i.e. blocks
+// c_first .. c_last, whose slots ((c + u) * 4 + w) are consecutive:
+//   M = max m_r,  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r
+// (the log2-domain partial states of the attention kernel). The 256 threads
+// of block (u, y) form RG = comb_groups record groups of OB = 256 / RG
+// threads; thread (g, i) folds records g, g + RG, ... of output y OB + i of
+// unit u, and group 0 merges the RG partials. The host picks RG from the
+// expected records per unit (more groups when units span many blocks).
+// Dense calls compute the unit's chunk range from the sequence lengths before
+// waiting for the attention kernel (the lengths are inputs, not its output),
+// so only the record loads follow the wait.
+constexpr int kCombineThreads = 256;
 template <int D, int GE>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
+__global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const AttnParams p) {
   constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
-  constexpr int OUTS = GE * D;
-  const int u = blockIdx.x, tid = threadIdx.x;
-  const int U = p.num_units;
-  const long long W = __ldcg(p.ws_prefix + U), N = p.num_ctas;
-  const int s0 = __ldcg(p.ws_prefix + u), s1 = __ldcg(p.ws_prefix + u + 1);
-  if (s0 == s1) return;
-  const int c_first = cta_of(s0, W, N), c_last = cta_of(s1 - 1, W, N);
-  if (c_first == c_last) return;                 // finished by the attention kernel
+  constexpr int BATCH = 8;    // records in flight per thread
+  constexpr int NWC = kCombineThreads / 32;
+  __shared__ float part[3][kCombineThreads];
+  __shared__ long long red[3][NWC];
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int RG = p.comb_groups, OB = kCombineThreads / RG;
+  const int grp = tid / OB;
+  const int o = blockIdx.y * OB + (tid - grp * OB);   // output of the unit
+  const bool active = o < GE * D;
   const bool sparse = p.sel_pages != nullptr;
   const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-  const int qh0 = sparse ? hu : hu * p.group;
-  // One pass: each thread folds the covering blocks' (m, l, acc) of its own
-  // output online; the loads of 16 records are issued together. Block
-  // (unit, y) takes outputs [128 y, 128 y + 128) of the unit.
-  const int o = blockIdx.y * 128 + tid;
-  if (o >= OUTS) return;
-  const int h = o / D;
-  // With at least one chunk per block (W >= N) every covering block holds a
-  // record; otherwise blocks with empty ranges are skipped (64-bit divisions,
-  // too slow to do per record in the common case).
-  const bool dense_cover = W >= N;
-  float M = -INFINITY, L = 0.f, A = 0.f;
-  for (int cc0 = c_first; cc0 <= c_last; cc0 += 16) {
-    float mc[16], lc[16], ac[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int cc = cc0 + i;
-      const bool ok = cc <= c_last && (dense_cover || cta_lo(cc, W, N) < cta_lo(cc + 1, W, N));
-      const float* rr = p.ws_crec + (size_t)((ok ? cc : c_first) + u) * RS;
-      mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
-      lc[i] = __ldcg(rr + GE + h);
-      ac[i] = __ldcg(rr + HDR + o);
+  long long W = 0, s0 = 0, s1 = 0;
+  if (!sparse) {
+    // chunks of each kv head of sequence b' = ceil(clamped length / 16), as in
+    // the attention kernel: W = units_per_b * sum_b' n_b', and unit u starts
+    // after all units of sequences b' < b and hu units of sequence b
+    const int cap = p.max_pages * p.page_size;
+    long long tot = 0, before = 0, nb = 0;
+    for (int bb = tid; bb < p.batch; bb += kCombineThreads) {
+      int L = p.seq_lens[bb];
+      L = L < 0 ? 0 : (L > cap ? cap : L);
+      const long long n = (L + kChunk - 1) / kChunk;
+      tot += n;
+      if (bb < b) before += n;
+      if (bb == b) nb = n;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (mc[i] == -INFINITY) continue;
+    for (int off = 16; off > 0; off >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, off);
+      before += __shfl_xor_sync(0xffffffffu, before, off);
+      nb += __shfl_xor_sync(0xffffffffu, nb, off);
+    }
+    if (lane == 0) {
+      red[0][warp] = tot;
+      red[1][warp] = before;
+      red[2][warp] = nb;
+    }
+    __syncthreads();
+    tot = 0; before = 0; nb = 0;
+#pragma unroll
+    for (int w = 0; w < NWC; ++w) {
+      tot += red[0][w];
+      before += red[1][w];
+      nb += red[2][w];
+    }
+    W = tot * p.units_per_b;
+    s0 = before * p.units_per_b + (long long)hu * nb;
+    s1 = s0 + nb;
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (sparse) {
+    W = __ldcg(p.ws_prefix + p.num_units);
+    s0 = __ldcg(p.ws_prefix + u);
+    s1 = __ldcg(p.ws_prefix + u + 1);
+  }
+  if (s0 == s1) return;   // no chunks: the attention kernel wrote zeros
+  const long long N = p.num_ctas;
+  const int c_first = cta_of(s0, W, N), c_last = cta_of(s1 - 1, W, N);
+  const int R4 = (c_last - c_first + 1) * kConsumerWarps;
+  // With at least one chunk per block (W >= N) every covering block wrote its
+  // records; otherwise blocks with empty ranges are skipped.
+  const bool dense_cover = W >= N;
+  const int oo = active ? o : 0;
+  const int h = oo / D;
+  const float* rec0 = p.ws_wrec + (size_t)(c_first + u) * kConsumerWarps * RS;
+  float M = -INFINITY, L = 0.f, A = 0.f;
+  for (int r0 = grp; r0 < R4; r0 += RG * BATCH) {
+    float mc[BATCH], lc[BATCH], ac[BATCH];
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int r = r0 + i * RG;
+      const int cc = c_first + r / kConsumerWarps;
+      const bool ok = r < R4 && (dense_cover || cta_lo(cc, W, N) < cta_lo(cc + 1, W, N));
+      const float* rr = rec0 + (size_t)(ok ? r : 0) * RS;
+      mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
+      lc[i] = __ldcg(rr + GE + h);
+      ac[i] = __ldcg(rr + HDR + oo);
+    }
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      if (mc[i] == -INFINITY) continue;   // empty record: its acc is not written
       const float Mn = fmaxf(M, mc[i]);
       const float sc = exp2f(M - Mn), f = exp2f(mc[i] - Mn);
       L = fmaf(L, sc, f * lc[i]);
@@ -1194,6 +1198,24 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
       M = Mn;
     }
   }
+  if (RG > 1) {
+    part[0][tid] = M;
+    part[1][tid] = L;
+    part[2][tid] = A;
+    __syncthreads();
+    if (grp != 0) return;
+    for (int g = 1; g < RG; ++g) {
+      const float mw = part[0][g * OB + tid];
+      if (mw == -INFINITY) continue;
+      const float Mn = fmaxf(M, mw);
+      const float sc = exp2f(M - Mn), f = exp2f(mw - Mn);
+      L = fmaf(L, sc, f * part[1][g * OB + tid]);
+      A = fmaf(A, sc, f * part[2][g * OB + tid]);
+      M = Mn;
+    }
+  }
+  if (!active) return;
+  const int qh0 = sparse ? hu : hu * p.group;
   store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o, L > 0.f ? A / L : 0.f);
 }
 
