@@ -219,13 +219,14 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     pl.ctas = di.sms * nb;
   }
   // Combine layout: about 4 (blocks per unit + 1) records per unit; more
-  // record groups per block fold them in fewer dependent rounds, fewer give
-  // more outputs per block (fewer blocks). Cost ~ waves * (1 + rounds).
+  // record groups per block fold them in fewer rounds (loads of the next
+  // round overlap the current fold), fewer give more outputs per block
+  // (fewer blocks). Cost ~ waves * (3 + rounds).
   {
     const int outs = pl.ge * c->head_dim;
     const long long units = pl.units > 0 ? pl.units : 1;
     const long long rbar = (long long)kConsumerWarps * ((pl.ctas + units - 1) / units + 1);
-    const long long slots = (long long)di.sms * 3;
+    const long long slots = (long long)di.sms * 2;   // combine blocks resident at once
     long long best = -1;
     for (int rg = 1; rg <= 8; rg *= 2) {
       const int ob = kCombineThreads / rg;
@@ -233,7 +234,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
       const long long blocks = units * ((outs + ob - 1) / ob);
       const long long waves = (blocks + slots - 1) / slots;
       const long long rounds = (rbar + rg * 8 - 1) / (rg * 8);
-      const long long cost = waves * (1 + rounds);
+      const long long cost = waves * (3 + rounds);
       if (best < 0 || cost < best) {
         best = cost;
         pl.comb_groups = rg;

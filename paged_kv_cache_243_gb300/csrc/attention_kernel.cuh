@@ -302,10 +302,16 @@ __device__ __forceinline__ int find_unit(const int* prefix, int num_units, int x
   return lo;
 }
 
-__device__ __forceinline__ int cta_lo(long long c, long long W, long long N) { return (int)(c * W / N); }
+// 32-bit division when the operands fit (the common case), 64-bit otherwise.
+__device__ __forceinline__ long long div_fast(long long a, long long b) {
+  if (((unsigned long long)a | (unsigned long long)b) < (1ull << 32))
+    return (long long)((unsigned)a / (unsigned)b);
+  return a / b;
+}
+__device__ __forceinline__ int cta_lo(long long c, long long W, long long N) { return (int)div_fast(c * W, N); }
 // Largest block c whose range starts at or before chunk x.
 __device__ __forceinline__ int cta_of(long long x, long long W, long long N) {
-  return (int)(((x + 1) * N - 1) / W);
+  return (int)div_fast((x + 1) * N - 1, W);
 }
 
 // The tensor-core variant is held to 3 resident blocks per SM (<= 136 registers)
@@ -1107,7 +1113,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
 // so only the record loads follow the wait.
 constexpr int kCombineThreads = 256;
 template <int D, int GE>
-__global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const AttnParams p) {
   constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
   constexpr int BATCH = 8;    // records in flight per thread
   constexpr int NWC = kCombineThreads / 32;
@@ -1158,17 +1164,23 @@ __global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const 
     s0 = before * p.units_per_b + (long long)hu * nb;
     s1 = s0 + nb;
   }
+  const long long N = p.num_ctas;
+  // the unit's covering blocks (known before the wait for dense calls)
+  auto cover = [&](int& c_first, int& R4) {
+    c_first = cta_of(s0, W, N);
+    R4 = (cta_of(s1 - 1, W, N) - c_first + 1) * kConsumerWarps;
+  };
+  int c_first = 0, R4 = 0;
+  if (!sparse && s0 != s1) cover(c_first, R4);
   pdl_wait();
   pdl_launch_dependents();
   if (sparse) {
     W = __ldcg(p.ws_prefix + p.num_units);
     s0 = __ldcg(p.ws_prefix + u);
     s1 = __ldcg(p.ws_prefix + u + 1);
+    if (s0 != s1) cover(c_first, R4);
   }
   if (s0 == s1) return;   // no chunks: the attention kernel wrote zeros
-  const long long N = p.num_ctas;
-  const int c_first = cta_of(s0, W, N), c_last = cta_of(s1 - 1, W, N);
-  const int R4 = (c_last - c_first + 1) * kConsumerWarps;
   // With at least one chunk per block (W >= N) every covering block wrote its
   // records; otherwise blocks with empty ranges are skipped.
   const bool dense_cover = W >= N;
@@ -1176,8 +1188,9 @@ __global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const 
   const int h = oo / D;
   const float* rec0 = p.ws_wrec + (size_t)(c_first + u) * kConsumerWarps * RS;
   float M = -INFINITY, L = 0.f, A = 0.f;
-  for (int r0 = grp; r0 < R4; r0 += RG * BATCH) {
-    float mc[BATCH], lc[BATCH], ac[BATCH];
+  // BATCH records per load round, two rounds in flight: the next round's loads
+  // are issued before the current one is folded
+  auto load = [&](int r0, float (&mc)[BATCH], float (&lc)[BATCH], float (&ac)[BATCH]) {
 #pragma unroll
     for (int i = 0; i < BATCH; ++i) {
       const int r = r0 + i * RG;
@@ -1188,14 +1201,39 @@ __global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const 
       lc[i] = __ldcg(rr + GE + h);
       ac[i] = __ldcg(rr + HDR + oo);
     }
+  };
+  // merge (m, l, a) states: max first, then independent exponentials
+  auto fold = [&](const float (&mc)[BATCH], const float (&lc)[BATCH], const float (&ac)[BATCH]) {
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) Mb = fmaxf(Mb, mc[i]);
+    if (Mb == -INFINITY) return;
+    float Lb = M == -INFINITY ? 0.f : L * exp2f(M - Mb);
+    float Ab = M == -INFINITY ? 0.f : A * exp2f(M - Mb);
 #pragma unroll
     for (int i = 0; i < BATCH; ++i) {
       if (mc[i] == -INFINITY) continue;   // empty record: its acc is not written
-      const float Mn = fmaxf(M, mc[i]);
-      const float sc = exp2f(M - Mn), f = exp2f(mc[i] - Mn);
-      L = fmaf(L, sc, f * lc[i]);
-      A = fmaf(A, sc, f * ac[i]);
-      M = Mn;
+      const float f = exp2f(mc[i] - Mb);
+      Lb = fmaf(f, lc[i], Lb);
+      Ab = fmaf(f, ac[i], Ab);
+    }
+    M = Mb;
+    L = Lb;
+    A = Ab;
+  };
+  {
+    const int step = RG * BATCH;
+    float m0[BATCH], l0[BATCH], a0[BATCH], m1[BATCH], l1[BATCH], a1[BATCH];
+    int r0 = grp;
+    if (r0 < R4) load(r0, m0, l0, a0);
+    while (r0 < R4) {
+      if (r0 + step < R4) load(r0 + step, m1, l1, a1);
+      fold(m0, l0, a0);
+      r0 += step;
+      if (r0 >= R4) break;
+      if (r0 + step < R4) load(r0 + step, m0, l0, a0);
+      fold(m1, l1, a1);
+      r0 += step;
     }
   }
   if (RG > 1) {
@@ -1204,15 +1242,20 @@ __global__ void __launch_bounds__(kCombineThreads, 3) attn_combine_kernel(const 
     part[2][tid] = A;
     __syncthreads();
     if (grp != 0) return;
-    for (int g = 1; g < RG; ++g) {
-      const float mw = part[0][g * OB + tid];
-      if (mw == -INFINITY) continue;
-      const float Mn = fmaxf(M, mw);
-      const float sc = exp2f(M - Mn), f = exp2f(mw - Mn);
-      L = fmaf(L, sc, f * part[1][g * OB + tid]);
-      A = fmaf(A, sc, f * part[2][g * OB + tid]);
-      M = Mn;
+    float Mx = M;
+    for (int g = 1; g < RG; ++g) Mx = fmaxf(Mx, part[0][g * OB + tid]);
+    float Ls = 0.f, As = 0.f;
+    if (Mx != -INFINITY) {
+      for (int g = 0; g < RG; ++g) {
+        const float mw = part[0][g * OB + tid];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - Mx);
+        Ls = fmaf(f, part[1][g * OB + tid], Ls);
+        As = fmaf(f, part[2][g * OB + tid], As);
+      }
     }
+    L = Ls;
+    A = As;
   }
   if (!active) return;
   const int qh0 = sparse ? hu : hu * p.group;
