@@ -1,7 +1,7 @@
 // Paged decode attention: one persistent launch that splits the whole batch's
-// KV chunks evenly over its thread blocks, streams each chunk into shared
-// memory with 1-D bulk copies (TMA engine), and merges the per-block partial
-// softmax states in the same launch.
+// KV chunks evenly over its thread blocks and streams each chunk into shared
+// memory with 1-D bulk copies (TMA engine), then a small second launch that
+// merges the partial softmax states.
 //
 // What it computes [KV-practice page, section 2.1]: for query head h of
 // sequence b, out = softmax(sm_scale * q . K^T) V over the sequence's cached
@@ -19,25 +19,29 @@
 // number of chunks whatever the sequence lengths are.
 //
 // Inside a block: warp 4 is the producer. Its lanes resolve 32 chunks at a time
-// (unit, block-table lookup, addresses) and lane 0 issues cp.async.bulk copies
-// of the chunk's K rows, V rows and INT8 scales into a ring of shared-memory
-// stages, each guarded by a "full" and an "empty" mbarrier. Warps 0-3 consume
-// chunks round robin; each keeps its own online-softmax state (running max m,
-// sum l, accumulator) per query head, in the log2 domain. When a warp's chunk
-// stream moves to another unit it writes its partial state to the workspace.
+// (unit, block-table lookup, addresses) and up to S of them issue
+// cp.async.bulk copies of the chunks' K rows, V rows and INT8 scales into a
+// ring of S shared-memory stages, each guarded by a "full" and an "empty"
+// mbarrier. Warps 0-3 consume chunks round robin; each keeps its own
+// online-softmax state (running max m, sum l, accumulator) per query head, in
+// the log2 domain, and writes it to a workspace record whenever its chunk
+// stream leaves a unit (an empty record for units of the block's range it did
+// not see).
 //
-// Merge. Each unit's partials sit in workspace slots (block + unit) * 4 + warp.
-// After its warps finish, a block bumps an arrival counter per unit it touched;
-// the block that arrives last merges the unit's partials
-//   M = max m_s,  out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s
-// and resets the counter to zero for the next call.
+// Merge [TinyServe page, section 3.1 phase 4]: attn_combine_kernel, the next
+// launch on the stream, folds for every unit the records of all blocks whose
+// ranges overlap it:
+//   M = max m_s,  out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
 //
-// Lane layouts. Scores: lane = 8 r + j handles token 4 it + r of the chunk and
-// a D/8-wide slice of channels; the 8 lanes of a token reduce their partial
-// dot products with a butterfly that also scatters the G query heads over the
-// lanes (lane j ends with the full score of head j / (8 / G)). Values: lane
-// owns channels [lane * D / 32, (lane + 1) * D / 32) of every token and all G
-// heads. Probabilities move between the two layouts through shared memory.
+// Two consumer variants: CUDA cores (lane layouts below) and, for query-head
+// groups, mma.sync tensor-core tiles (see the tensor-core section).
+// CUDA-core lane layouts. Scores: lane = 8 r + j handles token 4 it + r of the
+// chunk and a D/8-wide slice of channels; the 8 lanes of a token reduce their
+// partial dot products with a butterfly that also scatters the G query heads
+// over the lanes (lane j ends with the full score of head j / (8 / G)).
+// Values: lane owns channels [lane * D / 32, (lane + 1) * D / 32) of every
+// token and all G heads. Probabilities move between the two layouts through
+// shared memory.
 #pragma once
 
 #include "pkv_common.cuh"
