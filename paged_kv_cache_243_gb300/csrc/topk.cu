@@ -2,21 +2,29 @@
 // the direction-aware bounding box, then keep the top-K pages [TinyServe page,
 // section 2.1 (metadata, score) and section 3.1 phases 1-2].
 //
-// One block per (sequence, query head). Phase 1: each warp scores pages
-// (lane-parallel over channels, butterfly sum), keeping the fp32 scores in
-// shared memory. Phase 2: an exact radix select (four 8-bit passes over an
-// order-preserving integer image of the scores) finds the K-th largest score
-// T; pages above T are kept, and of those equal to T the lowest page indices
-// fill the remaining places. Phase 3: a block-wide scan in page order writes
-// the kept pages in ascending order.
+// One cluster of kTopkCluster blocks per (sequence, query head). Phase 1:
+// block r of the cluster scores the r-th quarter of the pages (a warp per
+// page, lane-parallel over channels, butterfly sum) into its shared memory;
+// the leader then gathers the other blocks' scores through distributed shared
+// memory. Scoring is bound by the box bytes, and four blocks per row put every
+// SM to work on them. Phase 2 (leader): an exact radix select (four 8-bit
+// passes over an order-preserving integer image of the scores) finds the K-th
+// largest score T; pages above T are kept, and of those equal to T the lowest
+// page indices fill the remaining places. Phase 3: a block-wide scan in page
+// order writes the kept pages in ascending order.
+#include <cooperative_groups.h>
+
 #include "pkv_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace pkv {
 
 namespace {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkCluster = 4;
 
 // Larger float -> larger unsigned key; NaN is treated as -inf.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -48,7 +56,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkParams p) {
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, D == 64 ? 4 : 3)
+    score_topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint32_t keys[];  // [max pages of a sequence]
   __shared__ int hist[256];
   __shared__ int warp_tot[kTopkWarps];
@@ -56,7 +65,9 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
   pdl_wait();
   pdl_launch_dependents();
 
-  const int bh = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int bh = blockIdx.x / kTopkCluster;
   const int b = bh / p.num_q_heads, h = bh - b * p.num_q_heads;
   const int g = h / p.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -76,26 +87,29 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
     qv[e] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h) * D + lane * PL + e);
     qpos[e] = qv[e] >= 0.f;
   }
-  // The row's block-table entries are staged (coalesced) in the key array first;
+  // this block's pages [pg0, pg1) of the row
+  const int pg0 = (int)((long long)P * rank / kTopkCluster);
+  const int pg1 = (int)((long long)P * (rank + 1) / kTopkCluster);
+  // The block-table entries are staged (coalesced) in the key array first;
   // each page's entry is read before its score overwrites that slot.
-  for (int pg = tid; pg < P; pg += kTopkThreads)
+  for (int pg = pg0 + tid; pg < pg1; pg += kTopkThreads)
     keys[pg] = (uint32_t)p.block_table[(size_t)b * p.max_pages + pg];
   __syncthreads();
   constexpr int UNROLL = 16;   // pages in flight per warp (box loads issued before use)
-  for (int base = warp * UNROLL; base < P; base += kTopkWarps * UNROLL) {
+  for (int base = pg0 + warp * UNROLL; base < pg1; base += kTopkWarps * UNROLL) {
     float part[UNROLL];
     int phys[UNROLL];
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       const int pg = base + k;
-      phys[k] = pg < P ? (int)keys[pg] : -1;
+      phys[k] = pg < pg1 ? (int)keys[pg] : -1;
     }
     __syncwarp();
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       const int pg = base + k;
       part[k] = 0.f;
-      if (pg < P && phys[k] >= 0 && phys[k] < p.num_pages) {
+      if (pg < pg1 && phys[k] >= 0 && phys[k] < p.num_pages) {
         const float* mrow = p.page_meta + (((size_t)phys[k] * p.num_kv_heads + g) * 2) * D + lane * PL;
         float mn[PL], mx[PL];
         if constexpr (PL == 4) {
@@ -124,7 +138,7 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) {
         const int pg = base + k;
-        if (pg >= P) break;
+        if (pg >= pg1) break;
         float s = part[k];
         if (phys[k] < 0 || phys[k] >= p.num_pages) {
           flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
@@ -135,11 +149,22 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const TopkPara
       }
     }
   }
-  if (p.scores_out) {
+  if (p.scores_out && rank == 0) {
     for (int pg = P + tid; pg < p.max_pages; pg += kTopkThreads)
       p.scores_out[((size_t)b * p.num_q_heads + h) * p.max_pages + pg] = -INFINITY;
   }
-  __syncthreads();
+  // every score of the row now sits in the cluster's shared memory; the leader
+  // copies the other blocks' parts, which stay resident until it is done
+  cluster.sync();
+  if (rank == 0) {
+    for (int r = 1; r < kTopkCluster; ++r) {
+      const uint32_t* remote = cluster.map_shared_rank(keys, r);
+      const int a0 = (int)((long long)P * r / kTopkCluster), a1 = (int)((long long)P * (r + 1) / kTopkCluster);
+      for (int i = a0 + tid; i < a1; i += kTopkThreads) keys[i] = remote[i];
+    }
+  }
+  cluster.sync();
+  if (rank != 0) return;
 
   int32_t* sel = p.sel_pages + ((size_t)b * p.num_q_heads + h) * p.top_k;
   if (tid == 0) p.sel_count[(size_t)b * p.num_q_heads + h] = K;
@@ -245,7 +270,7 @@ pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
-  const unsigned grid = (unsigned)(p.batch * p.num_q_heads);
+  const unsigned grid = (unsigned)(p.batch * p.num_q_heads * kTopkCluster);
   TopkParams pc = p;
   void* args[] = {&pc};
   if (launch_pdl(fn, dim3(grid), dim3(kTopkThreads), smem, st, args) != cudaSuccess) return PKV_ERR_CUDA;
