@@ -206,16 +206,25 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   if (num_splits > 0) {
     pl.ctas = num_splits;
   } else {
+    // CUDA-core consumers on 8 KB chunks (fp16/bf16, d = 128) keep the HBM
+    // busy with 2 blocks (16 stages) per SM, and fewer blocks mean fewer
+    // partial records and a shorter merge (W2: 28.8 -> 28.0 us, dense 32K
+    // -2.6 %). Smaller chunks and the tensor-core consumers want 3.
+    auto blocks_per_sm = [&](const void* fn, bool mma, int& nb) {
+      pkv_status r = prepare_kernel(fn, kAttnThreads, smem, nb);
+      int cap = env_int("PKV_ATTN_CTAS_PER_SM", 0);
+      if (cap <= 0 && !mma && stage >= 8192) cap = 2;
+      if (cap > 0 && cap < nb) nb = cap;
+      return r;
+    };
     int nb = 0;
-    st = prepare_kernel(pl.fn, kAttnThreads, smem, nb);
+    st = blocks_per_sm(pl.fn, pl.mma, nb);
     if (st != PKV_OK) return st;
     if (q_dtype < 0 && pl.ge >= 2) {   // the tensor-core variant may fit more blocks
       int nb2 = 0;
       const void* f2 = attn_kernel(kind, c->head_dim, pl.ge, true);
-      if (f2 && prepare_kernel(f2, kAttnThreads, smem, nb2) == PKV_OK && nb2 > nb) nb = nb2;
+      if (f2 && blocks_per_sm(f2, true, nb2) == PKV_OK && nb2 > nb) nb = nb2;
     }
-    const int cap = env_int("PKV_ATTN_CTAS_PER_SM", 0);
-    if (cap > 0 && cap < nb) nb = cap;
     pl.ctas = di.sms * nb;
   }
   // Combine layout: about 4 (blocks per unit + 1) records per unit; more
