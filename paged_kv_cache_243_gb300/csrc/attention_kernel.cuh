@@ -806,6 +806,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   constexpr int KS = D / 16;                  // k-steps of q.K^T
   constexpr int MT = D / 16;                  // m-tiles of P.V
   constexpr int DPT = D / 8;                  // channels per thread group in P.V
+  // With G <= 4 the hi and lo parts of P fill the 8 columns of one P.V MMA
+  // (columns [0, G) hi, [G, 2G) lo), halving the P.V tensor work; the lo
+  // columns are added to the hi ones at flush.
+  constexpr bool PACK = GE <= 4;
   const int g = lane >> 2, t = lane & 3;
   float* pb = pbuf_all + warp * PBUF;
   auto chan = [&](int i) { return (t + 4 * (i / E)) * E + (i % E); };
@@ -828,6 +832,12 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   auto flush = [&](int u) {
     if (early) pdl_wait();
     float* rec = rec_of(u);
+    if constexpr (PACK) {   // lo columns (threads t + G/2) into the hi ones
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][e] += __shfl_down_sync(0xffffffffu, acc[mt][e], GE / 2);
+    }
     // l and the zero-point sum are kept per lane (tokens g, g + 8); sum the 8
     // lanes of each head here instead of on every chunk
 #pragma unroll
@@ -1006,21 +1016,33 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       pb[(2 * t) * kChunk + g + 8] = pw[2];
       pb[(2 * t + 1) * kChunk + g + 8] = pw[3];
       __syncwarp();
-      float4 pv4 = *reinterpret_cast<const float4*>(pb + g * kChunk + 4 * t);   // head g, tokens 4t..4t+3
+      // B column g: head g (hi part), or with PACK the lo part of head g - GE
+      const int hb = (PACK && g >= GE) ? g - GE : g;
+      float4 pv4 = *reinterpret_cast<const float4*>(pb + (hb < GE ? hb : 0) * kChunk + 4 * t);   // tokens 4t..4t+3
       __syncwarp();
-      if (g >= GE) pv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g >= (PACK ? 2 * GE : GE)) pv4 = make_float4(0.f, 0.f, 0.f, 0.f);
       uint32_t bh0, bl0, bh1, bl1;
       split_hi_lo<BF>(pv4.x, pv4.y, bh0, bl0);
       split_hi_lo<BF>(pv4.z, pv4.w, bh1, bl1);
+      if (PACK && g >= GE) {
+        bh0 = bl0;
+        bh1 = bl1;
+      }
       // ---- P.V on the tensor cores. The accumulator is rescaled only when
       // the running max of some head of the warp grew on this chunk.
       if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+        float a0 = al[0], a1 = al[1];
+        if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
+          const int src = t >= GE / 2 ? lane - GE / 2 : lane;
+          a0 = __shfl_sync(0xffffffffu, al[0], src);
+          a1 = __shfl_sync(0xffffffffu, al[1], src);
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          acc[mt][0] *= al[0];
-          acc[mt][2] *= al[0];
-          acc[mt][1] *= al[1];
-          acc[mt][3] *= al[1];
+          acc[mt][0] *= a0;
+          acc[mt][2] *= a0;
+          acc[mt][1] *= a1;
+          acc[mt][3] *= a1;
         }
       }
       const uint8_t* vrow = st + KB;
@@ -1050,7 +1072,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
           const uint32_t a0 = u8x2_to_h2_biased(t01, 0x4140u), a1 = u8x2_to_h2_biased(t01, 0x4342u);
           const uint32_t a2 = u8x2_to_h2_biased(t23, 0x4140u), a3 = u8x2_to_h2_biased(t23, 0x4342u);
           mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
-          mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       } else {
         // fp16 / bf16: dims [g DPT, (g+1) DPT) of tokens 4t .. 4t+3 (2 DPT bytes per row)
@@ -1079,7 +1101,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
           const uint32_t a2 = __byte_perm(rw[2][mt], rw[3][mt], 0x5410u);
           const uint32_t a3 = __byte_perm(rw[2][mt], rw[3][mt], 0x7632u);
           mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
-          mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       }
     }
