@@ -181,9 +181,7 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  * dequantised in the kernel. Dense mode attends over tokens [0, seq_lens[b]).
  * Sparse mode (sel_pages != NULL) attends over the tokens of the logical pages
  * sel_pages[b][h][0 .. sel_count[b][h]) of each query head, softmax
- * renormalised over them [TinyServe page, section 3.1 phase 3]; the list must
- * be ascending for the work estimate to be exact (any order gives the same
- * result).
+ * renormalised over them [TinyServe page, section 3.1 phase 3], in any order.
  *   q           : [batch][num_q_heads][head_dim] of q_dtype (F16/BF16/F32).
  *   sel_stride  : row length of sel_pages (its top_k); ignored in dense mode.
  *   out         : [batch][num_q_heads][head_dim] of out_dtype (F32/F16/BF16).

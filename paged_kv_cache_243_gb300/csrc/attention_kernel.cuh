@@ -391,15 +391,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     } else {
       int cnt = p.sel_count[b * p.num_q_heads + hu];
       cnt = cnt < 0 ? 0 : (cnt > p.sel_stride ? p.sel_stride : cnt);
-      if (cnt == 0) {
-        n = 0;
-      } else {
-        const int cpp = ps / kChunk;
-        const int last = p.sel_pages[(size_t)(b * p.num_q_heads + hu) * p.sel_stride + cnt - 1];
-        const int P = (L + ps - 1) / ps;
-        const int lastc = (last >= 0 && last == P - 1) ? (L - last * ps + kChunk - 1) / kChunk : cpp;
-        n = (cnt - 1) * cpp + lastc;
-      }
+      // every selected page counts as full: a partial last page only adds
+      // chunks past the sequence end, which are skipped, and the count needs
+      // no dependent load of the page list
+      n = cnt * (ps / kChunk);
     }
     prefix[u] = n;
     my_sum += n;
