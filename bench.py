@@ -329,11 +329,12 @@ class Replica:
 
     def launches_per_replay(self, append=True, attention=True, sparse=False) -> int:
         """Kernels of libpkv launched by one replay (append: one quantise/copy kernel,
-        plus the bounding-box kernel when the cache keeps page metadata)."""
+        plus the bounding-box kernel when the cache keeps page metadata; attention:
+        the attention kernel and its combine kernel)."""
         per_layer = 0
         if append:
             per_layer += 1 + (1 if self.caches[0].page_meta is not None else 0)
-        per_layer += (1 if sparse else 0) + (1 if attention else 0)
+        per_layer += (1 if sparse else 0) + (2 if attention else 0)
         return self.steps_per_replay * self.layers * per_layer
 
 
