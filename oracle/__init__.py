@@ -28,6 +28,6 @@ from .attention import (  # noqa: F401
     split_partials, combine_partials,
 )
 from .sparse import (  # noqa: F401
-    page_bounding_boxes, page_scores, select_top_k, top_k_count,
+    page_bounding_boxes, page_scores, group_page_scores, select_top_k, top_k_count,
 )
 from .sizes import kv_cache_bytes, blocks_needed  # noqa: F401

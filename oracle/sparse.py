@@ -62,6 +62,36 @@ def page_scores(q, mn, mx, group: int) -> np.ndarray:
     return r
 
 
+def group_page_scores(r, group: int, mode: str) -> np.ndarray:
+    """Page scores of each kv head's query-head group, for a selection shared by
+    the group (so the group's K/V pages are read once for its G query heads).
+
+    r: [Hq][P] per-query-head scores (page_scores); query heads g*G .. g*G+G-1
+    share kv head g. mode "sum": the sum of the group's G scores; mode "max":
+    their maximum. Returns [Hkv][P], fp64.
+
+    The pages score one query per page [TinyServe page, section 2.1] and say
+    nothing of query-head groups; these two reductions are the readings taken
+    (each is an upper bound of the matching query-key products: "max" bounds
+    every head's q . k on the page, "sum" bounds (sum of the heads' q) . k).
+    """
+    r = np.asarray(r, dtype=np.float64)
+    Hq, P = r.shape
+    out = np.empty((Hq // group, P), dtype=np.float64)
+    for g in range(Hq // group):
+        rows = [r[g * group + j] for j in range(group)]
+        acc = rows[0].copy()
+        for row in rows[1:]:
+            if mode == "sum":
+                acc = acc + row
+            elif mode == "max":
+                acc = np.maximum(acc, row)
+            else:
+                raise ValueError(mode)
+        out[g] = acc
+    return out
+
+
 def top_k_count(ratio_or_k, num_pages: int) -> int:
     """Number of pages kept: an int is taken as K, a float as ceil(ratio * P); clipped to P."""
     if isinstance(ratio_or_k, float):

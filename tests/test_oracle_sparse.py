@@ -84,3 +84,36 @@ def test_top_k_count():
     assert oracle.top_k_count(0.3, 1) == 1
     assert oracle.top_k_count(1024, 1000) == 1000
     assert oracle.top_k_count(0.3, 0) == 0
+
+
+def test_group_scores_hand_example():
+    # two query heads sharing one kv head
+    r = np.array([[1.0, 5.0, -2.0], [3.0, -2.0, -1.0]])
+    assert np.array_equal(oracle.group_page_scores(r, 2, "sum"), [[4.0, 3.0, -3.0]])
+    assert np.array_equal(oracle.group_page_scores(r, 2, "max"), [[3.0, 5.0, -1.0]])
+    # group of one: the per-head scores themselves
+    assert np.array_equal(oracle.group_page_scores(r, 1, "sum"), r)
+    assert np.array_equal(oracle.group_page_scores(r, 1, "max"), r)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_group_scores_bound_the_group_products(seed):
+    # "max" bounds q_h . k for every head of the group and key of the page;
+    # "sum" bounds (sum of the group's q) . k, brute force over the keys
+    rng = np.random.default_rng(seed)
+    G, Hkv, d, ps, L = 4, 2, 8, 4, 23
+    keys = rng.standard_normal((L, Hkv, d)).astype(np.float32)
+    q = rng.standard_normal((G * Hkv, d))
+    mn, mx = oracle.page_bounding_boxes(keys, ps)
+    r = oracle.page_scores(q, mn, mx, G)
+    smax = oracle.group_page_scores(r, G, "max")
+    ssum = oracle.group_page_scores(r, G, "sum")
+    P = mn.shape[0]
+    for g in range(Hkv):
+        qs = q[g * G:(g + 1) * G]
+        for p in range(P):
+            blk = keys[p * ps:min(L, (p + 1) * ps), g].astype(np.float64)
+            assert smax[g, p] >= (qs @ blk.T).max() - 1e-12
+            assert ssum[g, p] >= (qs.sum(0) @ blk.T).max() - 1e-12
+            # and the sum is never below any single head's bound
+            assert ssum[g, p] <= G * smax[g, p] + 1e-12
