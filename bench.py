@@ -84,13 +84,15 @@ def reduce_sum(value: float, world: int, device=None) -> float:
 
 
 def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 1,
-                      sparse_pages: Optional[int] = None, out_bytes: int = 2) -> Dict[str, int]:
+                      sparse_pages: Optional[int] = None, out_bytes: int = 2,
+                      group_shared: bool = False) -> Dict[str, int]:
     """Bytes one layer's decode step must move (no padding, no re-reads).
 
     attention: K and V of every attended token (codes or fp16/bf16 values) plus
     INT8 scales/zero-points, the queries, the output and block-table entries;
     append: the new tokens read and written (codes + scales when INT8);
     score: the page bounding boxes read by the page scoring (sparse mode).
+    group_shared: one page list per kv head, read once for its query-head group.
     """
     H, d, Hq = w.num_kv_heads, w.head_dim, w.num_q_heads
     esz = 1 if w.quant != "none" else 2
@@ -99,9 +101,9 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
         toks = lens.astype(np.int64)
         units = H
     else:
-        # each query head reads its own selected pages
+        # each query head reads its own selected pages (or each group its list)
         toks = np.minimum(lens.astype(np.int64), sparse_pages * ps)
-        units = Hq
+        units = H if group_shared else Hq
     per_tok = 2 * d * esz
     if w.quant == "per_token":
         per_tok += 16
@@ -122,7 +124,8 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
             dst = w.batch * H * 2 * (64 * d + 8) + w.batch * H * 2 * 64 * d * 4  # open group + tail
         res["append"] = src + dst
     if sparse_pages is not None:
-        res["score"] = int(pages.sum()) * Hq * 2 * d * 4 + w.batch * Hq * sparse_pages * 4
+        rows = H if group_shared else Hq
+        res["score"] = int(pages.sum()) * rows * 2 * d * 4 + w.batch * rows * sparse_pages * 4
     res["total"] = sum(res.values())
     return res
 
@@ -220,13 +223,14 @@ class Replica:
     """One workload's caches, inputs and captured CUDA graphs on this GPU."""
 
     def __init__(self, w: synth.Workload, seed: int, layers: Optional[int] = None,
-                 with_meta: bool = False, top_k: Optional[int] = None):
+                 with_meta: bool = False, top_k: Optional[int] = None, group_mode: int = 0):
         import torch
         from paged_kv_cache_243_gb300.cache import PagedKVCache
         self.torch = torch
         self.w = w
         self.layers = layers or w.layers
         self.top_k = top_k
+        self.group_mode = group_mode   # 0: page lists per query head; 1/2: per kv head (sum / max)
         dev = torch.device("cuda")
         gen = torch.Generator(device=dev)
         gen.manual_seed(seed)
@@ -286,8 +290,9 @@ class Replica:
         self.pos_list = [torch.from_numpy((base + s).astype(np.int32)).to(dev) for s in range(steps)]
         self.len_list = [torch.from_numpy((base + s + 1).astype(np.int32)).to(dev) for s in range(steps)]
         if top_k is not None:
-            self.sel = [torch.empty((B, Hq, top_k), dtype=torch.int32, device=dev) for _ in range(self.layers)]
-            self.cnt = [torch.empty((B, Hq), dtype=torch.int32, device=dev) for _ in range(self.layers)]
+            R = Hq if group_mode == 0 else H
+            self.sel = [torch.empty((B, R, top_k), dtype=torch.int32, device=dev) for _ in range(self.layers)]
+            self.cnt = [torch.empty((B, R), dtype=torch.int32, device=dev) for _ in range(self.layers)]
         torch.cuda.synchronize()
         self.steps_per_replay = steps
 
@@ -298,7 +303,7 @@ class Replica:
                      dev_status=self.status, stream=stream)
         if sparse:
             c.score_topk(self.qs[i], self.bts[i], self.len_list[s], self.top_k, dev_status=self.status,
-                         sel=self.sel[i], count=self.cnt[i], stream=stream)
+                         sel=self.sel[i], count=self.cnt[i], stream=stream, group_mode=self.group_mode)
         if attention:
             # early start: after this step's append, the kernel before the
             # attention writes only the new token's rows (fresh_rows = 1); after
@@ -307,6 +312,7 @@ class Replica:
             fresh = -1 if (sparse or not EARLY_START) else (1 if append else 0)
             c.attention(self.qs[i], self.bts[i], self.len_list[s], sm_scale=self.w.sm_scale,
                         sel=self.sel[i] if sparse else None, sel_count=self.cnt[i] if sparse else None,
+                        sel_shared=sparse and self.group_mode != 0,
                         out=self.outs[i], dev_status=self.status, stream=stream, fresh_rows=fresh)
 
     def capture(self, append=True, attention=True, sparse=False):
@@ -401,6 +407,24 @@ def extra_workloads(peak: float) -> Dict:
                  "dense_gb_s": round(bd["attention"] / (ms_d * 1e-3) / 1e9, 1),
                  "sparse_speedup_vs_dense": round(ms_d / ms_s, 3),
                  "context_pages_14.2_to_4.8ms_A100": "pages' figure, context only"})
+    del rep
+    torch.cuda.empty_cache()
+    # W6: GQA per-token INT8 with one page list per kv head (sum of the group's
+    # scores), so the group's K/V pages are read once
+    w = synth.WORKLOADS["w6_gqa_sparse_int8"]
+    P = w.seq_len // w.page_size
+    K = int(math.ceil(w.top_k_ratio * P))
+    rep = Replica(w, w.seed, with_meta=True, top_k=K, group_mode=1)
+    gs, _ = rep.capture(append=False, attention=True, sparse=True)
+    ms_s = time_graph(gs, 30, 3)
+    gd, _ = rep.capture(append=False, attention=True, sparse=False)
+    ms_d = time_graph(gd, 30, 3)
+    bs = algorithmic_bytes(w, rep.lens, append_tokens=0, sparse_pages=K, group_shared=True)
+    bd = algorithmic_bytes(w, rep.lens, append_tokens=0)
+    entry("w6_gqa_sparse_int8", w, ms_s, bs["total"], 1,
+          extra={"top_k": K, "selection": "group sum", "dense_us": round(ms_d * 1e3, 2),
+                 "dense_gb_s": round(bd["attention"] / (ms_d * 1e-3) / 1e9, 1),
+                 "sparse_speedup_vs_dense": round(ms_d / ms_s, 3)})
     del rep
     torch.cuda.empty_cache()
     return res

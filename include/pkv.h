@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 typedef enum {
   PKV_OK = 0,
@@ -59,6 +59,14 @@ typedef enum {
 #define PKV_DEV_BAD_CONFIG 16   /* launch parameters a kernel refuses to run with */
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2, PKV_I8 = 3 } pkv_dtype;
+
+/* Who selects pages in pkv_page_score_topk. The pages score one query per page;
+ * the group modes are this library's readings for query-head groups (GQA). */
+typedef enum {
+  PKV_SELECT_PER_HEAD = 0,   /* every query head selects its own pages */
+  PKV_SELECT_GROUP_SUM = 1,  /* one list per kv head: the sum of its G heads' scores */
+  PKV_SELECT_GROUP_MAX = 2   /* one list per kv head: the max of its G heads' scores */
+} pkv_select_mode;
 
 typedef enum {
   PKV_QUANT_NONE = 0,       /* kv_dtype F16 or BF16: values stored as is */
@@ -147,29 +155,33 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new,
  * page_score_topk — relevance of every page of every sequence to each query
  * head, and the top-K pages [TinyServe page, sections 2.1 and 3.1 phases 1-2]:
  *   r(q, page) = sum_i (q_i >= 0 ? q_i * max_i : q_i * min_i)      (fp32)
- * Query head h uses kv head h / (num_q_heads / num_kv_heads); each query head
- * selects on its own. K = min(top_k, pages of the sequence); ties go to the
+ * Query head h uses kv head h / G (G = num_q_heads / num_kv_heads). A "row" is
+ * what selects: each query head (group_mode PKV_SELECT_PER_HEAD, R = num_q_heads
+ * rows per sequence), or each kv head with the sum or the max of its G heads'
+ * scores (PKV_SELECT_GROUP_SUM / _MAX, R = num_kv_heads), so that the group
+ * reads one page list. K = min(top_k, pages of the sequence); ties go to the
  * lower logical page index; the kept pages are written in ascending order.
  *   q          : [batch][num_q_heads][head_dim] of q_dtype (F16/BF16/F32).
  *   seq_lens   : int32 [batch]; sequence b has ceil(seq_lens[b] / page_size) pages.
- *   sel_pages  : int32 [batch][num_q_heads][top_k] (entries past sel_count are -1).
- *   sel_count  : int32 [batch][num_q_heads].
- *   scores_out : fp32 [batch][num_q_heads][max_pages] or NULL; entries past the
- *                sequence's pages are -inf.
+ *   sel_pages  : int32 [batch][R][top_k] (entries past sel_count are -1).
+ *   sel_count  : int32 [batch][R].
+ *   scores_out : fp32 [batch][R][max_pages] or NULL (the row's scores); entries
+ *                past the sequence's pages are -inf.
  * Needs cache->page_meta. Pages per sequence are limited to 16384.
  * Device errors: PKV_DEV_BAD_PAGE (that page scores -inf).
  */
 pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                const void* q, pkv_dtype q_dtype,
                                const int32_t* block_table, int32_t max_pages,
-                               const int32_t* seq_lens, int32_t top_k,
+                               const int32_t* seq_lens, int32_t top_k, int32_t group_mode,
                                int32_t* sel_pages, int32_t* sel_count, float* scores_out,
                                int32_t* dev_status, void* stream);
 
 /*
  * Workspace bytes needed by pkv_paged_decode_attention for these shapes.
- * sparse != 0 sizes for the selected-pages mode. num_splits as in the call
- * (0 = automatic, which queries the current device). Returns 0 on bad input.
+ * sparse: 0 dense, 1 page lists per query head, 2 page lists shared by each
+ * kv head's group (sel_shared). num_splits as in the call (0 = automatic,
+ * which queries the current device). Returns 0 on bad input.
  */
 size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                      int32_t sparse, int32_t num_splits);
@@ -180,10 +192,14 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  * h / G (G = num_q_heads / num_kv_heads), read through the block table and
  * dequantised in the kernel. Dense mode attends over tokens [0, seq_lens[b]).
  * Sparse mode (sel_pages != NULL) attends over the tokens of the logical pages
- * sel_pages[b][h][0 .. sel_count[b][h]) of each query head, softmax
- * renormalised over them [TinyServe page, section 3.1 phase 3], in any order.
+ * sel_pages[b][r][0 .. sel_count[b][r]) of row r, softmax renormalised over
+ * them [TinyServe page, section 3.1 phase 3], in any order. With sel_shared = 0
+ * a row is a query head (r = h, lists from PKV_SELECT_PER_HEAD); with
+ * sel_shared = 1 a row is a kv head whose G query heads share its list (r =
+ * h / G, lists from a group mode), and the group's K/V are read once.
  *   q           : [batch][num_q_heads][head_dim] of q_dtype (F16/BF16/F32).
  *   sel_stride  : row length of sel_pages (its top_k); ignored in dense mode.
+ *   sel_shared  : 0 or 1, as above; ignored in dense mode.
  *   out         : [batch][num_q_heads][head_dim] of out_dtype (F32/F16/BF16).
  *   num_splits  : number of cooperating thread blocks that share the work
  *                 (split-K over the whole batch's pages, each block taking an
@@ -225,7 +241,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       const int32_t* block_table, int32_t max_pages,
                                       const int32_t* seq_lens,
                                       const int32_t* sel_pages, const int32_t* sel_count,
-                                      int32_t sel_stride,
+                                      int32_t sel_stride, int32_t sel_shared,
                                       void* out, pkv_dtype out_dtype, int32_t num_splits,
                                       int32_t fresh_rows, void* workspace, size_t workspace_bytes,
                                       int32_t* dev_status, void* stream);
@@ -255,8 +271,9 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t ba
                                               float sm_scale, const int32_t* block_table,
                                               int32_t max_pages, const int32_t* seq_lens,
                                               const int32_t* sel_pages, const int32_t* sel_count,
-                                              int32_t sel_stride, void* out, pkv_dtype out_dtype,
-                                              int32_t num_splits, int32_t* dev_status, void* stream);
+                                              int32_t sel_stride, int32_t sel_shared, void* out,
+                                              pkv_dtype out_dtype, int32_t num_splits,
+                                              int32_t* dev_status, void* stream);
 
 /*
  * Host page allocator [HBM-layout page, section 三 allocate_blocks /

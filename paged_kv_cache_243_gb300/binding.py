@@ -17,6 +17,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 # pkv_dtype / pkv_quant / status values of include/pkv.h
 F16, BF16, F32, I8 = 0, 1, 2, 3
 QUANT_NONE, QUANT_PER_TOKEN, QUANT_PER_GROUP64 = 0, 1, 2
+SELECT_PER_HEAD, SELECT_GROUP_SUM, SELECT_GROUP_MAX = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_PAGES, ERR_CUDA, ERR_WORKSPACE = range(6)
 DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_BAD_CONFIG = 1, 2, 4, 8, 16
 
@@ -67,12 +68,12 @@ def lib() -> ctypes.CDLL:
         "pkv_status_string": (ctypes.c_char_p, [c_int]),
         "pkv_abi_version": (i32, []),
         "pkv_kv_append": (c_int, [P, i32, i32, vp, vp, c_int, vp, i32, vp, vp, vp, vp]),
-        "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, vp, vp, vp, vp, vp]),
+        "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, i32, vp, vp, vp, vp, vp]),
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp, vp,
-                                               i32, vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
+                                               i32, i32, vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
         "pkv_paged_decode_attention_noalloc": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp,
-                                                       vp, i32, vp, c_int, i32, vp, vp]),
+                                                       vp, i32, i32, vp, c_int, i32, vp, vp]),
         "pkv_alloc_create": (c_int, [i32, POINTER(c_void_p)]),
         "pkv_alloc_destroy": (None, [vp]),
         "pkv_alloc_reserve": (c_int, [vp, i64, i32, i32, vp, i32]),
@@ -112,17 +113,20 @@ def kv_append(cache: PkvCache, batch: int, t_new: int, k_new: int, v_new: int, s
 
 def page_score_topk(cache: PkvCache, batch: int, num_q_heads: int, q: int, q_dtype: int,
                     block_table: int, max_pages: int, seq_lens: int, top_k: int, sel_pages: int,
-                    sel_count: int, scores_out: int, dev_status: int, stream: int) -> None:
+                    sel_count: int, scores_out: int, dev_status: int, stream: int,
+                    group_mode: int = SELECT_PER_HEAD) -> None:
+    """group_mode comes last here (keyword) and goes after top_k in the C call."""
     _check(lib().pkv_page_score_topk(ctypes.byref(cache), batch, num_q_heads, q, q_dtype,
-                                     block_table, max_pages, seq_lens, top_k, sel_pages, sel_count,
-                                     scores_out or None, dev_status or None, stream or None),
+                                     block_table, max_pages, seq_lens, top_k, group_mode, sel_pages,
+                                     sel_count, scores_out or None, dev_status or None, stream or None),
            "page_score_topk")
 
 
-def attention_workspace_bytes(cache: PkvCache, batch: int, num_q_heads: int, sparse: bool,
+def attention_workspace_bytes(cache: PkvCache, batch: int, num_q_heads: int, sparse: int,
                               num_splits: int) -> int:
-    n = lib().pkv_attention_workspace_bytes(ctypes.byref(cache), batch, num_q_heads,
-                                            1 if sparse else 0, num_splits)
+    """sparse: 0 dense, 1 page lists per query head, 2 lists shared by each group."""
+    n = lib().pkv_attention_workspace_bytes(ctypes.byref(cache), batch, num_q_heads, int(sparse),
+                                            num_splits)
     if n == 0:
         raise PkvError(ERR_INVALID_ARG, "attention_workspace_bytes")
     return n
@@ -132,13 +136,14 @@ def paged_decode_attention(cache: PkvCache, batch: int, num_q_heads: int, q: int
                            sm_scale: float, block_table: int, max_pages: int, seq_lens: int,
                            sel_pages: int, sel_count: int, sel_stride: int, out: int,
                            out_dtype: int, num_splits: int, workspace: int, workspace_bytes: int,
-                           dev_status: int, stream: int, fresh_rows: int = -1) -> None:
-    """fresh_rows comes last here (keyword, default -1: no early start) and
-    goes to its place after num_splits in the C call."""
+                           dev_status: int, stream: int, fresh_rows: int = -1,
+                           sel_shared: int = 0) -> None:
+    """fresh_rows and sel_shared come last here (keywords; defaults: no early
+    start, page lists per query head) and go to their places in the C call."""
     _check(lib().pkv_paged_decode_attention(ctypes.byref(cache), batch, num_q_heads, q, q_dtype,
                                             sm_scale, block_table, max_pages, seq_lens,
-                                            sel_pages or None, sel_count or None, sel_stride, out,
-                                            out_dtype, num_splits, fresh_rows, workspace,
+                                            sel_pages or None, sel_count or None, sel_stride,
+                                            sel_shared, out, out_dtype, num_splits, fresh_rows, workspace,
                                             workspace_bytes, dev_status or None, stream or None),
            "paged_decode_attention")
 
@@ -147,13 +152,13 @@ def paged_decode_attention_noalloc(cache: PkvCache, batch: int, num_q_heads: int
                                    q_dtype: int, sm_scale: float, block_table: int, max_pages: int,
                                    seq_lens: int, sel_pages: int, sel_count: int, sel_stride: int,
                                    out: int, out_dtype: int, num_splits: int, dev_status: int,
-                                   stream: int) -> None:
+                                   stream: int, sel_shared: int = 0) -> None:
     """paged_decode_attention with the library's fixed device scratch instead of a
     caller workspace (for callers that cannot allocate device memory)."""
     _check(lib().pkv_paged_decode_attention_noalloc(
         ctypes.byref(cache), batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages,
-        seq_lens, sel_pages or None, sel_count or None, sel_stride, out, out_dtype, num_splits,
-        dev_status or None, stream or None), "paged_decode_attention_noalloc")
+        seq_lens, sel_pages or None, sel_count or None, sel_stride, sel_shared, out, out_dtype,
+        num_splits, dev_status or None, stream or None), "paged_decode_attention_noalloc")
 
 
 def alloc_create(num_pages: int) -> int:

@@ -114,26 +114,30 @@ class PagedKVCache:
                    top_k: int, want_scores: bool = False, dev_status: Optional[torch.Tensor] = None,
                    sel: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
                    scores: Optional[torch.Tensor] = None,
-                   stream: Optional[torch.cuda.Stream] = None):
-        """Top-K pages per (sequence, query head). Returns (sel [B][Hq][K], count [B][Hq], scores|None)."""
+                   stream: Optional[torch.cuda.Stream] = None, group_mode: int = 0):
+        """Top-K pages per row: per (sequence, query head), or with group_mode 1 / 2
+        (sum / max of the group's scores) per (sequence, kv head). Returns
+        (sel [B][R][K], count [B][R], scores [B][R][max_pages] or None)."""
         _need(q, "q", device=self.device)
         Bsz, Hq = q.shape[0], q.shape[1]
+        R = Hq if group_mode == 0 else self.num_kv_heads
         mp = block_table.shape[1]
         if sel is None:
-            sel = torch.empty((Bsz, Hq, top_k), dtype=torch.int32, device=self.device)
+            sel = torch.empty((Bsz, R, top_k), dtype=torch.int32, device=self.device)
         if count is None:
-            count = torch.empty((Bsz, Hq), dtype=torch.int32, device=self.device)
+            count = torch.empty((Bsz, R), dtype=torch.int32, device=self.device)
         if want_scores and scores is None:
-            scores = torch.empty((Bsz, Hq, mp), dtype=torch.float32, device=self.device)
+            scores = torch.empty((Bsz, R, mp), dtype=torch.float32, device=self.device)
         B.page_score_topk(self._desc, Bsz, Hq, q.data_ptr(), pkv_dtype(q), block_table.data_ptr(),
                           mp, seq_lens.data_ptr(), top_k, sel.data_ptr(), count.data_ptr(),
-                          _ptr(scores), _ptr(dev_status), _stream(stream))
+                          _ptr(scores), _ptr(dev_status), _stream(stream), group_mode=group_mode)
         return sel, count, scores
 
     # --------------------------------------------------------------- attention
-    def workspace(self, batch: int, num_q_heads: int, sparse: bool, num_splits: int) -> torch.Tensor:
-        """Zero-filled workspace of at least the size the library asks for (kept and reused)."""
-        key = (batch, num_q_heads, bool(sparse), num_splits)
+    def workspace(self, batch: int, num_q_heads: int, sparse: int, num_splits: int) -> torch.Tensor:
+        """Zero-filled workspace of at least the size the library asks for (kept and reused).
+        sparse: 0 dense, 1 page lists per query head, 2 lists shared by each group."""
+        key = (batch, num_q_heads, int(sparse), num_splits)
         n = B.attention_workspace_bytes(self._desc, batch, num_q_heads, sparse, num_splits)
         ws = self._ws.get(key)
         if ws is None or ws.numel() < n:
@@ -146,7 +150,8 @@ class PagedKVCache:
                   sel_count: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   out_dtype: torch.dtype = torch.float32, num_splits: int = 0,
                   dev_status: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None, fresh_rows: int = -1) -> torch.Tensor:
+                  stream: Optional[torch.cuda.Stream] = None, fresh_rows: int = -1,
+                  sel_shared: bool = False) -> torch.Tensor:
         """Decode attention for q [B][Hq][d]; dense, or over sel[b][h][:sel_count[b][h]] pages.
 
         fresh_rows >= 0 lets the call start while the kernel launched just before
@@ -163,13 +168,14 @@ class PagedKVCache:
         if out is None:
             out = torch.empty((Bsz, Hq, d), dtype=out_dtype, device=self.device)
         sparse = sel is not None
-        ws = self.workspace(Bsz, Hq, sparse, num_splits)
+        mode = 0 if not sparse else (2 if sel_shared else 1)
+        ws = self.workspace(Bsz, Hq, mode, num_splits)
         B.paged_decode_attention(
             self._desc, Bsz, Hq, q.data_ptr(), pkv_dtype(q), float(sm_scale),
             block_table.data_ptr(), block_table.shape[1], seq_lens.data_ptr(), _ptr(sel),
             _ptr(sel_count), sel.shape[2] if sparse else 0, out.data_ptr(), pkv_dtype(out),
             num_splits, ws.data_ptr(), ws.numel(), _ptr(dev_status), _stream(stream),
-            fresh_rows=fresh_rows)
+            fresh_rows=fresh_rows, sel_shared=1 if (sparse and sel_shared) else 0)
         return out
 
 

@@ -166,16 +166,17 @@ struct AttnPlan {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // q_dtype < 0: size the workspace for whichever kernel variant a call may use.
-pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads, bool sparse,
+// sparse: 0 dense, 1 page lists per query head, 2 one page list per kv head shared by its group.
+pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads, int sparse,
                           int32_t num_splits, int q_dtype, AttnPlan& pl) {
   pkv_status st = check_cache(c, false);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (num_splits < 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / c->num_kv_heads;
-  pl.ge = sparse ? 1 : G;
+  pl.ge = sparse == 1 ? 1 : G;
   if (pl.ge != 1 && pl.ge != 2 && pl.ge != 4 && pl.ge != 8) return PKV_ERR_UNSUPPORTED;
-  pl.units = batch * (sparse ? num_q_heads : c->num_kv_heads);
+  pl.units = batch * (sparse == 1 ? num_q_heads : c->num_kv_heads);
   const int kind = kv_kind(c);
   pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, q_dtype);
   pl.fn = attn_kernel(kind, c->head_dim, pl.ge, pl.mma);
@@ -283,7 +284,8 @@ int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
 size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                      int32_t sparse, int32_t num_splits) {
   AttnPlan pl;
-  if (plan_attention(cache, batch, num_q_heads, sparse != 0, num_splits, -1, pl) != PKV_OK) return 0;
+  if (sparse < 0 || sparse > 2) return 0;
+  if (plan_attention(cache, batch, num_q_heads, sparse, num_splits, -1, pl) != PKV_OK) return 0;
   return pl.ws_bytes;
 }
 
@@ -291,10 +293,10 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       const void* q, pkv_dtype q_dtype, float sm_scale,
                                       const int32_t* block_table, int32_t max_pages,
                                       const int32_t* seq_lens, const int32_t* sel_pages,
-                                      const int32_t* sel_count, int32_t sel_stride, void* out,
-                                      pkv_dtype out_dtype, int32_t num_splits, int32_t fresh_rows,
-                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                      void* stream) {
+                                      const int32_t* sel_count, int32_t sel_stride,
+                                      int32_t sel_shared, void* out, pkv_dtype out_dtype,
+                                      int32_t num_splits, int32_t fresh_rows, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
   pkv_status st = check_cache(cache, true);
   if (st != PKV_OK) return st;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
@@ -305,10 +307,12 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
     return PKV_ERR_INVALID_ARG;
   const bool sparse = sel_pages != nullptr;
   if (sparse && (!sel_count || sel_stride <= 0)) return PKV_ERR_INVALID_ARG;
+  if (sel_shared != 0 && sel_shared != 1) return PKV_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !(sm_scale < 1e30f)) return PKV_ERR_INVALID_ARG;
   if (fresh_rows < -1) return PKV_ERR_INVALID_ARG;
+  const int mode = !sparse ? 0 : (sel_shared ? 2 : 1);
   AttnPlan pl;
-  st = plan_attention(cache, batch, num_q_heads, sparse, num_splits, q_dtype, pl);
+  st = plan_attention(cache, batch, num_q_heads, mode, num_splits, q_dtype, pl);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < pl.ws_bytes)
     return PKV_ERR_WORKSPACE;
@@ -338,7 +342,8 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.batch = batch;
   p.max_pages = max_pages;
   p.sel_stride = sparse ? sel_stride : 0;
-  p.units_per_b = sparse ? num_q_heads : cache->num_kv_heads;
+  p.units_per_b = mode == 1 ? num_q_heads : cache->num_kv_heads;
+  p.unit_is_q = mode == 1;
   p.num_units = pl.units;
   p.num_ctas = pl.ctas;
   p.stages = pl.stages;
@@ -402,14 +407,15 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
 pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                const void* q, pkv_dtype q_dtype, const int32_t* block_table,
                                int32_t max_pages, const int32_t* seq_lens, int32_t top_k,
-                               int32_t* sel_pages, int32_t* sel_count, float* scores_out,
-                               int32_t* dev_status, void* stream) {
+                               int32_t group_mode, int32_t* sel_pages, int32_t* sel_count,
+                               float* scores_out, int32_t* dev_status, void* stream) {
   pkv_status st = check_cache(cache, false);
   if (st != PKV_OK) return st;
   if (!cache->page_meta) return PKV_ERR_INVALID_ARG;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (max_pages <= 0 || top_k < 1) return PKV_ERR_INVALID_ARG;
+  if (group_mode < PKV_SELECT_PER_HEAD || group_mode > PKV_SELECT_GROUP_MAX) return PKV_ERR_INVALID_ARG;
   if (max_pages > 16384) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
   if (!q || !block_table || !seq_lens || !sel_pages || !sel_count) return PKV_ERR_INVALID_ARG;
@@ -432,6 +438,7 @@ pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t nu
   p.max_pages = max_pages;
   p.top_k = top_k;
   p.q_dtype = q_dtype;
+  p.group_mode = group_mode;
   return launch_topk(p, static_cast<cudaStream_t>(stream));
 }
 

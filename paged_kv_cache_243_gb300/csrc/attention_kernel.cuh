@@ -80,6 +80,10 @@ struct AttnParams {
   // while it still runs; see the early-start notes in the kernel.
   int fresh_rows;
   int comb_groups;  // record groups of the combine kernel (1, 2, 4 or 8)
+  // 1: a unit is (sequence, query head) with its own page list (sparse, per
+  // query head); 0: (sequence, kv head) serving the G query heads of its group
+  // (dense, or sparse with one page list shared by the group).
+  int unit_is_q;
 };
 
 struct ChunkInfo {
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     if (!sparse) {
       n = (L + kChunk - 1) / kChunk;
     } else {
-      int cnt = p.sel_count[b * p.num_q_heads + hu];
+      int cnt = p.sel_count[b * p.units_per_b + hu];
       cnt = cnt < 0 ? 0 : (cnt > p.sel_stride ? p.sel_stride : cnt);
       // every selected page counts as full: a partial last page only adds
       // chunks past the sequence end, which are skipped, and the count needs
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       if (prefix[u] != prefix[u + 1]) continue;
       if (early) pdl_wait();
       const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-      const int qh0 = sparse ? hu : hu * p.group;
+      const int qh0 = p.unit_is_q ? hu : hu * p.group;
       for (int i = tid; i < GE * D; i += NW * 32)
         store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + i, 0.f);
     }
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         const int lp = (r.k * kChunk) / ps;
         if (r.k * kChunk < lens[b]) r.phys = p.block_table[(size_t)b * p.max_pages + lp];
       } else {
-        r.sp = p.sel_pages[(size_t)(b * p.num_q_heads + hu) * p.sel_stride + r.k / cpp];
+        r.sp = p.sel_pages[(size_t)(b * p.units_per_b + hu) * p.sel_stride + r.k / cpp];
       }
     };
     auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         t0 = r.k * kChunk;
         g = hu;
       } else {
-        g = hu / p.group;
+        g = p.unit_is_q ? hu / p.group : hu;
         if (r.sp < 0 || (long long)r.sp * ps >= L) {
           flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
           return;
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
 
   auto start_unit = [&](int u) {
     const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-    const int qh0 = sparse ? hu : hu * p.group;
+    const int qh0 = p.unit_is_q ? hu : hu * p.group;
     float part[GE];
 #pragma unroll
     for (int h = 0; h < GE; ++h) {
@@ -863,7 +867,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   };
   auto start_unit = [&](int u) {
     const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-    const int qh0 = hu * p.group;   // dense only on this path
+    const int qh0 = hu * p.group;   // units are (sequence, kv head) on this path
     float part = 0.f;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
         reinterpret_cast<const uint16_t*>(p.q) + ((size_t)b * p.num_q_heads + qh0 + (g < GE ? g : 0)) * D);
@@ -1279,7 +1283,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
     A = As;
   }
   if (!active) return;
-  const int qh0 = sparse ? hu : hu * p.group;
+  const int qh0 = p.unit_is_q ? hu : hu * p.group;
   store_out_elem(p.out, p.out_dtype, ((size_t)b * p.num_q_heads + qh0) * D + o, L > 0.f ? A / L : 0.f);
 }
 

@@ -54,10 +54,11 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t ba
                                               float sm_scale, const int32_t* block_table,
                                               int32_t max_pages, const int32_t* seq_lens,
                                               const int32_t* sel_pages, const int32_t* sel_count,
-                                              int32_t sel_stride, void* out, pkv_dtype out_dtype,
-                                              int32_t num_splits, int32_t* dev_status, void* stream) {
-  const size_t need = pkv_attention_workspace_bytes(cache, batch, num_q_heads, sel_pages != nullptr,
-                                                    num_splits);
+                                              int32_t sel_stride, int32_t sel_shared, void* out,
+                                              pkv_dtype out_dtype, int32_t num_splits,
+                                              int32_t* dev_status, void* stream) {
+  const int32_t mode = sel_pages == nullptr ? 0 : (sel_shared ? 2 : 1);
+  const size_t need = pkv_attention_workspace_bytes(cache, batch, num_q_heads, mode, num_splits);
   if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > pkv::kNoallocScratchBytes) return PKV_ERR_WORKSPACE;
   void* scratch = nullptr;
@@ -65,9 +66,9 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t ba
   if (st != PKV_OK) return st;
   // The workspace needs no initial contents, so nothing is cleared here.
   return pkv_paged_decode_attention(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table,
-                                    max_pages, seq_lens, sel_pages, sel_count, sel_stride, out,
-                                    out_dtype, num_splits, -1, scratch, pkv::kNoallocScratchBytes,
-                                    dev_status, stream);
+                                    max_pages, seq_lens, sel_pages, sel_count, sel_stride, sel_shared,
+                                    out, out_dtype, num_splits, -1, scratch,
+                                    pkv::kNoallocScratchBytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -33,6 +33,7 @@ struct TopkParams {
   int32_t* dev_status;
   int num_pages, page_size, num_kv_heads, head_dim;
   int num_q_heads, group, batch, max_pages, top_k, q_dtype;
+  int group_mode;  // PKV_SELECT_*: rows are query heads, or kv heads (group sum / max)
 };
 
 pkv_status launch_append(const AppendParams& p, cudaStream_t st);

@@ -1,8 +1,11 @@
 // page_score_topk: score every page of a sequence against one query head with
 // the direction-aware bounding box, then keep the top-K pages [TinyServe page,
-// section 2.1 (metadata, score) and section 3.1 phases 1-2].
+// section 2.1 (metadata, score) and section 3.1 phases 1-2]. A row that selects
+// is a query head, or a kv head whose G query heads' scores are summed or
+// maxed (one shared page list per group; a reading, the pages score one query).
 //
-// One cluster of kTopkCluster blocks per (sequence, query head). Phase 1:
+// One cluster of CS blocks per (sequence, row): 4 for a query head, 8 for a
+// kv head's group (G heads to score per page). Phase 1:
 // block r of the cluster scores the r-th quarter of the pages (a warp per
 // page, lane-parallel over channels, butterfly sum) into its shared memory;
 // the leader then gathers the other blocks' scores through distributed shared
@@ -24,7 +27,8 @@ namespace {
 
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkCluster = 4;
+constexpr int kTopkClusterHead = 4;    // rows of one query head
+constexpr int kTopkClusterGroup = 8;   // rows of a query-head group
 
 // Larger float -> larger unsigned key; NaN is treated as -inf.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -55,21 +59,27 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
   return pre + x - v;
 }
 
-template <int D>
-__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, D == 64 ? 4 : 3)
+template <int D, int CS>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kTopkThreads, D == 64 ? 4 : 3)
     score_topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint32_t keys[];  // [max pages of a sequence]
   __shared__ int hist[256];
   __shared__ int warp_tot[kTopkWarps];
   __shared__ int sel_digit, sel_remaining;
+  __shared__ float qsm[8 * D];   // the row's query heads (<= 8)
   pdl_wait();
   pdl_launch_dependents();
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const int bh = blockIdx.x / kTopkCluster;
-  const int b = bh / p.num_q_heads, h = bh - b * p.num_q_heads;
-  const int g = h / p.group;
+  // a row selects: a query head, or a kv head for its group (sum / max)
+  const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
+  const int rows_per_b = grouped ? p.num_kv_heads : p.num_q_heads;
+  const int HR = grouped ? p.group : 1;             // query heads scored per row
+  const int bh = blockIdx.x / CS;                   // row index b * rows_per_b + r
+  const int b = bh / rows_per_b, hr = bh - b * rows_per_b;
+  const int g = grouped ? hr : hr / p.group;        // kv head whose boxes are read
+  const int h0 = grouped ? hr * p.group : hr;       // first query head of the row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.page_size;
   int L = p.seq_lens[b];
@@ -80,94 +90,139 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 
   // ---- phase 1: scores
   constexpr int PL = D / 32;  // channels per lane
-  float qv[PL];
-  bool qpos[PL];
-#pragma unroll
-  for (int e = 0; e < PL; ++e) {
-    qv[e] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h) * D + lane * PL + e);
-    qpos[e] = qv[e] >= 0.f;
-  }
+  for (int i = tid; i < HR * D; i += kTopkThreads)
+    qsm[i] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h0) * D + i);
   // this block's pages [pg0, pg1) of the row
-  const int pg0 = (int)((long long)P * rank / kTopkCluster);
-  const int pg1 = (int)((long long)P * (rank + 1) / kTopkCluster);
+  const int pg0 = (int)((long long)P * rank / CS);
+  const int pg1 = (int)((long long)P * (rank + 1) / CS);
   // The block-table entries are staged (coalesced) in the key array first;
   // each page's entry is read before its score overwrites that slot.
   for (int pg = pg0 + tid; pg < pg1; pg += kTopkThreads)
     keys[pg] = (uint32_t)p.block_table[(size_t)b * p.max_pages + pg];
   __syncthreads();
-  constexpr int UNROLL = 16;   // pages in flight per warp (box loads issued before use)
+  // pages in flight per warp (box loads issued before use); a group's rows
+  // keep fewer pages in flight and score every head of the group from one
+  // load of each box
+  constexpr bool GROUPED = CS == kTopkClusterGroup;
+  constexpr int UNROLL = GROUPED ? 4 : 16;
   for (int base = pg0 + warp * UNROLL; base < pg1; base += kTopkWarps * UNROLL) {
     float part[UNROLL];
-    int phys[UNROLL];
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const int pg = base + k;
-      phys[k] = pg < pg1 ? (int)keys[pg] : -1;
-    }
     __syncwarp();
+    if constexpr (!GROUPED) {
+      // one query head: each page's partial right after its box loads
+      float qv[PL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const int pg = base + k;
-      part[k] = 0.f;
-      if (pg < pg1 && phys[k] >= 0 && phys[k] < p.num_pages) {
-        const float* mrow = p.page_meta + (((size_t)phys[k] * p.num_kv_heads + g) * 2) * D + lane * PL;
-        float mn[PL], mx[PL];
-        if constexpr (PL == 4) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
-          const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
-          mn[0] = a.x; mn[1] = a.y; mn[2] = a.z; mn[3] = a.w;
-          mx[0] = c.x; mx[1] = c.y; mx[2] = c.z; mx[3] = c.w;
-        } else {
-          const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
-          const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
-          mn[0] = a.x; mn[1] = a.y;
-          mx[0] = c.x; mx[1] = c.y;
+      for (int e = 0; e < PL; ++e) qv[e] = qsm[lane * PL + e];
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const int pg = base + k;
+        const int ph = pg < pg1 ? (int)keys[pg] : -1;   // staged table entry
+        part[k] = 0.f;
+        if (ph >= 0 && ph < p.num_pages) {
+          const float* mrow = p.page_meta + (((size_t)ph * p.num_kv_heads + g) * 2) * D + lane * PL;
+          float mn[PL], mx[PL];
+          if constexpr (PL == 4) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
+            const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
+            mn[0] = a.x; mn[1] = a.y; mn[2] = a.z; mn[3] = a.w;
+            mx[0] = c.x; mx[1] = c.y; mx[2] = c.z; mx[3] = c.w;
+          } else {
+            const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
+            const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
+            mn[0] = a.x; mn[1] = a.y;
+            mx[0] = c.x; mx[1] = c.y;
+          }
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < PL; ++e) acc = fmaf(qv[e], qv[e] >= 0.f ? mx[e] : mn[e], acc);
+          part[k] = acc;
         }
-        float s = 0.f;
+      }
 #pragma unroll
-        for (int e = 0; e < PL; ++e) s = fmaf(qv[e], qpos[e] ? mx[e] : mn[e], s);
-        part[k] = s;
+      for (int k = 0; k < UNROLL; ++k)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part[k] += __shfl_xor_sync(0xffffffffu, part[k], off);
+    } else {
+      float mn[UNROLL][PL], mx[UNROLL][PL];
+  #pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const int pg = base + k;
+        const int ph = pg < pg1 ? (int)keys[pg] : -1;   // staged table entry
+  #pragma unroll
+        for (int e = 0; e < PL; ++e) { mn[k][e] = 0.f; mx[k][e] = 0.f; }
+        if (ph >= 0 && ph < p.num_pages) {
+          const float* mrow = p.page_meta + (((size_t)ph * p.num_kv_heads + g) * 2) * D + lane * PL;
+          if constexpr (PL == 4) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
+            const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
+            mn[k][0] = a.x; mn[k][1] = a.y; mn[k][2] = a.z; mn[k][3] = a.w;
+            mx[k][0] = c.x; mx[k][1] = c.y; mx[k][2] = c.z; mx[k][3] = c.w;
+          } else {
+            const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
+            const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
+            mn[k][0] = a.x; mn[k][1] = a.y;
+            mx[k][0] = c.x; mx[k][1] = c.y;
+          }
+        }
+      }
+      // each query head of the row: the pages' lane partials, butterfly sums,
+      // then the row's reduction (one head: itself; a group: sum or max)
+      for (int j = 0; j < HR; ++j) {
+        float qv[PL];
+  #pragma unroll
+        for (int e = 0; e < PL; ++e) qv[e] = qsm[j * D + lane * PL + e];
+        float sj[UNROLL];
+  #pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+          float acc = 0.f;
+  #pragma unroll
+          for (int e = 0; e < PL; ++e) acc = fmaf(qv[e], qv[e] >= 0.f ? mx[k][e] : mn[k][e], acc);
+          sj[k] = acc;
+        }
+  #pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+  #pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sj[k] += __shfl_xor_sync(0xffffffffu, sj[k], off);
+          part[k] = j == 0 ? sj[k] : (p.group_mode == PKV_SELECT_GROUP_MAX ? fmaxf(part[k], sj[k]) : part[k] + sj[k]);
+        }
       }
     }
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part[k] += __shfl_xor_sync(0xffffffffu, part[k], off);
-    }
+    __syncwarp();
     if (lane == 0) {
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) {
         const int pg = base + k;
         if (pg >= pg1) break;
         float s = part[k];
-        if (phys[k] < 0 || phys[k] >= p.num_pages) {
+        const int ph = (int)keys[pg];
+        if (ph < 0 || ph >= p.num_pages) {
           flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
           s = -INFINITY;
         }
         keys[pg] = __float_as_uint(s);
-        if (p.scores_out) p.scores_out[((size_t)b * p.num_q_heads + h) * p.max_pages + pg] = s;
+        if (p.scores_out) p.scores_out[(size_t)bh * p.max_pages + pg] = s;
       }
     }
   }
   if (p.scores_out && rank == 0) {
     for (int pg = P + tid; pg < p.max_pages; pg += kTopkThreads)
-      p.scores_out[((size_t)b * p.num_q_heads + h) * p.max_pages + pg] = -INFINITY;
+      p.scores_out[(size_t)bh * p.max_pages + pg] = -INFINITY;
   }
   // every score of the row now sits in the cluster's shared memory; the leader
   // copies the other blocks' parts, which stay resident until it is done
   cluster.sync();
   if (rank == 0) {
-    for (int r = 1; r < kTopkCluster; ++r) {
+    for (int r = 1; r < CS; ++r) {
       const uint32_t* remote = cluster.map_shared_rank(keys, r);
-      const int a0 = (int)((long long)P * r / kTopkCluster), a1 = (int)((long long)P * (r + 1) / kTopkCluster);
+      const int a0 = (int)((long long)P * r / CS), a1 = (int)((long long)P * (r + 1) / CS);
       for (int i = a0 + tid; i < a1; i += kTopkThreads) keys[i] = remote[i];
     }
   }
   cluster.sync();
   if (rank != 0) return;
 
-  int32_t* sel = p.sel_pages + ((size_t)b * p.num_q_heads + h) * p.top_k;
-  if (tid == 0) p.sel_count[(size_t)b * p.num_q_heads + h] = K;
+  int32_t* sel = p.sel_pages + (size_t)bh * p.top_k;
+  if (tid == 0) p.sel_count[bh] = K;
   for (int i = K + tid; i < p.top_k; i += kTopkThreads) sel[i] = -1;
   if (K == 0) return;
   if (K == P) {
@@ -262,15 +317,23 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 
 pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
   const size_t smem = (size_t)p.max_pages * 4;
-  const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&score_topk_kernel<128>)
-                                     : reinterpret_cast<const void*>(&score_topk_kernel<64>);
+  const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
+  const int cs = grouped ? kTopkClusterGroup : kTopkClusterHead;
+  const void* fn;
+  if (p.head_dim == 128)
+    fn = grouped ? reinterpret_cast<const void*>(&score_topk_kernel<128, kTopkClusterGroup>)
+                 : reinterpret_cast<const void*>(&score_topk_kernel<128, kTopkClusterHead>);
+  else
+    fn = grouped ? reinterpret_cast<const void*>(&score_topk_kernel<64, kTopkClusterGroup>)
+                 : reinterpret_cast<const void*>(&score_topk_kernel<64, kTopkClusterHead>);
   if (smem > 48 * 1024) {
     // always the one maximum (16384 pages), never a per-call size, so a
     // concurrent or later launch with more pages is never left below its need
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
-  const unsigned grid = (unsigned)(p.batch * p.num_q_heads * kTopkCluster);
+  const int rows = p.batch * (grouped ? p.num_kv_heads : p.num_q_heads);
+  const unsigned grid = (unsigned)(rows * cs);
   TopkParams pc = p;
   void* args[] = {&pc};
   if (launch_pdl(fn, dim3(grid), dim3(kTopkThreads), smem, st, args) != cudaSuccess) return PKV_ERR_CUDA;

@@ -106,6 +106,12 @@ WORKLOADS: Dict[str, Workload] = {
         page_offset_std=0.5, top_k_ratio=0.3,
         description="query-aware sparse: B=8, 16 = 16 heads, d=64, L=16384, page 16 "
                     "(1024 pages/seq), per-page K offset ~ N(0, 0.5^2), top-K 30%"),
+    "w6_gqa_sparse_int8": Workload(
+        name="w6_gqa_sparse_int8", seed=1241, batch=8, layers=1, num_q_heads=32, num_kv_heads=8,
+        head_dim=128, page_size=16, dtype="f16", quant="per_token", seq_len=16384,
+        outlier_channels=4, outlier_scale=15.0, page_offset_std=0.5, top_k_ratio=0.3,
+        description="GQA 32/8 per-token INT8 sparse: B=8, d=128, L=16384, page 16, per-page K "
+                    "offset ~ N(0, 0.5^2), top-K 30 % per kv head from the group's summed scores"),
     "dense_32k_bf16": Workload(
         name="dense_32k_bf16", seed=1240, batch=4, layers=1, num_q_heads=32, num_kv_heads=32,
         head_dim=128, page_size=16, dtype="bf16", quant="none", seq_len=32768,

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(B):
 
 
 def test_status_strings_and_version(B):
-    assert B.abi_version() == 2
+    assert B.abi_version() == 3
     assert B.status_string(B.OK) == "ok"
     assert B.status_string(B.ERR_OUT_OF_PAGES) == "out of pages"
 
@@ -82,6 +82,15 @@ def test_argument_checks_before_cuda(B):
     assert e.value.status == B.ERR_INVALID_ARG
     with pytest.raises(B.PkvError) as e:   # scoring needs page metadata
         B.page_score_topk(good, 1, 2, 0x4000, B.F16, 0x5000, 4, 0x6000, 2, 0x9000, 0xA000, 0, 0, 0)
+    assert e.value.status == B.ERR_INVALID_ARG
+    with_meta = _desc(B, page_meta=0xB000)
+    with pytest.raises(B.PkvError) as e:   # unknown selection mode
+        B.page_score_topk(with_meta, 1, 2, 0x4000, B.F16, 0x5000, 4, 0x6000, 2, 0x9000, 0xA000, 0, 0, 0,
+                          group_mode=3)
+    assert e.value.status == B.ERR_INVALID_ARG
+    with pytest.raises(B.PkvError) as e:   # sel_shared must be 0 or 1
+        B.paged_decode_attention(good, 1, 2, 0x4000, B.F16, 0.125, 0x5000, 4, 0x6000, 0x9000, 0xA000, 4,
+                                 0x7000, B.F32, 0, 0x8000, 1 << 20, 0, 0, sel_shared=2)
     assert e.value.status == B.ERR_INVALID_ARG
     with pytest.raises(B.PkvError) as e:   # per-group append without a tail
         B.kv_append(_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000, page_size=64),

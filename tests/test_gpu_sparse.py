@@ -148,3 +148,57 @@ def test_bad_selected_page_is_reported():
     for h in range(4):
         o = oracle.decode_attention_tokens(qf[0, h], ld.seqs[0].k[:16, h], ld.seqs[0].v[:16, h], w.sm_scale)
         assert np.abs(out[0, h] - o).max() <= TOL["f16"]
+
+
+@pytest.mark.parametrize("mode", ["sum", "max"])
+@pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("none", 64, 8, 2, 16, 4), ("per_token", 128, 16, 4, 16, 5),
+                                                     ("none", 128, 8, 1, 32, 3), ("none", 64, 16, 2, 64, 2)])
+def test_group_shared_selection(mode, quant, d, Hq, Hkv, ps, top_k):
+    # one page list per kv head, from the sum or max of its group's scores;
+    # each query head of the group attends over that list
+    from helpers import oracle_kv
+    from paged_kv_cache_243_gb300 import binding as B
+    G = Hq // Hkv
+    w = synth.Workload(name="spg", seed=970 + d + Hq + ps, batch=4, layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_dim=d, page_size=ps, dtype="f16", quant=quant, seq_len=None,
+                       seq_len_range=(1, 400), outlier_channels=4 if quant != "none" else 0,
+                       outlier_scale=15.0, page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([400, 1, 37, 200], dtype=np.int32), with_meta=True)
+    q, qf = queries_dev(w)
+    gm = B.SELECT_GROUP_SUM if mode == "sum" else B.SELECT_GROUP_MAX
+    sel, cnt, scores = ld.cache.score_topk(q, ld.bt_dev, ld.lens_dev, top_k, want_scores=True,
+                                           dev_status=ld.status, group_mode=gm)
+    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, sel=sel, sel_count=cnt,
+                             sel_shared=True, dev_status=ld.status)
+    torch.cuda.synchronize()
+    sel, cnt, scores, out = sel.cpu().numpy(), cnt.cpu().numpy(), scores.cpu().numpy(), out.cpu().numpy()
+    assert sel.shape == (w.batch, Hkv, top_k)
+    for b in range(w.batch):
+        L = int(ld.lens[b])
+        P = -(-L // ps)
+        mn, mx = oracle.page_bounding_boxes(oracle_bbox_keys(w, ld.seqs[b]), ps)
+        r = oracle.page_scores(qf[b], mn, mx, G)
+        rg = oracle.group_page_scores(r, G, mode)
+        k, v = oracle_kv(ld, b)
+        for g in range(Hkv):
+            K = min(top_k, P)
+            assert cnt[b, g] == K
+            per_head = [1e-5 * (np.abs(qf[b, h])[None, :] * np.maximum(np.abs(mn[:, g]), np.abs(mx[:, g]))).sum(1)
+                        for h in range(g * G, (g + 1) * G)]
+            slack = np.sum(per_head, axis=0) + 1e-6
+            assert (np.abs(scores[b, g, :P] - rg[g]) <= slack).all()
+            assert np.isneginf(scores[b, g, P:]).all()
+            want = oracle.select_top_k(rg[g], K)
+            got = sel[b, g, :K]
+            assert (sel[b, g, K:] == -1).all() and (np.diff(got) > 0).all()
+            if not np.array_equal(got, want):
+                srt = np.sort(rg[g])[::-1]
+                kth, nxt = srt[K - 1], srt[K]
+                assert abs(kth - nxt) <= 1e-4 * max(abs(kth), abs(nxt)), (b, g)
+                assert (rg[g][got] >= nxt - slack[got]).all()
+            for h in range(g * G, (g + 1) * G):
+                o = oracle.sparse_decode_attention(qf[b, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], w.sm_scale,
+                                                   [got], ps)[0]
+                tol = TOL["int8"] if quant != "none" else TOL["f16"]
+                assert np.abs(out[b, h] - o).max() <= tol, (b, h)
+    assert int(ld.status.item()) == 0
