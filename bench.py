@@ -359,6 +359,55 @@ def time_graph(g, replays: int, warmup: int) -> float:
     return e0.elapsed_time(e1) / replays
 
 
+def prefill_append(w: synth.Workload, with_meta: bool, peak: float) -> Dict:
+    """One kv_append of the whole context (T = L tokens per sequence) into an
+    empty cache, timed in a CUDA graph; bytes = K/V input read + what is stored."""
+    import torch
+    from paged_kv_cache_243_gb300.cache import PagedKVCache
+    dev = torch.device("cuda")
+    B, H, d, T = w.batch, w.num_kv_heads, w.head_dim, int(synth.seq_lens(w).max())
+    kv_name = "int8" if w.quant != "none" else w.dtype
+    qdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    bt, pool = synth.block_tables(w, 0, 1 if w.append_steps else 0)
+    cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=w.quant, with_meta=with_meta,
+                         tail_rows=B)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed + 7)
+    k = torch.randn((B, T, H, d), generator=gen, device=dev).to(qdt)
+    v = torch.randn((B, T, H, d), generator=gen, device=dev).to(qdt)
+    bt_d = torch.from_numpy(bt).to(dev)
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cache.append(k, v, bt_d, pos, dev_status=status, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cache.append(k, v, bt_d, pos, dev_status=status, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ms = time_graph(g, 10, 3)
+    toks = B * T
+    src = toks * H * d * 2 * 2
+    if w.quant == "none":
+        dst = src
+    elif w.quant == "per_token":
+        dst = toks * H * 2 * (d + 8)
+    else:
+        dst = toks * H * 2 * d + (toks // 64) * H * 2 * 8
+    P = -(-T // w.page_size)
+    if with_meta:
+        dst += B * P * H * 2 * d * 4
+    byts = src + dst
+    gbs = byts / (ms * 1e-3) / 1e9
+    out = {"tokens": toks, "ms": round(ms, 4), "bytes": int(byts), "gb_s": round(gbs, 1),
+           "frac_of_hbm_peak": round(gbs / peak, 4), "with_meta": with_meta,
+           "dev_status": int(status.item())}
+    del cache, k, v
+    return out
+
+
 def extra_workloads(peak: float) -> Dict:
     """Other workloads of the pages, one line each (not the headline)."""
     import torch
@@ -409,6 +458,14 @@ def extra_workloads(peak: float) -> Dict:
                  "context_pages_14.2_to_4.8ms_A100": "pages' figure, context only"})
     del rep
     torch.cuda.empty_cache()
+    # Bulk prefill through kv_append: T tokens per sequence written at positions
+    # 0 .. T-1 in one call (copy, per-token quantise with boxes, per-group
+    # quantise), as GB/s of input read + codes, scales and boxes written
+    for name, with_meta in (("w2_llama7b_bf16", False), ("w6_gqa_sparse_int8", True),
+                            ("w4_long_int8_group", False)):
+        w = synth.WORKLOADS[name]
+        res["prefill_append_" + name] = prefill_append(w, with_meta, peak)
+        torch.cuda.empty_cache()
     # W6: GQA per-token INT8 with one page list per kv head (sum of the group's
     # scores), so the group's K/V pages are read once
     w = synth.WORKLOADS["w6_gqa_sparse_int8"]

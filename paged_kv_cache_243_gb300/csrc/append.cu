@@ -20,11 +20,61 @@ __device__ __forceinline__ float load_src(const void* p, int dtype, size_t i) {
                            : __half2float(reinterpret_cast<const __half*>(p)[i]);
 }
 
-__device__ __forceinline__ int quant_code(float x, float s, float z) {
-  if (s == 0.f) return -128;
-  float u = rintf(__fdiv_rn(__fsub_rn(x, z), s));
-  u = fminf(fmaxf(u, 0.f), 255.f);
-  return (int)u - 128;
+// code = rint((x - z) / s) - 128 with the correctly rounded quotient (the
+// quotient is in [0, 255], so the clamp of the definition never acts).
+// rs = the correctly rounded 1/s (0 when 1/s would not be finite):
+// for quotients in [0, 256), (x - z) * rs is within 255 * 2^-23 of (x - z) / s
+// and the correctly rounded quotient within 2^-17, so rint of either agrees
+// unless the product lies within 1e-3 of a half-integer; there, and when rs
+// is 0, the quotient itself is computed (warp-uniform branch, rarely taken).
+// Rounding to nearest even uses the standard magic-number method: adding
+// 1.5 * 2^23 leaves rint(q) in the low mantissa bits for 0 <= q < 2^22.
+__device__ __forceinline__ float quant_recip(float s) { return s >= 1e-30f ? __frcp_rn(s) : 0.f; }
+constexpr float kRoundMagic = 12582912.f;   // 1.5 * 2^23
+
+// Codes of N values as bytes (code + 128 = u in [0, 255], stored as the int8
+// u - 128, i.e. u ^ 0x80), packed 4 per word: w[k] holds values 4k .. 4k+3.
+// The quotient q lies in [0, 255 (1 + 2^-22)], so rint(q) needs no clamp.
+template <int N>
+__device__ __forceinline__ void quant_words(const float (&x)[N], float s, float z, float rs,
+                                            uint32_t (&w)[N / 4]) {
+  if (s == 0.f) {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) w[k] = 0x80808080u;   // every code -128
+    return;
+  }
+  float d[N], m[N];
+  bool near = rs == 0.f;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    d[e] = __fsub_rn(x[e], z);
+    const float q = __fmul_rn(d[e], rs);
+    m[e] = __fadd_rn(q, kRoundMagic);                        // rint(q) in the low bits
+    const float diff = __fsub_rn(q, __fsub_rn(m[e], kRoundMagic));
+    near |= fabsf(diff) > 0.499f;
+  }
+  if (__any_sync(__activemask(), near)) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) m[e] = __fadd_rn(__fdiv_rn(d[e], s), kRoundMagic);
+  }
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) {
+    const uint32_t lo = __byte_perm(__float_as_uint(m[4 * k]), __float_as_uint(m[4 * k + 1]), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(m[4 * k + 2]), __float_as_uint(m[4 * k + 3]), 0x0040);
+    w[k] = __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
+  }
+}
+
+// Four consecutive source values (f16/bf16) widened to fp32; i is a multiple of 4.
+__device__ __forceinline__ float4 load_src4(const void* p, int dtype, size_t i) {
+  const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p) + i);
+  if (dtype == PKV_BF16)
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+  return make_float4(__half2float(__ushort_as_half((unsigned short)(w.x & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.x >> 16))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y >> 16))));
 }
 
 __device__ __forceinline__ bool row_window(const AppendParams& p, int b, int& pos, int& n) {
@@ -109,55 +159,70 @@ __global__ void append_copy_kernel(const AppendParams p) {
   }
 }
 
-// Per-token INT8: one warp per (row, token, kv head, K|V) quantises head_dim values.
-__global__ void append_per_token_kernel(const AppendParams p) {
+// Per-token INT8: 8 lanes per (row, token, kv head, K|V), each quantising D/8
+// consecutive values, so a warp serves 4 consecutive tokens of one (row, kv
+// head, K|V) and the per-token work (min/max across lanes, scale, reciprocal)
+// is shared by 8 lanes, not 32. The source values are loaded before the
+// position and block-table lookups.
+constexpr int kTokPerWarp = 4;
+template <int D>
+__global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParams p) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int EPL = D / 8;   // values per lane: 16 (D = 128) or 8 (D = 64)
   const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int H = p.num_kv_heads, D = p.head_dim;
-  const long long total = (long long)p.batch * p.t_new * H * 2;
+  const int lane = threadIdx.x & 31, sub = lane >> 3, part = lane & 7;
+  const int H = p.num_kv_heads;
+  const int tblocks = (p.t_new + kTokPerWarp - 1) / kTokPerWarp;
+  const long long total = (long long)p.batch * tblocks * H * 2;
   if (wid >= total) return;
   const int kv = (int)(wid & 1);
   const int g = (int)((wid >> 1) % H);
-  const long long bt = (wid >> 1) / H;
-  const int t = (int)(bt % p.t_new), b = (int)(bt / p.t_new);
-  int pos, n;
-  if (!row_window(p, b, pos, n) || t >= n) return;
-  const int tp = pos + t;
-  const int phys = page_of(p, b, tp / p.page_size);
-  if (phys < 0) return;
-  const int slot = tp % p.page_size;
+  const long long rest = (wid >> 1) / H;
+  const int t = (int)(rest % tblocks) * kTokPerWarp + sub, b = (int)(rest / tblocks);
   const void* sp = kv ? p.v_new : p.k_new;
-  const size_t src = (((size_t)b * p.t_new + t) * H + g) * D;
-  const int per = D / 32;  // 4 (D = 128) or 2 (D = 64)
-  float x[4];
-  float mn = INFINITY, mx = -INFINITY;
+  float x[EPL];
+  {
+    const size_t src = (((size_t)b * p.t_new + (t < p.t_new ? t : 0)) * H + g) * D + part * EPL;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (e < per) {
-      x[e] = load_src(sp, p.src_dtype, src + lane * per + e);
-      mn = fminf(mn, x[e]);
-      mx = fmaxf(mx, x[e]);
+    for (int e = 0; e < EPL; e += 4) {
+      const float4 f = load_src4(sp, p.src_dtype, src + e);
+      x[e] = f.x; x[e + 1] = f.y; x[e + 2] = f.z; x[e + 3] = f.w;
     }
   }
-  for (int off = 16; off > 0; off >>= 1) {
+  int pos, n;
+  if (!row_window(p, b, pos, n)) return;
+  const bool live = t < n;
+  const int tp = pos + t;
+  const int phys = live ? p.block_table[(size_t)b * p.max_pages + tp / p.page_size] : -1;
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int e = 1; e < EPL; ++e) {
+    mn = fminf(mn, x[e]);
+    mx = fmaxf(mx, x[e]);
+  }
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {   // the token's 8 lanes
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
+  if (!live) return;
+  if (phys < 0 || phys >= p.num_pages) {
+    if (part == 0) flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+    return;
+  }
   const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
   const float z = mn;
-  const size_t row = ((size_t)phys * H + g) * p.page_size + slot;
-  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + lane * per;
-  uint32_t packed = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e)
-    if (e < per) packed |= (uint32_t)(uint8_t)(int8_t)quant_code(x[e], s, z) << (8 * e);
-  if (per == 4)
-    *reinterpret_cast<uint32_t*>(dst) = packed;
+  const float rs = quant_recip(s);
+  uint32_t w[EPL / 4];
+  quant_words<EPL>(x, s, z, rs, w);
+  const size_t row = ((size_t)phys * H + g) * p.page_size + tp % p.page_size;
+  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
+  if constexpr (EPL == 16)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   else
-    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-  if (lane == 0) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  if (part == 0) {
     p.kv_sz[row * 4 + kv * 2 + 0] = s;
     p.kv_sz[row * 4 + kv * 2 + 1] = z;
   }
@@ -165,25 +230,6 @@ __global__ void append_per_token_kernel(const AppendParams p) {
 
 __device__ __forceinline__ float* tail_row(const AppendParams& p, int b, int g, int kv, int parity) {
   return p.tail + ((((size_t)b * p.num_kv_heads + g) * 2 + kv) * 2 + parity) * 64 * p.head_dim;
-}
-
-// Four consecutive source values (f16/bf16) widened to fp32; i is a multiple of 4.
-__device__ __forceinline__ float4 load_src4(const void* p, int dtype, size_t i) {
-  const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p) + i);
-  if (dtype == PKV_BF16)
-    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-  return make_float4(__half2float(__ushort_as_half((unsigned short)(w.x & 0xffffu))),
-                     __half2float(__ushort_as_half((unsigned short)(w.x >> 16))),
-                     __half2float(__ushort_as_half((unsigned short)(w.y & 0xffffu))),
-                     __half2float(__ushort_as_half((unsigned short)(w.y >> 16))));
-}
-
-__device__ __forceinline__ uint32_t quant4(const float4& x, float s, float z) {
-  return (uint32_t)(uint8_t)(int8_t)quant_code(x.x, s, z) |
-         (uint32_t)(uint8_t)(int8_t)quant_code(x.y, s, z) << 8 |
-         (uint32_t)(uint8_t)(int8_t)quant_code(x.z, s, z) << 16 |
-         (uint32_t)(uint8_t)(int8_t)quant_code(x.w, s, z) << 24;
 }
 
 // Per-64-token-group INT8. grid (group slot, kv head * 2 + kv, row); one block
@@ -195,7 +241,7 @@ __device__ __forceinline__ uint32_t quant4(const float4& x, float s, float z) {
 // before the block-table lookup, so the block pays about one memory latency.
 constexpr int kGroupThreads = 256;
 constexpr int kGroupVec4 = 64 * 128 / 4 / kGroupThreads;   // head_dim <= 128
-__global__ void __launch_bounds__(kGroupThreads) append_per_group_kernel(const AppendParams p, int write_tail) {
+__global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(const AppendParams p, int write_tail) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red_mn[kGroupThreads / 32], red_mx[kGroupThreads / 32];
@@ -251,6 +297,7 @@ __global__ void __launch_bounds__(kGroupThreads) append_per_group_kernel(const A
   }
   const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
   const float z = mn;
+  const float rs = quant_recip(s);
   const int off0 = t0 % p.page_size;
   int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) +
                 (((size_t)phys * H + g) * p.page_size + off0) * D;
@@ -261,7 +308,10 @@ __global__ void __launch_bounds__(kGroupThreads) append_per_group_kernel(const A
     const int f = threadIdx.x + k * kGroupThreads;
     if (f < nf) {
       const int i = 4 * f;
-      *reinterpret_cast<uint32_t*>(dst + i) = quant4(x[k], s, z);
+      const float xv[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+      uint32_t wq[1];
+      quant_words<4>(xv, s, z, rs, wq);
+      *reinterpret_cast<uint32_t*>(dst + i) = wq[0];
       if (keep && t0 + i / D >= pos) *reinterpret_cast<float4*>(tw + i) = x[k];
     }
   }
@@ -351,10 +401,11 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
     e = launch_pdl(reinterpret_cast<const void*>(&append_copy_kernel), dim3(p.t_new, p.batch), dim3(256), 0,
                    st, args1);
   } else if (p.quant == PKV_QUANT_PER_TOKEN) {
-    const long long warps = (long long)p.batch * p.t_new * H * 2;
+    const long long warps = (long long)p.batch * ((p.t_new + kTokPerWarp - 1) / kTokPerWarp) * H * 2;
     const long long blocks = (warps * 32 + 255) / 256;
-    e = launch_pdl(reinterpret_cast<const void*>(&append_per_token_kernel), dim3((unsigned)blocks), dim3(256),
-                   0, st, args1);
+    const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&append_per_token_kernel<128>)
+                                       : reinterpret_cast<const void*>(&append_per_token_kernel<64>);
+    e = launch_pdl(fn, dim3((unsigned)blocks), dim3(256), 0, st, args1);
   } else {
     const int groups = (p.t_new + 63) / 64 + 1;
     int inline_tail = p.t_new <= 64;
