@@ -50,8 +50,7 @@ namespace pkv {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-// Small shared scratch: [0] [1] merge masks, [4, 4 + 2 * 8) per-head M and L of
-// the cross-block merge, [8, 8 + warps) scan totals (used before streaming).
+// Small shared scratch: [8, 8 + warps) the unit prefix scan's warp totals.
 constexpr int kMiscInts = 32;
 
 struct AttnParams {
