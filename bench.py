@@ -44,6 +44,9 @@ import synth  # noqa: E402
 DEFAULT_WORKLOAD = "w2_llama7b_bf16"
 # attention launches overlap the kernel before them (see Replica._layer)
 EARLY_START = True
+# the step's append is done by the attention kernel itself where the cache
+# allows it (pkv_append_decode_attention)
+FUSED_APPEND = True
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -296,8 +299,21 @@ class Replica:
         torch.cuda.synchronize()
         self.steps_per_replay = steps
 
+    def fused(self, append: bool, attention: bool, sparse: bool) -> bool:
+        """Whether a step's append + attention run as one call."""
+        c = self.caches[0]
+        return (FUSED_APPEND and append and attention and not sparse and c.page_meta is None
+                and self.w.quant != "per_group64")
+
     def _layer(self, i: int, s: int, stream, append=True, attention=True, sparse=False):
         c = self.caches[i]
+        if self.fused(append, attention, sparse):
+            # the preceding kernel (another layer's combine) touches nothing
+            # this call reads or the new rows: fresh_rows = 0
+            c.append_attention(self.knews[i][s][:, 0], self.vnews[i][s][:, 0], self.qs[i], self.bts[i],
+                               self.len_list[s], sm_scale=self.w.sm_scale, out=self.outs[i],
+                               dev_status=self.status, stream=stream, fresh_rows=0 if EARLY_START else -1)
+            return
         if append:
             c.append(self.knews[i][s], self.vnews[i][s], self.bts[i], self.pos_list[s],
                      dev_status=self.status, stream=stream)
@@ -338,7 +354,7 @@ class Replica:
         plus the bounding-box kernel when the cache keeps page metadata; attention:
         the attention kernel and its combine kernel)."""
         per_layer = 0
-        if append:
+        if append and not self.fused(append, attention, sparse):
             per_layer += 1 + (1 if self.caches[0].page_meta is not None else 0)
         per_layer += (1 if sparse else 0) + (2 if attention else 0)
         return self.steps_per_replay * self.layers * per_layer
@@ -706,8 +722,10 @@ def run_ours(args) -> None:
                        "layers": rep.layers, "num_q_heads": w.num_q_heads,
                        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                        "seq_len": int(lens.max()), "page_size": w.page_size,
-                       "step": "per layer: kv_append of 1 token per sequence + dense "
-                               "paged_decode_attention; 32 layers in one CUDA graph",
+                       "step": ("per layer: append of 1 token per sequence + dense attention, "
+                                "as one append_decode_attention call" if rep.fused(True, True, False) else
+                                "per layer: kv_append of 1 token per sequence + dense "
+                                "paged_decode_attention") + "; all layers in one CUDA graph",
                        "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush"},
             "steps_per_s": round(1e3 / ms * world, 2),
             "frac_of_hbm_peak": round(value / world / peak, 4),
@@ -780,9 +798,12 @@ def main(argv: Optional[List[str]] = None) -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-early-start", action="store_true",
                     help="attention waits for the preceding kernel before any read (fresh_rows = -1)")
+    ap.add_argument("--no-fused-append", action="store_true",
+                    help="the step's append is a separate kv_append launch")
     args = ap.parse_args(argv)
-    global EARLY_START
+    global EARLY_START, FUSED_APPEND
     EARLY_START = not args.no_early_start
+    FUSED_APPEND = not args.no_fused_append
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

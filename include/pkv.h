@@ -247,6 +247,34 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
                                       int32_t* dev_status, void* stream);
 
 /*
+ * append_decode_attention — one decode step of a layer in one call: write each
+ * sequence's new token (K and V of every kv head) at position seq_lens[b] - 1,
+ * as pkv_kv_append with t_new = 1 would [HBM-layout page, section 三; per-token
+ * INT8: section 二], then dense paged_decode_attention over [0, seq_lens[b]).
+ * The block that streams the sequence's last chunk writes the row itself and
+ * copies the chunk after it, so the step needs no separate append launch and
+ * no wait between the two. The pages have no counterpart; this is a packaging
+ * choice of the library.
+ *   k_new, v_new : [batch][num_kv_heads][head_dim] of src_dtype (F16/BF16),
+ *                  16-byte aligned; for fp16/bf16 caches src_dtype must be the
+ *                  cache dtype.
+ *   Other arguments as pkv_paged_decode_attention in dense mode; with
+ *   fresh_rows >= 0 the kernel before the call must also leave the new rows
+ *   alone.
+ * Caches: fp16/bf16 and per-token INT8 without page metadata; per-group INT8
+ * (which re-quantises the whole open group) and caches with page boxes return
+ * PKV_ERR_UNSUPPORTED (use pkv_kv_append and pkv_paged_decode_attention).
+ * Sequences with seq_lens[b] = 0 get no token.
+ */
+pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                       const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                       const void* q, pkv_dtype q_dtype, float sm_scale,
+                                       const int32_t* block_table, int32_t max_pages,
+                                       const int32_t* seq_lens, void* out, pkv_dtype out_dtype,
+                                       int32_t num_splits, int32_t fresh_rows, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * paged_decode_attention_noalloc — the same computation and arguments as
  * pkv_paged_decode_attention with fresh_rows = -1, minus the workspace, for callers that cannot
  * allocate device memory: a program that reserves all device memory at start-up

@@ -23,7 +23,7 @@ DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_BAD_CONFIG = 
 
 EXPORTED = [
     "pkv_status_string", "pkv_abi_version", "pkv_kv_append", "pkv_page_score_topk",
-    "pkv_attention_workspace_bytes", "pkv_paged_decode_attention",
+    "pkv_attention_workspace_bytes", "pkv_paged_decode_attention", "pkv_append_decode_attention",
     "pkv_paged_decode_attention_noalloc",
     "pkv_alloc_create", "pkv_alloc_destroy", "pkv_alloc_reserve", "pkv_alloc_free",
     "pkv_alloc_num_free", "pkv_alloc_seq_pages", "pkv_alloc_check",
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp, vp,
                                                i32, i32, vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
+        "pkv_append_decode_attention": (c_int, [P, i32, i32, vp, vp, c_int, vp, c_int, c_float, vp, i32, vp,
+                                                vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
         "pkv_paged_decode_attention_noalloc": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp,
                                                        vp, i32, i32, vp, c_int, i32, vp, vp]),
         "pkv_alloc_create": (c_int, [i32, POINTER(c_void_p)]),
@@ -146,6 +148,18 @@ def paged_decode_attention(cache: PkvCache, batch: int, num_q_heads: int, q: int
                                             sel_shared, out, out_dtype, num_splits, fresh_rows, workspace,
                                             workspace_bytes, dev_status or None, stream or None),
            "paged_decode_attention")
+
+
+def append_decode_attention(cache: PkvCache, batch: int, num_q_heads: int, k_new: int, v_new: int,
+                            src_dtype: int, q: int, q_dtype: int, sm_scale: float, block_table: int,
+                            max_pages: int, seq_lens: int, out: int, out_dtype: int, num_splits: int,
+                            fresh_rows: int, workspace: int, workspace_bytes: int, dev_status: int,
+                            stream: int) -> None:
+    _check(lib().pkv_append_decode_attention(ctypes.byref(cache), batch, num_q_heads, k_new, v_new,
+                                             src_dtype, q, q_dtype, sm_scale, block_table, max_pages,
+                                             seq_lens, out, out_dtype, num_splits, fresh_rows, workspace,
+                                             workspace_bytes, dev_status or None, stream or None),
+           "append_decode_attention")
 
 
 def paged_decode_attention_noalloc(cache: PkvCache, batch: int, num_q_heads: int, q: int,

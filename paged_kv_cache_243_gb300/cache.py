@@ -178,6 +178,32 @@ class PagedKVCache:
             fresh_rows=fresh_rows, sel_shared=1 if (sparse and sel_shared) else 0)
         return out
 
+    def append_attention(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                         block_table: torch.Tensor, seq_lens: torch.Tensor, sm_scale: Optional[float] = None,
+                         out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                         num_splits: int = 0, dev_status: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None, fresh_rows: int = -1) -> torch.Tensor:
+        """One decode step: write k_new / v_new [B][Hkv][d] (each sequence's token at
+        position seq_lens[b] - 1) and attend over [0, seq_lens[b]), in one call."""
+        _need(q, "q", device=self.device)
+        _need(k_new, "k_new", device=self.device)
+        _need(v_new, "v_new", device=self.device)
+        _need(block_table, "block_table", torch.int32, self.device)
+        _need(seq_lens, "seq_lens", torch.int32, self.device)
+        Bsz, Hq, d = q.shape
+        if sm_scale is None:
+            sm_scale = 1.0 / float(np.sqrt(d))
+        if out is None:
+            out = torch.empty((Bsz, Hq, d), dtype=out_dtype, device=self.device)
+        ws = self.workspace(Bsz, Hq, 0, num_splits)
+        src = B.BF16 if k_new.dtype == torch.bfloat16 else B.F16
+        B.append_decode_attention(
+            self._desc, Bsz, Hq, k_new.data_ptr(), v_new.data_ptr(), src, q.data_ptr(), pkv_dtype(q),
+            float(sm_scale), block_table.data_ptr(), block_table.shape[1], seq_lens.data_ptr(),
+            out.data_ptr(), pkv_dtype(out), num_splits, fresh_rows, ws.data_ptr(), ws.numel(),
+            _ptr(dev_status), _stream(stream))
+        return out
+
 
 class PageAllocator:
     """Host free-list page allocator of libpkv (pkv_alloc_*)."""

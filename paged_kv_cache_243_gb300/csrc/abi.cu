@@ -289,14 +289,19 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
   return pl.ws_bytes;
 }
 
-pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
-                                      const void* q, pkv_dtype q_dtype, float sm_scale,
-                                      const int32_t* block_table, int32_t max_pages,
-                                      const int32_t* seq_lens, const int32_t* sel_pages,
-                                      const int32_t* sel_count, int32_t sel_stride,
-                                      int32_t sel_shared, void* out, pkv_dtype out_dtype,
-                                      int32_t num_splits, int32_t fresh_rows, void* workspace,
-                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Both attention entry points; k_new / v_new non-NULL: fused append (dense only).
+pkv_status attention_impl(const pkv_cache* cache, int32_t batch, int32_t num_q_heads, const void* q,
+                          pkv_dtype q_dtype, float sm_scale, const int32_t* block_table, int32_t max_pages,
+                          const int32_t* seq_lens, const int32_t* sel_pages, const int32_t* sel_count,
+                          int32_t sel_stride, int32_t sel_shared, void* out, pkv_dtype out_dtype,
+                          int32_t num_splits, int32_t fresh_rows, const void* k_new, const void* v_new,
+                          pkv_dtype src_dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          void* stream) {
   pkv_status st = check_cache(cache, true);
   if (st != PKV_OK) return st;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
@@ -352,6 +357,9 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
   p.q_scale = sm_scale * 1.4426950408889634f;
   p.fresh_rows = fresh_rows;
   p.comb_groups = pl.comb_groups;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.src_dtype = src_dtype;
   void* args[] = {&p};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);
@@ -362,6 +370,42 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
     e = launch_pdl(comb, dim3(pl.units, (outs + ob - 1) / ob), dim3(kCombineThreads), 0, cs, args);
   }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                      const void* q, pkv_dtype q_dtype, float sm_scale,
+                                      const int32_t* block_table, int32_t max_pages,
+                                      const int32_t* seq_lens, const int32_t* sel_pages,
+                                      const int32_t* sel_count, int32_t sel_stride,
+                                      int32_t sel_shared, void* out, pkv_dtype out_dtype,
+                                      int32_t num_splits, int32_t fresh_rows, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
+                        sel_pages, sel_count, sel_stride, sel_shared, out, out_dtype, num_splits, fresh_rows,
+                        nullptr, nullptr, PKV_F16, workspace, workspace_bytes, dev_status, stream);
+}
+
+pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
+                                       const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                       const void* q, pkv_dtype q_dtype, float sm_scale,
+                                       const int32_t* block_table, int32_t max_pages,
+                                       const int32_t* seq_lens, void* out, pkv_dtype out_dtype,
+                                       int32_t num_splits, int32_t fresh_rows, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  pkv_status st = check_cache(cache, true);
+  if (st != PKV_OK) return st;
+  if (cache->quant == PKV_QUANT_PER_GROUP64 || cache->page_meta) return PKV_ERR_UNSUPPORTED;
+  if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (cache->kv_dtype != PKV_I8 && src_dtype != cache->kv_dtype) return PKV_ERR_UNSUPPORTED;
+  if (batch > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
+  return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
+                        nullptr, nullptr, 0, 0, out, out_dtype, num_splits, fresh_rows, k_new, v_new,
+                        src_dtype, workspace, workspace_bytes, dev_status, stream);
 }
 
 pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, const void* k_new,

@@ -45,6 +45,7 @@
 #pragma once
 
 #include "pkv_common.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 
@@ -83,6 +84,13 @@ struct AttnParams {
   // query head); 0: (sequence, kv head) serving the G query heads of its group
   // (dense, or sparse with one page list shared by the group).
   int unit_is_q;
+  // Fused append (dense calls; NULL: none): k_new / v_new [batch][Hkv][D] of
+  // src_dtype hold each sequence's token at position seq_len - 1, which the
+  // block streaming that position writes into its page (quantised per token
+  // for INT8 caches) before it copies the chunk.
+  const void* k_new;
+  const void* v_new;
+  int src_dtype;
 };
 
 struct ChunkInfo {
@@ -93,6 +101,7 @@ struct ChunkInfo {
   int nvalid;
   int valid;
   int fresh;  // overlaps rows the preceding kernel may still be writing
+  int last;   // the unit's last chunk (holds position seq_len - 1), dense only
 };
 
 template <int D, int KV>
@@ -321,6 +330,72 @@ __device__ __forceinline__ int cta_of(long long x, long long W, long long N) {
   return (int)div_fast((x + 1) * N - 1, W);
 }
 
+// Fused append of one token row (K and V of one kv head) at row r of the
+// chunk whose K, V (and per-token scale) rows start at ck, cv (csz), by the 32
+// lanes of a warp: a copy for fp16/bf16 caches (source dtype = cache dtype),
+// the per-token quantiser of kv_append for INT8 caches [HBM-layout page,
+// section 二].
+template <int D, int KV>
+__device__ __forceinline__ void append_token_row(const AttnParams& p, int u, int r, uint8_t* ck, uint8_t* cv,
+                                                 float* csz, int lane) {
+  const int b = u / p.units_per_b, g = u - b * p.units_per_b;
+  const size_t src = ((size_t)b * p.num_kv_heads + g) * D;
+  constexpr int PL = D / 32;   // values per lane
+  if constexpr (KV == KV_I8T) {
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const void* sp = kv ? p.v_new : p.k_new;
+      float x[4];
+      if constexpr (PL == 4) {
+        const float4 f = load_src4(sp, p.src_dtype, src + lane * 4);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+      } else {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(sp) + src)[lane];
+        const bool bf = p.src_dtype == PKV_BF16;
+        x[0] = bf ? __uint_as_float(w << 16) : __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+        x[1] = bf ? __uint_as_float(w & 0xffff0000u) : __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+        x[2] = x[0];
+        x[3] = x[1];
+      }
+      float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
+      const float z = mn;
+      uint32_t w[1];
+      quant_words<4>(x, s, z, quant_recip(s), w);
+      uint8_t* dst = (kv ? cv : ck) + (size_t)r * D + lane * PL;
+      if constexpr (PL == 4)
+        *reinterpret_cast<uint32_t*>(dst) = w[0];
+      else
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+      if (lane == 0) {
+        csz[r * 4 + kv * 2 + 0] = s;
+        csz[r * 4 + kv * 2 + 1] = z;
+      }
+    }
+  } else {
+    // fp16 / bf16: D * 2 bytes per row, 8 (D = 128) or 4 (D = 64) bytes per lane
+    const uint16_t* ks = reinterpret_cast<const uint16_t*>(p.k_new) + src;
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(p.v_new) + src;
+    if constexpr (PL == 4) {
+      const uint2 a = reinterpret_cast<const uint2*>(ks)[lane];
+      const uint2 c = reinterpret_cast<const uint2*>(vs)[lane];
+      reinterpret_cast<uint2*>(ck + (size_t)r * D * 2)[lane] = a;
+      reinterpret_cast<uint2*>(cv + (size_t)r * D * 2)[lane] = c;
+    } else {
+      const uint32_t a = reinterpret_cast<const uint32_t*>(ks)[lane];
+      const uint32_t c = reinterpret_cast<const uint32_t*>(vs)[lane];
+      reinterpret_cast<uint32_t*>(ck + (size_t)r * D * 2)[lane] = a;
+      reinterpret_cast<uint32_t*>(cv + (size_t)r * D * 2)[lane] = c;
+    }
+  }
+}
+
 // The tensor-core variant is held to 3 resident blocks per SM (<= 136 registers)
 // so that 12 consumer warps hide its per-chunk latency.
 template <int D, int GE, int KV, bool MMA>
@@ -479,7 +554,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     };
     auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
       ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
-      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0;
+      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0; ci.last = 0;
       if (r.u < 0) return;
       const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
       const int L = lens[b];
@@ -511,6 +586,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
       ci.nvalid = nv;
       ci.valid = 1;
+      ci.last = !sparse && t0 + nv == L;
       if (early) {
         int bnd = L - p.fresh_rows;   // first row the preceding kernel may write
         if constexpr (KV == KV_I8G) bnd = bnd <= 0 ? 0 : bnd / 64 * 64;
@@ -539,6 +615,29 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       for (int k0 = 0; k0 < cnt; k0 += S) {
         const bool mine = lane >= k0 && lane < min(cnt, k0 + S);
         if (!waited && __any_sync(0xffffffffu, mine && e.fresh)) wait_prior();
+        if constexpr (KV == KV_F16 || KV == KV_BF16 || KV == KV_I8T) {
+          unsigned todo = p.k_new ? __ballot_sync(0xffffffffu, mine && e.valid && e.last) : 0u;
+          if (todo) {
+            // the new token of each of these units, written by the whole warp
+            // (after the preceding kernel, which must not touch the row)
+            if (!waited) wait_prior();
+            while (todo) {
+              const int src = __ffs(todo) - 1;
+              todo &= todo - 1;
+              const unsigned long long pk = __shfl_sync(0xffffffffu, (unsigned long long)e.k, src);
+              const unsigned long long pv = __shfl_sync(0xffffffffu, (unsigned long long)e.v, src);
+              const unsigned long long pz = __shfl_sync(0xffffffffu, (unsigned long long)e.sz, src);
+              append_token_row<D, KV>(p, __shfl_sync(0xffffffffu, e.u, src),
+                                      __shfl_sync(0xffffffffu, e.nvalid, src) - 1,
+                                      reinterpret_cast<uint8_t*>(pk), reinterpret_cast<uint8_t*>(pv),
+                                      reinterpret_cast<float*>(pz), lane);
+            }
+            __syncwarp();
+            // the rows were written through the generic proxy; the bulk copies
+            // below read them through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+        }
         if (mine) {
           const int n = nbase + lane;
           const int s = n % S, use = n / S;
