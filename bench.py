@@ -135,7 +135,7 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("attention_kernel.cuh", "pkv_common.cuh"):
+    for f in ("attention_kernel.cuh", "pkv_common.cuh", "quant.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_243_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
