@@ -531,8 +531,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   if (warp == NW) {
     // ================================================================ producer
     // Lane l resolves chunk base + l of each batch of 32. The table entries of
-    // batch k + 1 are loaded before lane 0 issues the copies of batch k, so
-    // their latency overlaps the streaming of batch k.
+    // batch k + 1 are loaded right after batch k's copies are issued, so their
+    // latency overlaps the streaming of batch k.
     const uint64_t pol = policy_evict_first();
     const int cpp = ps / kChunk;
     // raw lookup of chunk x: unit, chunk-in-unit, and the loaded table entries
