@@ -205,8 +205,9 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *                 (split-K over the whole batch's pages, each block taking an
  *                 equal share); 0 = one full wave of the device.
  *   fresh_rows  : -1, or a promise that lets the call start before the
- *                 kernel launched just before it on `stream` has finished:
- *                 that kernel writes nothing this call reads except the K/V
+ *                 work launched just before it on `stream` (one kernel, or
+ *                 both kernels of a preceding attention call) has finished:
+ *                 that work writes nothing this call reads except the K/V
  *                 rows (and scales) that a pkv_kv_append of the last
  *                 fresh_rows tokens of each sequence writes, i.e. positions
  *                 >= seq_lens[b] - fresh_rows (per-group INT8: from the
@@ -224,14 +225,16 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *   workspace   : >= pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                 aligned, any contents (it holds the per-block partial states
  *                 of one call; no initialisation is needed).
- * Two launches: the attention kernel, and (when num_splits != 1) a combine
- * kernel that merges, for each (sequence, kv head) shared by several blocks,
+ * Two launches: the attention kernel, and a combine kernel that merges, for each (sequence, kv head) shared by several blocks,
  * the blocks' partial (running max, sum, accumulator) states. Both are
  * launched with programmatic stream serialization. Every kernel of this
  * library waits for the preceding kernel on the stream before its first
  * global memory access (the attention kernel with fresh_rows >= 0: before
- * its first access to anything outside the promise above), and lets its own
- * dependents start only after that wait, so stream order is kept.
+ * its first access to anything outside the promise above) and before it
+ * completes, so stream order is kept. The attention kernel and the
+ * single-launch calls let their dependents start only after that wait; the
+ * combine kernel lets them start at once, so the next call's kernel can
+ * overlap this call's tail (its own wait still covers this whole call).
  * A sequence with no tokens (or no selected pages) yields zeros.
  * Device errors: PKV_DEV_BAD_PAGE, PKV_DEV_BAD_SELECTED (chunk skipped),
  * PKV_DEV_TIMEOUT.
@@ -259,8 +262,8 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
  *                  16-byte aligned; for fp16/bf16 caches src_dtype must be the
  *                  cache dtype.
  *   Other arguments as pkv_paged_decode_attention in dense mode; with
- *   fresh_rows >= 0 the kernel before the call must also leave the new rows
- *   alone.
+ *   fresh_rows >= 0 the work before the call must also leave the new rows
+ *   alone (the kernel writes them before it waits for that work).
  * Caches: fp16/bf16 and per-token INT8 without page metadata; per-group INT8
  * (which re-quantises the whole open group) and caches with page boxes return
  * PKV_ERR_UNSUPPORTED (use pkv_kv_append and pkv_paged_decode_attention).

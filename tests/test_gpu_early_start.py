@@ -97,3 +97,58 @@ def test_back_to_back_calls_share_output_and_workspace():
     last = out.cpu().numpy()
     assert np.array_equal(last, outs[3].cpu().numpy())
     assert int(ld.status.item()) == 0
+
+
+FUSED_CASES = [
+    # name, dtype, quant, d, Hq, Hkv, page
+    ("bf16-gqa", "bf16", "none", 128, 16, 4, 16),
+    ("i8-token-mha", "f16", "per_token", 64, 4, 4, 16),
+]
+
+
+@pytest.mark.parametrize("layers,fresh", [(2, 0), (1, 2)])
+@pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps", FUSED_CASES)
+def test_fused_steps_enqueued_back_to_back(name, dt, quant, d, Hq, Hkv, ps, layers, fresh):
+    # decode steps of one-call append + attention, all enqueued before any
+    # synchronisation, so each call may start while the previous call's kernels
+    # still run. Two layers: the previous call works on the other cache and
+    # writes nothing this one reads (fresh_rows = 0). One layer: the previous
+    # step wrote the row just before this step's new row (fresh_rows = 2).
+    w = synth.Workload(name="early-fused-" + name, seed=700 + d + Hq, batch=3, layers=layers,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt, quant=quant,
+                       seq_len=None, seq_len_range=(1, 400),
+                       outlier_channels=4 if quant != "none" else 0, outlier_scale=15.0)
+    lens = np.array([400, 17, 130], dtype=np.int32)
+    steps = 4
+    lds = [load_workload(w, layer=l, lens=lens, extra_pages=1) for l in range(layers)]
+    toks = [[[synth.append_tokens(w, b, 10 * l + s) for b in range(w.batch)] for s in range(steps)]
+            for l in range(layers)]
+    dev = lambda bits: bits_to_torch(bits, dt).cuda()  # noqa: E731
+    k_in = [[dev(np.stack([t.k_bits[0] for t in toks[l][s]])) for s in range(steps)] for l in range(layers)]
+    v_in = [[dev(np.stack([t.v_bits[0] for t in toks[l][s]])) for s in range(steps)] for l in range(layers)]
+    qs = [[queries_dev(w, step=10 * l + s) for s in range(steps)] for l in range(layers)]
+    lens_dev = [torch.from_numpy(lens + s + 1).cuda() for s in range(steps)]
+    outs = [[torch.empty((w.batch, Hq, d), dtype=torch.float32, device="cuda") for _ in range(steps)]
+            for _ in range(layers)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for l in range(layers):
+            lds[l].cache.append_attention(k_in[l][s], v_in[l][s], qs[l][s][0], lds[l].bt_dev, lens_dev[s],
+                                          sm_scale=w.sm_scale, out=outs[l][s], dev_status=lds[l].status,
+                                          fresh_rows=fresh)
+    torch.cuda.synchronize()
+    for l in range(layers):
+        assert int(lds[l].status.item()) == 0
+        for b in range(w.batch):
+            Kb, Vb = lds[l].seqs[b].k, lds[l].seqs[b].v
+            for s in range(steps):
+                Kb = np.concatenate([Kb, toks[l][s][b].k])
+                Vb = np.concatenate([Vb, toks[l][s][b].v])
+                kd, vd = _restored(w, Kb), _restored(w, Vb)
+                got = outs[l][s][b].cpu().numpy()
+                qf = qs[l][s][1]
+                for h in range(Hq):
+                    o = oracle.decode_attention_tokens(qf[b, h], kd[:, h // w.group], vd[:, h // w.group],
+                                                       w.sm_scale)
+                    tol = TOL["int8"] if quant != "none" else TOL[dt]
+                    assert np.abs(got[h] - o).max() <= tol, (l, s, b, h)
