@@ -195,8 +195,16 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   if (forced > 0) stages = forced;
   stages = stages / kConsumerWarps * kConsumerWarps;
   stages = stages < kConsumerWarps ? kConsumerWarps : (stages > 32 ? 32 : stages);
+  // after the stream the ring holds the four consumer warps' states of the
+  // block's last unit, merged there into one record
+  const size_t staging = (size_t)kConsumerWarps * rec_floats(pl.ge, c->head_dim) * 4;
+  int min_stages = (int)((staging + stage - 1) / stage);
+  min_stages = (min_stages + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+  if (min_stages < kConsumerWarps) min_stages = kConsumerWarps;
+  if (min_stages > 32) return PKV_ERR_UNSUPPORTED;
+  if (stages < min_stages) stages = min_stages;
   size_t smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
-  while (smem > (size_t)di.max_smem_optin && stages > kConsumerWarps) {
+  while (smem > (size_t)di.max_smem_optin && stages > min_stages) {
     stages -= kConsumerWarps;
     smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
   }
@@ -228,14 +236,15 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     }
     pl.ctas = di.sms * nb;
   }
-  // Combine layout: about 4 (blocks per unit + 1) records per unit; more
+  // Combine layout: about blocks per unit + 4 records per unit (one from each
+  // block that ends inside the unit, four from the one that moves on); more
   // record groups per block fold them in fewer rounds (loads of the next
   // round overlap the current fold), fewer give more outputs per block
   // (fewer blocks). Cost ~ waves * (3 + rounds).
   {
     const int outs = pl.ge * c->head_dim;
     const long long units = pl.units > 0 ? pl.units : 1;
-    const long long rbar = (long long)kConsumerWarps * ((pl.ctas + units - 1) / units + 1);
+    const long long rbar = (pl.ctas + units - 1) / units + kConsumerWarps;
     const long long slots = (long long)di.sms * 2;   // combine blocks resident at once
     long long best = -1;
     for (int rg = 1; rg <= 8; rg *= 2) {

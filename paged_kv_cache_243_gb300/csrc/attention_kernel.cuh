@@ -53,6 +53,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 // Small shared scratch: [8, 8 + warps) the unit prefix scan's warp totals.
 constexpr int kMiscInts = 32;
+constexpr int kMiscAbort = 24;   // misc slot: some consumer warp timed out
 
 struct AttnParams {
   const uint8_t* k_pages;
@@ -64,7 +65,9 @@ struct AttnParams {
   const int32_t* seq_lens;
   const int32_t* sel_pages;  // NULL: dense
   const int32_t* sel_count;
-  float* ws_wrec;     // per-warp partial records, slot ((block + unit) * 4 + warp)
+  // partial records, slot ((block + unit) * 4 + warp); for the block's last
+  // unit only slot 0, holding the merge of its four warps
+  float* ws_wrec;
   int32_t* ws_prefix; // [num_units + 1] chunk prefix, written by block 0 for the combine
   int32_t* dev_status;
   int num_pages, page_size, num_kv_heads, num_q_heads, group;
@@ -420,7 +423,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.num_units;
-  if (S <= 0 || S % NW != 0 || S > 32) {  // the host never launches this; refuse rather than race
+  // the host never launches these; refuse rather than race (the ring must also
+  // hold the four warps' states of the block's last unit after the stream)
+  if (S <= 0 || S % NW != 0 || S > 32 || (size_t)S * STAGE < (size_t)NW * rec_floats(GE, D) * 4) {
     if (tid == 0) flag_status(p.dev_status, PKV_DEV_BAD_CONFIG);
     return;
   }
@@ -456,6 +461,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     mbar_init(smem_u32(&full[tid]), 1);
     mbar_init(smem_u32(&empty[tid]), 1);
   }
+  if (tid == 0) misc[kMiscAbort] = 0;
   fence_mbar_init();
   __syncthreads();
 
@@ -686,6 +692,61 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     return;
   }
 
+  // The block's last unit ub: its four warps' states are merged here into one
+  // record at slot (c + ub) * 4 (the other units keep one record per warp), so
+  // the combine reads one record from each block but a unit's last. After the
+  // stream every copy this block issued has been consumed, so the ring holds
+  // the four states; a warp that timed out may leave a copy in flight, and the
+  // slot then gets an empty record (the status already reports the failure).
+  auto merge_last_unit = [&](bool aborted, bool holds_ub, auto&& stage_state) {
+    constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
+    float* staged = reinterpret_cast<float*>(ring);
+    if (aborted) misc[kMiscAbort] = 1;
+    named_bar_sync(1, NW * 32);               // every consumer is done with the ring
+    const bool any_abort = misc[kMiscAbort] != 0;
+    if (!any_abort) {
+      float* mine = staged + warp * RS;
+      if (holds_ub) {
+        stage_state(mine);
+      } else if (lane < GE) {
+        mine[lane] = -INFINITY;
+        mine[GE + lane] = 0.f;
+      }
+    }
+    named_bar_sync(1, NW * 32);
+    if (early) pdl_wait();
+    float* dst = p.ws_wrec + (size_t)(c + ub) * NW * RS;
+    if (any_abort) {
+      if (tid < GE) {
+        dst[tid] = -INFINITY;
+        dst[GE + tid] = 0.f;
+      }
+      return;
+    }
+    for (int o = tid; o < GE * D; o += NW * 32) {
+      const int h = o / D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, staged[w * RS + h]);
+      float L = 0.f, A = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float m = staged[w * RS + h];
+          if (m == -INFINITY) continue;   // empty state: its acc is not written
+          const float f = exp2f(m - M);
+          L = fmaf(f, staged[w * RS + GE + h], L);
+          A = fmaf(f, staged[w * RS + HDR + o], A);
+        }
+      }
+      dst[HDR + o] = A;
+      if (o % D == 0) {
+        dst[h] = M;
+        dst[GE + h] = L;
+      }
+    }
+  };
+
   if constexpr (!MMA) {
   // ================================================================== consumers
   const int r = lane >> 3, j = lane & 7;
@@ -711,9 +772,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     }
   };
 
-  auto flush = [&](int u) {
-    if (early) pdl_wait();
-    float* rec = rec_of(u);
+  auto flush_to = [&](float* rec) {   // global or shared memory
 #pragma unroll
     for (int h = 0; h < GE; ++h) {
       const float zh = __shfl_sync(0xffffffffu, zs, h * DUP);
@@ -732,6 +791,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       rec[my_head] = m_h;
       rec[GE + my_head] = l_h;
     }
+  };
+  auto flush = [&](int u) {
+    if (early) pdl_wait();
+    flush_to(rec_of(u));
   };
 
   auto start_unit = [&](int u) {
@@ -883,12 +946,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
   }
   if (!abort) {
-    if (u_cur >= 0) {
+    if (u_cur >= 0 && u_cur != ub) {
       flush(u_cur);
       next_unit = u_cur + 1;
     }
-    for (int v = next_unit; v <= ub; ++v) write_empty(v);
+    for (int v = next_unit; v < ub; ++v) write_empty(v);
   }
+  merge_last_unit(abort, u_cur == ub, [&](float* rec) { flush_to(rec); });
 
   } else {
   // ============================================== consumers, tensor-core path
@@ -928,9 +992,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       rec[GE + lane] = 0.f;
     }
   };
-  auto flush = [&](int u) {
-    if (early) pdl_wait();
-    float* rec = rec_of(u);
+  auto flush_to = [&](float* rec) {   // global or shared memory
     if constexpr (PACK) {   // lo columns (threads t + G/2) into the hi ones
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -964,6 +1026,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         }
       }
     }
+  };
+  auto flush = [&](int u) {
+    if (early) pdl_wait();
+    flush_to(rec_of(u));
   };
   auto start_unit = [&](int u) {
     const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
@@ -1208,12 +1274,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
   }
   if (!abort) {
-    if (u_cur >= 0) {
+    if (u_cur >= 0 && u_cur != ub) {
       flush(u_cur);
       next_unit = u_cur + 1;
     }
-    for (int v = next_unit; v <= ub; ++v) write_empty(v);
+    for (int v = next_unit; v < ub; ++v) write_empty(v);
   }
+  merge_last_unit(abort, u_cur == ub, [&](float* rec) { flush_to(rec); });
   }
 
   // Block 0 publishes the unit prefix for the combine of sparse calls (dense
@@ -1224,9 +1291,11 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   }
 }
 
-// Merge of every unit's warp records: the 4 records (one per consumer warp,
-// some empty) of each block whose range overlaps the unit, i.e. blocks
-// c_first .. c_last, whose slots ((c + u) * 4 + w) are consecutive:
+// Merge of every unit's records: those of each block whose range overlaps the
+// unit, i.e. blocks c_first .. c_last, whose slots ((c + u) * 4 + w) are
+// consecutive: one (slot 0) from each block that ends inside the unit, where
+// the unit is the block's last and its four warps were merged in the block,
+// and four (one per warp, some empty) from a block that moves on past it:
 //   M = max m_r,  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r
 // (the log2-domain partial states of the attention kernel). The 256 threads
 // of block (u, y) form RG = comb_groups record groups of OB = 256 / RG
@@ -1291,12 +1360,17 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
   }
   const long long N = p.num_ctas;
   // the unit's covering blocks (known before the wait for dense calls)
-  auto cover = [&](int& c_first, int& R4) {
+  // Records of the unit: one (slot 0, the block's merged last unit) from each
+  // covering block before the last, then the last block's: one if the unit is
+  // its last unit too (the unit ends with the block), else four (one per warp).
+  auto cover = [&](int& c_first, int& nb1, int& R4) {
     c_first = cta_of(s0, W, N);
-    R4 = (cta_of(s1 - 1, W, N) - c_first + 1) * kConsumerWarps;
+    const int c_last = cta_of(s1 - 1, W, N);
+    nb1 = c_last - c_first;
+    R4 = nb1 + (cta_lo(c_last + 1, W, N) <= s1 ? 1 : kConsumerWarps);
   };
-  int c_first = 0, R4 = 0;
-  if (!sparse && s0 != s1) cover(c_first, R4);
+  int c_first = 0, nb1 = 0, R4 = 0;
+  if (!sparse && s0 != s1) cover(c_first, nb1, R4);
   // The next kernel may launch now, before this grid's wait: its own wait
   // covers this grid, which completes only after the attention grid it
   // merges. (Triggering at the very start measured slower: W2 25.4 against
@@ -1307,7 +1381,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
     W = __ldcg(p.ws_prefix + p.num_units);
     s0 = __ldcg(p.ws_prefix + u);
     s1 = __ldcg(p.ws_prefix + u + 1);
-    if (s0 != s1) cover(c_first, R4);
+    if (s0 != s1) cover(c_first, nb1, R4);
   }
   if (s0 == s1) return;   // no chunks: the attention kernel wrote zeros
   // With at least one chunk per block (W >= N) every covering block wrote its
@@ -1316,6 +1390,9 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
   const int oo = active ? o : 0;
   const int h = oo / D;
   const float* rec0 = p.ws_wrec + (size_t)(c_first + u) * kConsumerWarps * RS;
+  // slot of record r relative to rec0: block c_first + r (slot 0) for r < nb1,
+  // then slots 0.. of block c_first + nb1
+  auto rec_slot = [&](int r) { return r < nb1 ? r * kConsumerWarps : nb1 * kConsumerWarps + (r - nb1); };
   float M = -INFINITY, L = 0.f, A = 0.f;
   // BATCH records per load round, two rounds in flight: the next round's loads
   // are issued before the current one is folded
@@ -1323,9 +1400,9 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
 #pragma unroll
     for (int i = 0; i < BATCH; ++i) {
       const int r = r0 + i * RG;
-      const int cc = c_first + r / kConsumerWarps;
+      const int cc = c_first + (r < nb1 ? r : nb1);
       const bool ok = r < R4 && (dense_cover || cta_lo(cc, W, N) < cta_lo(cc + 1, W, N));
-      const float* rr = rec0 + (size_t)(ok ? r : 0) * RS;
+      const float* rr = rec0 + (size_t)(ok ? rec_slot(r) : 0) * RS;
       mc[i] = ok ? __ldcg(rr + h) : -INFINITY;
       lc[i] = __ldcg(rr + GE + h);
       ac[i] = __ldcg(rr + HDR + oo);
