@@ -4,17 +4,15 @@
 // is a query head, or a kv head whose G query heads' scores are summed or
 // maxed (one shared page list per group; a reading, the pages score one query).
 //
-// One cluster of CS blocks per (sequence, row): 4 for a query head, 8 for a
-// kv head's group (G heads to score per page). Phase 1:
-// block r of the cluster scores the r-th quarter of the pages (a warp per
-// page, lane-parallel over channels, butterfly sum) into its shared memory;
-// the leader then gathers the other blocks' scores through distributed shared
-// memory. Scoring is bound by the box bytes, and four blocks per row put every
-// SM to work on them. Phase 2 (leader): an exact radix select (four 8-bit
-// passes over an order-preserving integer image of the scores) finds the K-th
-// largest score T; pages above T are kept, and of those equal to T the lowest
-// page indices fill the remaining places. Phase 3: a block-wide scan in page
-// order writes the kept pages in ascending order.
+// One cluster of 8 blocks per (sequence, KBH consecutive kv heads), whose
+// boxes are one contiguous read per page (details at the kernel). Phase 1:
+// block r scores the r-th eighth of the pages for every query head of those
+// kv heads into its shared memory. Phase 2: block r gathers row r's scores
+// from the cluster through distributed shared memory and runs an exact radix
+// select (four 8-bit passes over an order-preserving integer image of the
+// scores) for the K-th largest score T; pages above T are kept, and of those
+// equal to T the lowest page indices fill the remaining places. Phase 3: a
+// block-wide scan in page order writes the kept pages in ascending order.
 #include <cooperative_groups.h>
 
 #include "pkv_internal.h"
@@ -27,8 +25,7 @@ namespace {
 
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkClusterHead = 4;    // rows of one query head
-constexpr int kTopkClusterGroup = 8;   // rows of a query-head group
+constexpr int kTopkCluster = 8;        // blocks per (sequence, kv-head block)
 
 // Larger float -> larger unsigned key; NaN is treated as -inf.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -59,181 +56,23 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
   return pre + x - v;
 }
 
-template <int D, int CS>
-__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kTopkThreads, D == 64 ? 4 : 3)
-    score_topk_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint32_t keys[];  // [max pages of a sequence]
-  __shared__ int hist[256];
-  __shared__ int warp_tot[kTopkWarps];
-  __shared__ int sel_digit, sel_remaining;
-  __shared__ float qsm[8 * D];   // the row's query heads (<= 8)
-  pdl_wait();
-  pdl_launch_dependents();
-
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  // a row selects: a query head, or a kv head for its group (sum / max)
-  const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
-  const int rows_per_b = grouped ? p.num_kv_heads : p.num_q_heads;
-  const int HR = grouped ? p.group : 1;             // query heads scored per row
-  const int bh = blockIdx.x / CS;                   // row index b * rows_per_b + r
-  const int b = bh / rows_per_b, hr = bh - b * rows_per_b;
-  const int g = grouped ? hr : hr / p.group;        // kv head whose boxes are read
-  const int h0 = grouped ? hr * p.group : hr;       // first query head of the row
+// Exact top-K of one row's scores keys[0, P) (float bits) into
+// sel[0, top_k), ascending page order; ties at the K-th score keep the lower
+// page indices. Whole block; keys is overwritten.
+__device__ void select_row(uint32_t* keys, int P, int K, int top_k, int32_t* sel, int32_t* count,
+                           int* hist, int* warp_tot, int& sel_digit, int& sel_remaining) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ps = p.page_size;
-  int L = p.seq_lens[b];
-  if (L < 0) L = 0;
-  int P = (L + ps - 1) / ps;
-  if (P > p.max_pages) P = p.max_pages;
-  const int K = min(p.top_k, P);
-
-  // ---- phase 1: scores
-  constexpr int PL = D / 32;  // channels per lane
-  for (int i = tid; i < HR * D; i += kTopkThreads)
-    qsm[i] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h0) * D + i);
-  // this block's pages [pg0, pg1) of the row
-  const int pg0 = (int)((long long)P * rank / CS);
-  const int pg1 = (int)((long long)P * (rank + 1) / CS);
-  // The block-table entries are staged (coalesced) in the key array first;
-  // each page's entry is read before its score overwrites that slot.
-  for (int pg = pg0 + tid; pg < pg1; pg += kTopkThreads)
-    keys[pg] = (uint32_t)p.block_table[(size_t)b * p.max_pages + pg];
-  __syncthreads();
-  // pages in flight per warp (box loads issued before use); a group's rows
-  // keep fewer pages in flight and score every head of the group from one
-  // load of each box
-  constexpr bool GROUPED = CS == kTopkClusterGroup;
-  constexpr int UNROLL = GROUPED ? 4 : 16;
-  for (int base = pg0 + warp * UNROLL; base < pg1; base += kTopkWarps * UNROLL) {
-    float part[UNROLL];
-    __syncwarp();
-    if constexpr (!GROUPED) {
-      // one query head: each page's partial right after its box loads
-      float qv[PL];
-#pragma unroll
-      for (int e = 0; e < PL; ++e) qv[e] = qsm[lane * PL + e];
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const int pg = base + k;
-        const int ph = pg < pg1 ? (int)keys[pg] : -1;   // staged table entry
-        part[k] = 0.f;
-        if (ph >= 0 && ph < p.num_pages) {
-          const float* mrow = p.page_meta + (((size_t)ph * p.num_kv_heads + g) * 2) * D + lane * PL;
-          float mn[PL], mx[PL];
-          if constexpr (PL == 4) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
-            const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
-            mn[0] = a.x; mn[1] = a.y; mn[2] = a.z; mn[3] = a.w;
-            mx[0] = c.x; mx[1] = c.y; mx[2] = c.z; mx[3] = c.w;
-          } else {
-            const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
-            const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
-            mn[0] = a.x; mn[1] = a.y;
-            mx[0] = c.x; mx[1] = c.y;
-          }
-          float acc = 0.f;
-#pragma unroll
-          for (int e = 0; e < PL; ++e) acc = fmaf(qv[e], qv[e] >= 0.f ? mx[e] : mn[e], acc);
-          part[k] = acc;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k)
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part[k] += __shfl_xor_sync(0xffffffffu, part[k], off);
-    } else {
-      float mn[UNROLL][PL], mx[UNROLL][PL];
-  #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const int pg = base + k;
-        const int ph = pg < pg1 ? (int)keys[pg] : -1;   // staged table entry
-  #pragma unroll
-        for (int e = 0; e < PL; ++e) { mn[k][e] = 0.f; mx[k][e] = 0.f; }
-        if (ph >= 0 && ph < p.num_pages) {
-          const float* mrow = p.page_meta + (((size_t)ph * p.num_kv_heads + g) * 2) * D + lane * PL;
-          if constexpr (PL == 4) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(mrow));
-            const float4 c = __ldg(reinterpret_cast<const float4*>(mrow + D));
-            mn[k][0] = a.x; mn[k][1] = a.y; mn[k][2] = a.z; mn[k][3] = a.w;
-            mx[k][0] = c.x; mx[k][1] = c.y; mx[k][2] = c.z; mx[k][3] = c.w;
-          } else {
-            const float2 a = __ldg(reinterpret_cast<const float2*>(mrow));
-            const float2 c = __ldg(reinterpret_cast<const float2*>(mrow + D));
-            mn[k][0] = a.x; mn[k][1] = a.y;
-            mx[k][0] = c.x; mx[k][1] = c.y;
-          }
-        }
-      }
-      // each query head of the row: the pages' lane partials, butterfly sums,
-      // then the row's reduction (one head: itself; a group: sum or max)
-      for (int j = 0; j < HR; ++j) {
-        float qv[PL];
-  #pragma unroll
-        for (int e = 0; e < PL; ++e) qv[e] = qsm[j * D + lane * PL + e];
-        float sj[UNROLL];
-  #pragma unroll
-        for (int k = 0; k < UNROLL; ++k) {
-          float acc = 0.f;
-  #pragma unroll
-          for (int e = 0; e < PL; ++e) acc = fmaf(qv[e], qv[e] >= 0.f ? mx[k][e] : mn[k][e], acc);
-          sj[k] = acc;
-        }
-  #pragma unroll
-        for (int k = 0; k < UNROLL; ++k) {
-  #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sj[k] += __shfl_xor_sync(0xffffffffu, sj[k], off);
-          part[k] = j == 0 ? sj[k] : (p.group_mode == PKV_SELECT_GROUP_MAX ? fmaxf(part[k], sj[k]) : part[k] + sj[k]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const int pg = base + k;
-        if (pg >= pg1) break;
-        float s = part[k];
-        const int ph = (int)keys[pg];
-        if (ph < 0 || ph >= p.num_pages) {
-          flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
-          s = -INFINITY;
-        }
-        keys[pg] = __float_as_uint(s);
-        if (p.scores_out) p.scores_out[(size_t)bh * p.max_pages + pg] = s;
-      }
-    }
-  }
-  if (p.scores_out && rank == 0) {
-    for (int pg = P + tid; pg < p.max_pages; pg += kTopkThreads)
-      p.scores_out[(size_t)bh * p.max_pages + pg] = -INFINITY;
-  }
-  // every score of the row now sits in the cluster's shared memory; the leader
-  // copies the other blocks' parts, which stay resident until it is done
-  cluster.sync();
-  if (rank == 0) {
-    for (int r = 1; r < CS; ++r) {
-      const uint32_t* remote = cluster.map_shared_rank(keys, r);
-      const int a0 = (int)((long long)P * r / CS), a1 = (int)((long long)P * (r + 1) / CS);
-      for (int i = a0 + tid; i < a1; i += kTopkThreads) keys[i] = remote[i];
-    }
-  }
-  cluster.sync();
-  if (rank != 0) return;
-
-  int32_t* sel = p.sel_pages + (size_t)bh * p.top_k;
-  if (tid == 0) p.sel_count[bh] = K;
-  for (int i = K + tid; i < p.top_k; i += kTopkThreads) sel[i] = -1;
+  if (tid == 0) *count = K;
+  for (int i = K + tid; i < top_k; i += kTopkThreads) sel[i] = -1;
   if (K == 0) return;
   if (K == P) {
     for (int i = tid; i < P; i += kTopkThreads) sel[i] = i;
     return;
   }
-
   for (int i = tid; i < P; i += kTopkThreads) keys[i] = order_key(__uint_as_float(keys[i]));
   __syncthreads();
 
-  // ---- phase 2: radix select of the K-th largest key
+  // ---- radix select of the K-th largest key
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
   for (int shift = 24; shift >= 0; shift -= 8) {
@@ -284,7 +123,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kTopkThreads, D == 
   const uint32_t T = prefix;
   const int need_eq = remaining;  // how many pages scoring exactly T are kept
 
-  // ---- phase 3: ordered compaction
+  // ---- ordered compaction
   const int per = (P + kTopkThreads - 1) / kTopkThreads;
   const int i0 = min(P, tid * per), i1 = min(P, i0 + per);
   int n_eq = 0;
@@ -311,29 +150,226 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kTopkThreads, D == 
       if (take) sel[out++] = i;
     }
   }
+  __syncthreads();   // keys is reused by the block's next row
+}
+
+// One cluster per (sequence, KBH consecutive kv heads). The boxes of those kv
+// heads sit next to each other in a page's metadata ([page][kv head][2][D]), so
+// each page is one contiguous read of KBH * 2 * D floats (2 KB at the chosen
+// KBH): random 2 KB reads stream near the HBM peak where 512 B reads (one
+// head's box) reach about half. The cluster scores its G * KBH query heads and
+// selects NR rows: the query heads (per-head lists) or the kv heads (a group's
+// sum or max). Block r of the cluster scores the r-th eighth of the pages, a
+// warp per page (UNROLL pages in flight), into its shared memory; then block r
+// gathers row r's scores (rows r, r + 8, ... when NR > 8) from the cluster
+// through distributed shared memory and selects them.
+template <int D, int KBH>
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
+    score_topk_kernel(const TopkParams p) {
+  constexpr int CS = kTopkCluster;
+  constexpr int NV = KBH * 2 * D / 128;    // float4 box loads per lane per page
+  constexpr int UNROLL = 16 / NV;          // pages in flight per warp (8 KB)
+  extern __shared__ __align__(16) uint32_t tk_smem[];
+  __shared__ int hist[256];
+  __shared__ int warp_tot[kTopkWarps];
+  __shared__ int sel_digit, sel_remaining;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
+  const int G = p.group;
+  const int NQ = KBH * G;                           // query heads scored
+  const int NR = grouped ? KBH : NQ;                // rows selected
+  const int cpb = p.num_kv_heads / KBH;             // clusters per sequence
+  const int cl = blockIdx.x / CS;
+  const int b = cl / cpb;
+  const int g0 = (cl - b * cpb) * KBH;              // first kv head
+  const int h0 = g0 * G;                            // first query head
+  const int rows_per_b = grouped ? p.num_kv_heads : p.num_q_heads;
+  const int row0 = grouped ? g0 : h0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ps = p.page_size;
+  int L = p.seq_lens[b];
+  if (L < 0) L = 0;
+  int P = (L + ps - 1) / ps;
+  if (P > p.max_pages) P = p.max_pages;
+  const int K = min(p.top_k, P);
+  // shared memory: keys [max_pages], own [NR][span], qsm [NQ][D], each
+  // rounded to 4 floats so that qsm takes float4 loads
+  const int span = ((p.max_pages + CS - 1) / CS + 3) / 4 * 4;
+  uint32_t* keys = tk_smem;
+  float* own = reinterpret_cast<float*>(tk_smem + (p.max_pages + 3) / 4 * 4);
+  float* qsm = own + (size_t)NR * span;
+
+  for (int i = tid; i < NQ * D; i += kTopkThreads)
+    qsm[i] = load_q_elem(p.q, p.q_dtype, ((size_t)b * p.num_q_heads + h0) * D + i);
+  const int pg0 = (int)((long long)P * rank / CS);
+  const int pg1 = (int)((long long)P * (rank + 1) / CS);
+  for (int pg = pg0 + tid; pg < pg1; pg += kTopkThreads)
+    keys[pg] = (uint32_t)p.block_table[(size_t)b * p.max_pages + pg];
+  __syncthreads();
+
+  // lane l's channels: 4 (l % 16) .. + 3 of the min (l < 16) or max box (d = 64;
+  // float4 i is kv head i), or 4 l .. + 3 of both (d = 128; float4 2k is kv
+  // head k's min, 2k + 1 its max)
+  const int ch = D == 64 ? 4 * (lane & 15) : 4 * lane;
+  const bool is_max = D == 64 && lane >= 16;
+  for (int base = pg0 + warp * UNROLL; base < pg1; base += kTopkWarps * UNROLL) {
+    float4 v[UNROLL][NV];
+    bool ok[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const int pg = base + k;
+      const int ph = pg < pg1 ? (int)keys[pg] : -1;   // staged table entry
+      ok[k] = ph >= 0 && ph < p.num_pages;
+      const float4* box = reinterpret_cast<const float4*>(
+          p.page_meta + ((size_t)(ok[k] ? ph : 0) * p.num_kv_heads + g0) * 2 * D);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[k][i] = ok[k] ? __ldg(box + i * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int kk = 0; kk < KBH; ++kk) {
+      float rowv[UNROLL];   // grouped: the kv head's row, over its G heads
+      for (int j = 0; j < G; ++j) {
+        const float4 q4 = *reinterpret_cast<const float4*>(qsm + (kk * G + j) * D + ch);
+        float sc[UNROLL];
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+          float4 lo4, hi4;
+          if constexpr (D == 64) {
+            lo4 = v[k][0];
+#pragma unroll
+            for (int i = 1; i < NV; ++i) if (i == kk) lo4 = v[k][i];
+            hi4 = lo4;
+          } else {
+            lo4 = v[k][0];
+            hi4 = v[k][1];
+#pragma unroll
+            for (int i = 1; i < NV / 2; ++i)
+              if (i == kk) {
+                lo4 = v[k][2 * i];
+                hi4 = v[k][2 * i + 1];
+              }
+          }
+          float a = 0.f;
+          if constexpr (D == 64) {
+            // this lane holds one bound: the max for q_i >= 0, the min for q_i < 0
+            auto pick = [&](float qc) { return is_max ? qc >= 0.f : qc < 0.f; };
+            a = pick(q4.x) ? q4.x * lo4.x : 0.f;
+            a = pick(q4.y) ? fmaf(q4.y, lo4.y, a) : a;
+            a = pick(q4.z) ? fmaf(q4.z, lo4.z, a) : a;
+            a = pick(q4.w) ? fmaf(q4.w, lo4.w, a) : a;
+          } else {
+            a = q4.x * (q4.x >= 0.f ? hi4.x : lo4.x);
+            a = fmaf(q4.y, q4.y >= 0.f ? hi4.y : lo4.y, a);
+            a = fmaf(q4.z, q4.z >= 0.f ? hi4.z : lo4.z, a);
+            a = fmaf(q4.w, q4.w >= 0.f ? hi4.w : lo4.w, a);
+          }
+          sc[k] = a;
+        }
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sc[k] += __shfl_xor_sync(0xffffffffu, sc[k], off);
+        }
+        if (!grouped) {
+          if (lane == 0) {
+            const int r = kk * G + j;
+#pragma unroll
+            for (int k = 0; k < UNROLL; ++k) {
+              const int pg = base + k;
+              if (pg < pg1) own[r * span + (pg - pg0)] = ok[k] ? sc[k] : -INFINITY;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < UNROLL; ++k)
+            rowv[k] = j == 0 ? sc[k]
+                             : (p.group_mode == PKV_SELECT_GROUP_MAX ? fmaxf(rowv[k], sc[k]) : rowv[k] + sc[k]);
+        }
+      }
+      if (grouped && lane == 0) {
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+          const int pg = base + k;
+          if (pg < pg1) own[kk * span + (pg - pg0)] = ok[k] ? rowv[k] : -INFINITY;
+        }
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k)
+        if (base + k < pg1 && !ok[k]) flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+    }
+  }
+  __syncthreads();
+  if (p.scores_out) {
+    for (int r = 0; r < NR; ++r) {
+      float* so = p.scores_out + ((size_t)b * rows_per_b + row0 + r) * p.max_pages;
+      for (int pg = pg0 + tid; pg < pg1; pg += kTopkThreads) so[pg] = own[r * span + (pg - pg0)];
+      if (rank == 0)
+        for (int pg = P + tid; pg < p.max_pages; pg += kTopkThreads) so[pg] = -INFINITY;
+    }
+  }
+  // every score of the cluster's rows now sits in its blocks' shared memory,
+  // which stays resident (and unchanged) until the last cluster.sync
+  cluster.sync();
+  for (int r = rank; r < NR; r += CS) {
+    __syncthreads();   // the previous row's select is done with keys
+    for (int rr = 0; rr < CS; ++rr) {
+      const float* remote = cluster.map_shared_rank(own, rr) + (size_t)r * span;
+      const int a0 = (int)((long long)P * rr / CS), a1 = (int)((long long)P * (rr + 1) / CS);
+      for (int i = a0 + tid; i < a1; i += kTopkThreads) keys[i] = __float_as_uint(remote[i - a0]);
+    }
+    __syncthreads();
+    const size_t bh = (size_t)b * rows_per_b + row0 + r;
+    select_row(keys, P, K, p.top_k, p.sel_pages + bh * p.top_k, p.sel_count + bh, hist, warp_tot, sel_digit,
+               sel_remaining);
+  }
+  cluster.sync();
 }
 
 }  // namespace
 
+// kv heads per cluster: 2 KB of boxes per page (4 heads at d = 64, 2 at 128),
+// dividing the kv heads; a cluster with per-head rows selects KBH * G rows.
+int topk_kv_heads_per_cluster(int D, int num_kv_heads) {
+  int kbh = D == 64 ? 4 : 2;
+  while (kbh > 1 && num_kv_heads % kbh != 0) kbh /= 2;
+  return kbh;
+}
+
 pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
-  const size_t smem = (size_t)p.max_pages * 4;
   const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
-  const int cs = grouped ? kTopkClusterGroup : kTopkClusterHead;
-  const void* fn;
-  if (p.head_dim == 128)
-    fn = grouped ? reinterpret_cast<const void*>(&score_topk_kernel<128, kTopkClusterGroup>)
-                 : reinterpret_cast<const void*>(&score_topk_kernel<128, kTopkClusterHead>);
+  const int kbh = topk_kv_heads_per_cluster(p.head_dim, p.num_kv_heads);
+  const int nq = kbh * p.group, nr = grouped ? kbh : nq;
+  const int span = ((p.max_pages + kTopkCluster - 1) / kTopkCluster + 3) / 4 * 4;
+  const size_t smem = ((size_t)(p.max_pages + 3) / 4 * 4 + (size_t)nr * span + (size_t)nq * p.head_dim) * 4;
+  const void* fn = nullptr;
+  if (p.head_dim == 64)
+    fn = kbh == 4 ? reinterpret_cast<const void*>(&score_topk_kernel<64, 4>)
+                  : (kbh == 2 ? reinterpret_cast<const void*>(&score_topk_kernel<64, 2>)
+                              : reinterpret_cast<const void*>(&score_topk_kernel<64, 1>));
   else
-    fn = grouped ? reinterpret_cast<const void*>(&score_topk_kernel<64, kTopkClusterGroup>)
-                 : reinterpret_cast<const void*>(&score_topk_kernel<64, kTopkClusterHead>);
+    fn = kbh == 2 ? reinterpret_cast<const void*>(&score_topk_kernel<128, 2>)
+                  : reinterpret_cast<const void*>(&score_topk_kernel<128, 1>);
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return PKV_ERR_CUDA;
+  if (smem + fa.sharedSizeBytes > (size_t)optin) return PKV_ERR_UNSUPPORTED;
   if (smem > 48 * 1024) {
-    // always the one maximum (16384 pages), never a per-call size, so a
-    // concurrent or later launch with more pages is never left below its need
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4) != cudaSuccess)
+    // always the device's maximum, never a per-call size, so a concurrent or
+    // later launch that needs more is never left below its need
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
-  const int rows = p.batch * (grouped ? p.num_kv_heads : p.num_q_heads);
-  const unsigned grid = (unsigned)(rows * cs);
+  const unsigned grid = (unsigned)(p.batch * (p.num_kv_heads / kbh) * kTopkCluster);
   TopkParams pc = p;
   void* args[] = {&pc};
   if (launch_pdl(fn, dim3(grid), dim3(kTopkThreads), smem, st, args) != cudaSuccess) return PKV_ERR_CUDA;

@@ -78,8 +78,11 @@ def run_sparse(ld, q, top_k):
     return sel.cpu().numpy(), cnt.cpu().numpy(), scores.cpu().numpy(), out.cpu().numpy()
 
 
-@pytest.mark.parametrize("d,Hq,Hkv,ps,top_k", [(64, 4, 4, 16, 5), (128, 8, 2, 32, 3), (64, 8, 4, 64, 2)])
+@pytest.mark.parametrize("d,Hq,Hkv,ps,top_k", [(64, 4, 4, 16, 5), (128, 8, 2, 32, 3), (64, 8, 4, 64, 2),
+                                               (64, 16, 4, 16, 4), (128, 32, 4, 16, 3), (64, 6, 3, 16, 2)])
 def test_small_sparse_all_outputs(d, Hq, Hkv, ps, top_k):
+    # kv heads are scored 4 (d = 64) or 2 (d = 128) per cluster when they divide
+    # the count; 16 query heads per cluster take two select rounds per block
     w = synth.Workload(name="sp", seed=900 + d + ps, batch=4, layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
                        head_dim=d, page_size=ps, dtype="f16", quant="none", seq_len=None,
                        seq_len_range=(1, 500), page_offset_std=0.5)
