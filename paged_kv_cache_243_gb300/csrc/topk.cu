@@ -1,4 +1,4 @@
-// page_score_topk: score every page of a sequence against one query head with
+// page_score_topk: score every page of a sequence against each query head with
 // the direction-aware bounding box, then keep the top-K pages [TinyServe page,
 // section 2.1 (metadata, score) and section 3.1 phases 1-2]. A row that selects
 // is a query head, or a kv head whose G query heads' scores are summed or
@@ -163,7 +163,9 @@ __device__ void select_row(uint32_t* keys, int P, int K, int top_k, int32_t* sel
 // warp per page (UNROLL pages in flight), into its shared memory; then block r
 // gathers row r's scores (rows r, r + 8, ... when NR > 8) from the cluster
 // through distributed shared memory and selects them.
-template <int D, int KBH>
+// SUM: rows are group sums (the lane partials of the G heads are added and
+// reduced once); otherwise per-head rows or group maxima.
+template <int D, int KBH, bool SUM>
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
     score_topk_kernel(const TopkParams p) {
   constexpr int CS = kTopkCluster;
@@ -179,6 +181,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const bool grouped = p.group_mode != PKV_SELECT_PER_HEAD;
+  constexpr bool sum_rows = SUM;
   const int G = p.group;
   const int NQ = KBH * G;                           // query heads scored
   const int NR = grouped ? KBH : NQ;                // rows selected
@@ -269,6 +272,11 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
           }
           sc[k] = a;
         }
+        if constexpr (sum_rows) {   // a group's sum: add the lane partials, reduce once below
+#pragma unroll
+          for (int k = 0; k < UNROLL; ++k) rowv[k] = j == 0 ? sc[k] : rowv[k] + sc[k];
+          continue;
+        }
 #pragma unroll
         for (int k = 0; k < UNROLL; ++k) {
 #pragma unroll
@@ -283,12 +291,16 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
               if (pg < pg1) own[r * span + (pg - pg0)] = ok[k] ? sc[k] : -INFINITY;
             }
           }
-        } else {
+        } else {   // a group's max
 #pragma unroll
-          for (int k = 0; k < UNROLL; ++k)
-            rowv[k] = j == 0 ? sc[k]
-                             : (p.group_mode == PKV_SELECT_GROUP_MAX ? fmaxf(rowv[k], sc[k]) : rowv[k] + sc[k]);
+          for (int k = 0; k < UNROLL; ++k) rowv[k] = j == 0 ? sc[k] : fmaxf(rowv[k], sc[k]);
         }
+      }
+      if constexpr (sum_rows) {
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k)
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) rowv[k] += __shfl_xor_sync(0xffffffffu, rowv[k], off);
       }
       if (grouped && lane == 0) {
 #pragma unroll
@@ -347,14 +359,15 @@ pkv_status launch_topk(const TopkParams& p, cudaStream_t st) {
   const int nq = kbh * p.group, nr = grouped ? kbh : nq;
   const int span = ((p.max_pages + kTopkCluster - 1) / kTopkCluster + 3) / 4 * 4;
   const size_t smem = ((size_t)(p.max_pages + 3) / 4 * 4 + (size_t)nr * span + (size_t)nq * p.head_dim) * 4;
+  const bool sum = p.group_mode == PKV_SELECT_GROUP_SUM;
   const void* fn = nullptr;
-  if (p.head_dim == 64)
-    fn = kbh == 4 ? reinterpret_cast<const void*>(&score_topk_kernel<64, 4>)
-                  : (kbh == 2 ? reinterpret_cast<const void*>(&score_topk_kernel<64, 2>)
-                              : reinterpret_cast<const void*>(&score_topk_kernel<64, 1>));
-  else
-    fn = kbh == 2 ? reinterpret_cast<const void*>(&score_topk_kernel<128, 2>)
-                  : reinterpret_cast<const void*>(&score_topk_kernel<128, 1>);
+#define PKV_TOPK(d, k)                                                                   \
+  if (p.head_dim == d && kbh == k)                                                       \
+    fn = sum ? reinterpret_cast<const void*>(&score_topk_kernel<d, k, true>)             \
+             : reinterpret_cast<const void*>(&score_topk_kernel<d, k, false>);
+  PKV_TOPK(64, 4) PKV_TOPK(64, 2) PKV_TOPK(64, 1) PKV_TOPK(128, 2) PKV_TOPK(128, 1)
+#undef PKV_TOPK
+  if (!fn) return PKV_ERR_UNSUPPORTED;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
