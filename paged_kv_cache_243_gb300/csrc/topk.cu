@@ -69,13 +69,40 @@ __device__ void select_row(uint32_t* keys, int P, int K, int top_k, int32_t* sel
     for (int i = tid; i < P; i += kTopkThreads) sel[i] = i;
     return;
   }
-  for (int i = tid; i < P; i += kTopkThreads) keys[i] = order_key(__uint_as_float(keys[i]));
+  // keys, and the bits where they all agree (AND == OR): leading bytes that
+  // every key shares need no radix pass (scores of one sign and binade share
+  // their top byte, and a pass over it would serialise P atomics on one bin)
+  uint32_t kand = 0xffffffffu, kor = 0u;
+  for (int i = tid; i < P; i += kTopkThreads) {
+    const uint32_t k = order_key(__uint_as_float(keys[i]));
+    keys[i] = k;
+    kand &= k;
+    kor |= k;
+  }
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  if (lane == 0) {
+    warp_tot[warp] = (int)kand;
+    hist[warp] = (int)kor;
+  }
   __syncthreads();
+  kand = 0xffffffffu;
+  kor = 0u;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    kand &= (uint32_t)warp_tot[w];
+    kor |= (uint32_t)hist[w];
+  }
+  __syncthreads();
+  const uint32_t diff = kand ^ kor;
+  // first pass: the byte holding the highest differing bit (all keys equal:
+  // no pass, T is that key and the K lowest pages are kept)
+  const int top_shift = diff == 0u ? -8 : (31 - __clz(diff)) / 8 * 8;
 
   // ---- radix select of the K-th largest key
-  uint32_t prefix = 0, mask = 0;
+  uint32_t mask = top_shift >= 24 ? 0u : (0xffffffffu << (top_shift + 8));
+  uint32_t prefix = kand & mask;
   int remaining = K;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = top_shift; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     for (int i = tid; i < P; i += kTopkThreads) {

@@ -205,3 +205,37 @@ def test_group_shared_selection(mode, quant, d, Hq, Hkv, ps, top_k):
                 tol = TOL["int8"] if quant != "none" else TOL["f16"]
                 assert np.abs(out[b, h] - o).max() <= tol, (b, h)
     assert int(ld.status.item()) == 0
+
+
+@pytest.mark.parametrize("d,Hkv,patterns", [(64, 4, 1), (64, 4, 3), (128, 2, 1), (128, 2, 5)])
+def test_tied_page_scores_keep_the_lowest_pages(d, Hkv, patterns):
+    # every page of a head repeats one of `patterns` token blocks, so page scores
+    # take at most that many values and tie exactly (same boxes, same arithmetic);
+    # one pattern makes every score equal. The top-K must be the pages with the
+    # higher values, ties broken by the lower page index, as in the oracle.
+    from paged_kv_cache_243_gb300.cache import PagedKVCache
+    ps, P, top_k = 16, 40, 13
+    rng = np.random.default_rng(1000 + d + patterns)
+    blocks = rng.standard_normal((patterns, ps, Hkv, d)).astype(np.float16)
+    which = rng.integers(0, patterns, size=P)
+    k = np.concatenate([blocks[which[pg]] for pg in range(P)])[None]      # [1][P ps][Hkv][d]
+    v = rng.standard_normal(k.shape).astype(np.float16)
+    pool = P + 3
+    bt = rng.permutation(pool)[:P].astype(np.int32)[None]
+    cache = PagedKVCache(pool, ps, Hkv, d, kv_dtype="f16", with_meta=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt_d = torch.from_numpy(bt).cuda()
+    cache.append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), bt_d,
+                 torch.zeros(1, dtype=torch.int32, device="cuda"), dev_status=status)
+    q = torch.from_numpy(rng.standard_normal((1, Hkv, d)).astype(np.float16)).cuda()
+    lens = torch.tensor([P * ps], dtype=torch.int32, device="cuda")
+    sel, cnt, _ = cache.score_topk(q, bt_d, lens, top_k, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    qf = q.cpu().numpy().astype(np.float64)[0]
+    for h in range(Hkv):
+        mn, mx = oracle.page_bounding_boxes(k[0][:, h:h + 1].astype(np.float64), ps)
+        r = oracle.page_scores(qf[h:h + 1], mn, mx, 1)[0]
+        assert cnt[0, h] == top_k
+        assert np.array_equal(sel[0, h], oracle.select_top_k(r, top_k)), h
