@@ -26,7 +26,8 @@
 // online-softmax state (running max m, sum l, accumulator) per query head, in
 // the log2 domain, and writes it to a workspace record whenever its chunk
 // stream leaves a unit (an empty record for units of the block's range it did
-// not see).
+// not see). The block's last unit is the exception: after the stream the four
+// warps' states meet in shared memory and the block writes one merged record.
 //
 // Merge [TinyServe page, section 3.1 phase 4]: attn_combine_kernel, the next
 // launch on the stream, folds for every unit the records of all blocks whose
