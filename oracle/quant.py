@@ -8,7 +8,7 @@ What the pages fix:
   * per-group INT8: every 64 tokens share one scale/zero-point [Gemini page,
     第一章 "KV Cache 优化核心策略"], stored as int8 [Gemini page, 第一章 code].
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * asymmetric form with a float zero-point equal to the block minimum:
         s = (max - min) / 255        (fp32 subtract, fp32 divide)
         z = min

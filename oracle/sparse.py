@@ -11,7 +11,7 @@ an upper bound on q . k for every key k of the page. The pages keep this
 metadata in fp32 [section 5.2] and keep the top-K pages [section 3.1 phase 2,
 whose body the page elides; ratio 0.3 in section 5.1].
 
-Readings (listed in the design doc): the box covers only the valid tokens of a
+Readings taken where the pages are silent: the box covers only the valid tokens of a
 partially filled page; ties in the score are broken towards the lower logical
 page index; the kept pages are returned in ascending page order; K = ceil(0.3 P)
 for the 30 % setting and is clipped to the number of pages P.
