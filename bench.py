@@ -503,6 +503,39 @@ def extra_workloads(peak: float) -> Dict:
     return res
 
 
+def sweep(peak: float) -> Dict:
+    """Attention call time over batch x context for the Llama-2-7B head shapes (bf16,
+    32 q heads over 32 or 8 kv heads, d = 128, page 16): each point is a chain of
+    attention calls over distinct layers (early start, as in the bench's step), with
+    enough layers that the chain's K/V exceed L2; points whose layer exceeds 4.3 GB
+    are skipped."""
+    import dataclasses as dc
+    import torch
+    base = synth.WORKLOADS["w2_llama7b_bf16"]
+    res = []
+    for hkv in (32, 8):
+        for B in (1, 4, 16, 64):
+            for L in (1024, 4096, 16384, 32768):
+                per_layer = B * L * hkv * base.head_dim * 2 * 2
+                if per_layer > 4.3e9:
+                    continue
+                layers = int(min(32, max(2, math.ceil(1.0e9 / per_layer))))
+                w = dc.replace(base, name="sweep", batch=B, num_kv_heads=hkv, seq_len=L, layers=layers,
+                               pool_pages=None, description="")
+                rep = Replica(w, w.seed, layers=layers)
+                ga, _ = rep.capture(append=False, attention=True)
+                ms = time_graph(ga, 20, 3) / layers
+                byts = algorithmic_bytes(w, rep.lens, append_tokens=0)["attention"]
+                res.append({"kv_heads": hkv, "batch": B, "seq_len": L, "layers": layers,
+                            "attention_us": round(ms * 1e3, 2),
+                            "gb_s": round(byts / (ms * 1e-3) / 1e9, 1),
+                            "frac_of_hbm_peak": round(byts / (ms * 1e-3) / 1e9 / peak, 4)})
+                del rep, ga
+                torch.cuda.empty_cache()
+    return {"metric": "attention call GB/s over batch x context (bf16, 32 q heads, d 128, page 16)",
+            "peak_gbs": peak, "points": res}
+
+
 # -------------------------------------------------------------- CPU baseline
 _SEQ_CACHE: Dict = {}
 
@@ -800,12 +833,21 @@ def main(argv: Optional[List[str]] = None) -> None:
                     help="attention waits for the preceding kernel before any read (fresh_rows = -1)")
     ap.add_argument("--no-fused-append", action="store_true",
                     help="the step's append is a separate kv_append launch")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print attention call times over batch x context instead of the bench line")
     args = ap.parse_args(argv)
     global EARLY_START, FUSED_APPEND
     EARLY_START = not args.no_early_start
     FUSED_APPEND = not args.no_fused_append
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.sweep:
+        import torch
+        from paged_kv_cache_243_gb300 import _build
+        _build.build()
+        torch.cuda.set_device(0)
+        print(json.dumps(sweep(load_peaks()["hbm_gbs"])), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
