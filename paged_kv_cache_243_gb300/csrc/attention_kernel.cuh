@@ -54,6 +54,8 @@ constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 // Small shared scratch: [8, 8 + warps) the unit prefix scan's warp totals.
 constexpr int kMiscInts = 32;
+constexpr int kQStageBytes = 2048;   // shared-memory copy of q for a block's first units (small: it must
+                                     // not cost a resident block per SM)
 constexpr int kMiscAbort = 24;   // misc slot: some consumer warp timed out
 
 struct AttnParams {
@@ -139,7 +141,8 @@ __host__ __device__ inline size_t attn_smem_bytes(int stage_bytes, int stages, i
   s += 32 * sizeof(ChunkInfo);
   s += kMiscInts * 4;                              // misc
   s += (size_t)(units + 1) * 4 + (size_t)batch * 4;
-  return (s + 15) / 16 * 16;
+  s = (s + 15) / 16 * 16 + kQStageBytes;           // q rows of the block's first units
+  return s;
 }
 
 // Channel index of element e of lane-slot j in the score layout.
@@ -421,6 +424,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   int* misc = reinterpret_cast<int*>(info + 32);
   int* prefix = misc + kMiscInts;
   int* lens = prefix + p.num_units + 1;
+  uint8_t* qstage = smem + ((reinterpret_cast<uintptr_t>(lens + p.batch) - reinterpret_cast<uintptr_t>(smem) + 15) & ~uintptr_t(15));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = p.num_units;
@@ -693,6 +697,30 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     return;
   }
 
+  // q of the block's first units, staged in shared memory by the consumer
+  // warps while the first copies are in flight: a unit's start then reads q
+  // there instead of waiting on global loads mid-stream (later units, beyond
+  // what kQStageBytes holds, load q as before)
+  const int q_esz = p.q_dtype == PKV_F32 ? 4 : 2;
+  const int q_unit_bytes = GE * D * q_esz;
+  const int n_staged = min(ub - ua + 1, kQStageBytes / q_unit_bytes);
+  for (int i = tid; i < n_staged * (q_unit_bytes / 16); i += NW * 32) {
+    const int k = i / (q_unit_bytes / 16), o = i - k * (q_unit_bytes / 16);
+    const int u = ua + k, b = u / p.units_per_b, hu = u - b * p.units_per_b;
+    const int qh0 = p.unit_is_q ? hu : hu * p.group;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        static_cast<const uint8_t*>(p.q) + ((size_t)b * p.num_q_heads + qh0) * D * q_esz);
+    reinterpret_cast<uint4*>(qstage + (size_t)k * q_unit_bytes)[o] = __ldg(src + o);
+  }
+  named_bar_sync(2, NW * 32);
+  // q of unit u: the staged copy, or its rows in global memory
+  auto q_of = [&](int u) -> const void* {
+    if (u - ua < n_staged) return qstage + (size_t)(u - ua) * q_unit_bytes;
+    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
+    const int qh0 = p.unit_is_q ? hu : hu * p.group;
+    return static_cast<const uint8_t*>(p.q) + ((size_t)b * p.num_q_heads + qh0) * D * q_esz;
+  };
+
   // The block's last unit ub: its four warps' states are merged here into one
   // record at slot (c + ub) * 4 (the other units keep one record per warp), so
   // the combine reads one record from each block but a unit's last. After the
@@ -799,17 +827,16 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   };
 
   auto start_unit = [&](int u) {
-    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-    const int qh0 = p.unit_is_q ? hu : hu * p.group;
+    const void* qu = q_of(u);
     float part[GE];
 #pragma unroll
     for (int h = 0; h < GE; ++h) {
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < QD2; ++e) {
-        const size_t idx = ((size_t)b * p.num_q_heads + qh0 + h) * D;
-        const float x0 = load_q_elem(p.q, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e)) * p.q_scale;
-        const float x1 = load_q_elem(p.q, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e + 1)) * p.q_scale;
+        const size_t idx = (size_t)h * D;
+        const float x0 = load_q_elem(qu, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e)) * p.q_scale;
+        const float x1 = load_q_elem(qu, p.q_dtype, idx + qk_dim<D, KV>(j, 2 * e + 1)) * p.q_scale;
         q2[h][e] = pack2f(x0, x1);
         s += x0 + x1;
       }
@@ -1033,11 +1060,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     flush_to(rec_of(u));
   };
   auto start_unit = [&](int u) {
-    const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
-    const int qh0 = hu * p.group;   // units are (sequence, kv head) on this path
-    float part = 0.f;
+    float part = 0.f;   // units are (sequence, kv head) on this path; q is 16-bit
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const uint16_t*>(p.q) + ((size_t)b * p.num_q_heads + qh0 + (g < GE ? g : 0)) * D);
+        static_cast<const uint16_t*>(q_of(u)) + (g < GE ? g : 0) * D);
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const int ch = chan(4 * kk);
