@@ -264,12 +264,18 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
       const long long blocks = units * ((outs + ob - 1) / ob);
       const long long waves = (blocks + slots - 1) / slots;
       const long long rounds = (rbar + rg * 8 - 1) / (rg * 8);
+      // (a grid of at most one block per SM releases the next launch sooner:
+      // W4 attention-only chain 34.2 -> 33.35 us with 128 blocks instead of
+      // 256, but its slower merge delays the next append: W4 step 37.8 ->
+      // 38.2 us, so the cost does not favour it)
       const long long cost = waves * (3 + rounds);
       if (best < 0 || cost < best) {
         best = cost;
         pl.comb_groups = rg;
       }
     }
+    const int forced_rg = env_int("PKV_ATTN_COMB_RG", 0);   // tuning knob
+    if (forced_rg == 1 || forced_rg == 2 || forced_rg == 4 || forced_rg == 8) pl.comb_groups = forced_rg;
   }
   const size_t rs = (size_t)rec_floats(pl.ge, c->head_dim);
   const size_t cslots = (size_t)(pl.ctas + pl.units);
