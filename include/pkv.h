@@ -203,7 +203,10 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *   out         : [batch][num_q_heads][head_dim] of out_dtype (F32/F16/BF16).
  *   num_splits  : number of cooperating thread blocks that share the work
  *                 (split-K over the whole batch's pages, each block taking an
- *                 equal share); 0 = one full wave of the device.
+ *                 equal share); 0 = automatic: one full wave of the device,
+ *                 or, for a call whose block-table width (dense) or page-list
+ *                 stride (sparse) bounds it below 4 chunks of 16 tokens per
+ *                 block of that wave, max(SMs, bound / 4) blocks.
  *   fresh_rows  : -1, or a promise that lets the call start before the
  *                 work launched just before it on `stream` (one kernel, or
  *                 both kernels of a preceding attention call) has finished:
