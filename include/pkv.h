@@ -124,6 +124,15 @@ const char* pkv_status_string(pkv_status s);
 int32_t pkv_abi_version(void);
 
 /*
+ * Re-read the tuning variables PKV_ATTN_MMA, PKV_ATTN_RING_KB, PKV_ATTN_STAGES,
+ * PKV_ATTN_CTAS_PER_SM and PKV_ATTN_COMB_RG from the environment. They only
+ * choose among equivalent launch shapes (results never depend on them) and are
+ * read once, by the first call that plans an attention launch; a process that
+ * changes them later calls this. Not part of the pages' problem statement.
+ */
+void pkv_tuning_reload(void);
+
+/*
  * kv_append — write new tokens' K and V into their pages.
  * [HBM-layout page, section 三 append_kv]: token position pos goes to logical
  * page pos / page_size, slot pos % page_size, through the block table.
@@ -287,13 +296,20 @@ pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, in
  * and allows no later cudaMalloc (which can stall every stream on the device),
  * or a plugin that only receives its input and output buffers. The pages have
  * no counterpart; this is a packaging choice of the library.
- *   Scratch: a fixed 8 MiB array inside the library's device image, present on
- *   every GPU that loads the library until the process exits. A call whose
- *   workspace (pkv_attention_workspace_bytes) exceeds 8 MiB returns
- *   PKV_ERR_WORKSPACE and launches nothing.
+ *   Scratch: a fixed 8 MiB array inside the library's device image. CUDA loads
+ *   the module holding it lazily by default, so the array's memory is taken
+ *   on a device by the first call made with that device current (or when the
+ *   context is created, if the process runs with CUDA_MODULE_LOADING=EAGER),
+ *   and held until the process exits: make that first call (it may be a
+ *   warm-up call) before reserving the rest of device memory, and before any
+ *   stream capture on that device. Later calls take no device memory.
+ *   A call whose workspace (its own plan's, as pkv_attention_workspace_bytes
+ *   gives for a full-wave split count) exceeds 8 MiB returns PKV_ERR_WORKSPACE
+ *   and launches nothing.
  *   Set-up: the first call with a given device current looks up the array's
- *   device address (cudaGetSymbolAddress); make that first call before any
- *   stream capture on that device.
+ *   device address (cudaGetSymbolAddress) and keeps it for that device; after
+ *   cudaDeviceReset on a device that address is stale, so no call may follow
+ *   a reset.
  *   Sharing: every call uses the same array, and its contents are whatever the
  *   last call left (nothing needs to start at zero). Calls that may run at the
  *   same time on the GPU (other streams, other host threads) race: issue them

@@ -22,7 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_PAGES, ERR_CUDA, ERR_WORKSPACE 
 DEV_BAD_PAGE, DEV_BAD_SELECTED, DEV_BAD_POSITION, DEV_TIMEOUT, DEV_BAD_CONFIG = 1, 2, 4, 8, 16
 
 EXPORTED = [
-    "pkv_status_string", "pkv_abi_version", "pkv_kv_append", "pkv_page_score_topk",
+    "pkv_status_string", "pkv_abi_version", "pkv_tuning_reload", "pkv_kv_append", "pkv_page_score_topk",
     "pkv_attention_workspace_bytes", "pkv_paged_decode_attention", "pkv_append_decode_attention",
     "pkv_paged_decode_attention_noalloc",
     "pkv_alloc_create", "pkv_alloc_destroy", "pkv_alloc_reserve", "pkv_alloc_free",
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "pkv_status_string": (ctypes.c_char_p, [c_int]),
         "pkv_abi_version": (i32, []),
+        "pkv_tuning_reload": (None, []),
         "pkv_kv_append": (c_int, [P, i32, i32, vp, vp, c_int, vp, i32, vp, vp, vp, vp]),
         "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, i32, vp, vp, vp, vp, vp]),
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
@@ -103,6 +104,11 @@ def status_string(status: int) -> str:
 
 def abi_version() -> int:
     return lib().pkv_abi_version()
+
+
+def tuning_reload() -> None:
+    """Re-read the PKV_ATTN_* tuning variables from the environment."""
+    lib().pkv_tuning_reload()
 
 
 def kv_append(cache: PkvCache, batch: int, t_new: int, k_new: int, v_new: int, src_dtype: int,

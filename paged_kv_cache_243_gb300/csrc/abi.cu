@@ -1,7 +1,11 @@
 // C-ABI entry points: argument checks, workspace sizing and kernel dispatch.
 // Every host-detectable error is returned before anything is launched.
+#include <cudaTypedefs.h>
+
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
 
 #include "attention_kernel.cuh"
@@ -9,13 +13,11 @@
 
 namespace pkv {
 
-int attn_stage_bytes(int kv_kind, int D) {
-  switch (kv_kind) {
-    case KV_F16:
-    case KV_BF16: return D == 128 ? AttnGeom<128, KV_F16>::STAGE : AttnGeom<64, KV_F16>::STAGE;
-    case KV_I8T: return D == 128 ? AttnGeom<128, KV_I8T>::STAGE : AttnGeom<64, KV_I8T>::STAGE;
-    default: return D == 128 ? AttnGeom<128, KV_I8G>::STAGE : AttnGeom<64, KV_I8G>::STAGE;
-  }
+int attn_stage_bytes(int kv_kind, int D, bool swz) {
+  const int esz = (kv_kind == KV_I8T || kv_kind == KV_I8G) ? 1 : 2;
+  const int kb = kChunk * D * esz;
+  const int szb = kv_kind == KV_I8T ? kChunk * 16 : (kv_kind == KV_I8G ? 16 : 0);
+  return stage_bytes_of(kb, szb, swz);
 }
 
 namespace {
@@ -26,6 +28,39 @@ int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (!v || !*v) return dflt;
   return std::atoi(v);
+}
+
+// Tuning knobs (environment variables; results never depend on them). They
+// are read from the environment once, at the first call that plans an
+// attention launch, and again only on pkv_tuning_reload(), so a call does no
+// getenv and a concurrent setenv cannot race with one.
+struct Tuning {
+  int mma = 1;            // PKV_ATTN_MMA=0: CUDA-core consumers for query-head groups
+  int ring_kb = 64;       // PKV_ATTN_RING_KB: ring size per block
+  int stages = 0;         // PKV_ATTN_STAGES: explicit stage count (rounded to a multiple of 4)
+  int ctas_per_sm = 0;    // PKV_ATTN_CTAS_PER_SM: cap on resident blocks per SM
+  int comb_rg = 0;        // PKV_ATTN_COMB_RG: record groups of the combine (1, 2, 4 or 8)
+};
+
+std::mutex g_tuning_mu;
+Tuning g_tuning;
+bool g_tuning_read = false;
+
+void read_tuning_locked() {
+  Tuning t;
+  t.mma = env_int("PKV_ATTN_MMA", 1);
+  t.ring_kb = env_int("PKV_ATTN_RING_KB", 64);
+  t.stages = env_int("PKV_ATTN_STAGES", 0);
+  t.ctas_per_sm = env_int("PKV_ATTN_CTAS_PER_SM", 0);
+  t.comb_rg = env_int("PKV_ATTN_COMB_RG", 0);
+  g_tuning = t;
+  g_tuning_read = true;
+}
+
+Tuning tuning() {
+  std::lock_guard<std::mutex> lk(g_tuning_mu);
+  if (!g_tuning_read) read_tuning_locked();
+  return g_tuning;
 }
 
 struct DeviceInfo {
@@ -149,14 +184,15 @@ const void* attn_kernel(int kind, int D, int ge, bool mma) {
 // The tensor-core variant serves dense query-head groups (G >= 2) when q has
 // the dtype of the products' operands: fp16 for fp16 and INT8 caches (codes
 // enter as exact fp16 integers), bf16 for bf16 caches.
-bool use_mma(int kind, int ge, int q_dtype) {
-  if (ge < 2 || env_int("PKV_ATTN_MMA", 1) == 0) return false;
+bool use_mma(int kind, int ge, int q_dtype, const Tuning& tn) {
+  if (ge < 2 || tn.mma == 0) return false;
   return kind == KV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16;
 }
 
 struct AttnPlan {
   const void* fn = nullptr;
   bool mma = false;
+  bool swz = false;   // swizzled tensor-copy staging (tensor-core INT8 at head_dim 128)
   int ge = 1, units = 0, stages = 0, ctas = 0;
   size_t smem = 0;
   size_t off_wrec = 0, ws_bytes = 0;
@@ -164,6 +200,55 @@ struct AttnPlan {
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Tensor maps of the K and V pools for the swizzled tensor-core INT8 variant:
+// each pool as a 2-D tensor [num_pages * Hkv * page_size rows][128 bytes],
+// copied in boxes of 16 rows x 128 bytes with the 128-byte swizzle. The
+// encoding is plain data (no context state); it is made once per (pool
+// address, rows) through the driver's cuTensorMapEncodeTiled, looked up with
+// cudaGetDriverEntryPointByVersion so the library does not link the driver.
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+pkv_status pool_tensor_map(const void* base, uint64_t rows, CUtensorMap& out) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, uint64_t>, CUtensorMap> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_pair(base, rows);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    out = it->second;
+    return PKV_OK;
+  }
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return PKV_ERR_CUDA;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)kChunk};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PKV_ERR_CUDA;
+  if (cache.size() >= 256) cache.clear();
+  cache[key] = m;
+  out = m;
+  return PKV_OK;
+}
 
 // q_dtype < 0: size the workspace for whichever kernel variant a call may use.
 // sparse: 0 dense, 1 page lists per query head, 2 one page list per kv head shared by its group.
@@ -180,7 +265,8 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   if (pl.ge != 1 && pl.ge != 2 && pl.ge != 4 && pl.ge != 8) return PKV_ERR_UNSUPPORTED;
   pl.units = batch * (sparse == 1 ? num_q_heads : c->num_kv_heads);
   const int kind = kv_kind(c);
-  pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, q_dtype);
+  const Tuning tn = tuning();
+  pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, q_dtype, tn);
   pl.fn = attn_kernel(kind, c->head_dim, pl.ge, pl.mma);
   if (!pl.fn) return PKV_ERR_UNSUPPORTED;
   DeviceInfo di;
@@ -190,10 +276,12 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   // takes chunks w, w + 4, ..., so every stage is then read by one warp only and
   // that warp waits on the stage's phases strictly in order. (A parity wait on a
   // phase two ahead of the barrier's current phase would pass at once.)
-  const int stage = attn_stage_bytes(kind, c->head_dim);
-  const int ring_kb = env_int("PKV_ATTN_RING_KB", 64);
+  pl.swz = pl.mma && (kind == KV_I8T || kind == KV_I8G) && c->head_dim == 128;
+  const int stage = attn_stage_bytes(kind, c->head_dim, pl.swz);
+  const size_t slack = pl.swz ? kSwizzleAlign : 0;   // the ring is moved to a 1024-byte boundary
+  const int ring_kb = tn.ring_kb > 0 ? tn.ring_kb : 64;
   int stages = (ring_kb * 1024) / stage;
-  const int forced = env_int("PKV_ATTN_STAGES", 0);
+  const int forced = tn.stages;
   if (forced > 0) stages = forced;
   stages = stages / kConsumerWarps * kConsumerWarps;
   stages = stages < kConsumerWarps ? kConsumerWarps : (stages > 32 ? 32 : stages);
@@ -205,10 +293,10 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   if (min_stages < kConsumerWarps) min_stages = kConsumerWarps;
   if (min_stages > 32) return PKV_ERR_UNSUPPORTED;
   if (stages < min_stages) stages = min_stages;
-  size_t smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
+  size_t smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch) + slack;
   while (smem > (size_t)di.max_smem_optin && stages > min_stages) {
     stages -= kConsumerWarps;
-    smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch);
+    smem = attn_smem_bytes(stage, stages, pl.ge, pl.units, batch) + slack;
   }
   if (smem > (size_t)di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
   if (stages % kConsumerWarps != 0) return PKV_ERR_UNSUPPORTED;
@@ -223,7 +311,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     // -2.6 %). Smaller chunks and the tensor-core consumers want 3.
     auto blocks_per_sm = [&](const void* fn, bool mma, int& nb) {
       pkv_status r = prepare_kernel(fn, kAttnThreads, smem, nb);
-      int cap = env_int("PKV_ATTN_CTAS_PER_SM", 0);
+      int cap = tn.ctas_per_sm;
       if (cap <= 0 && !mma && stage >= 8192) cap = 2;
       if (cap > 0 && cap < nb) nb = cap;
       return r;
@@ -274,7 +362,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
         pl.comb_groups = rg;
       }
     }
-    const int forced_rg = env_int("PKV_ATTN_COMB_RG", 0);   // tuning knob
+    const int forced_rg = tn.comb_rg;
     if (forced_rg == 1 || forced_rg == 2 || forced_rg == 4 || forced_rg == 8) pl.comb_groups = forced_rg;
   }
   const size_t rs = (size_t)rec_floats(pl.ge, c->head_dim);
@@ -306,6 +394,11 @@ const char* pkv_status_string(pkv_status s) {
 }
 
 int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+void pkv_tuning_reload(void) {
+  std::lock_guard<std::mutex> lk(g_tuning_mu);
+  read_tuning_locked();
+}
 
 size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                      int32_t sparse, int32_t num_splits) {
@@ -356,7 +449,15 @@ pkv_status attention_impl(const pkv_cache* cache, int32_t batch, int32_t num_q_h
   st = prepare_kernel(pl.fn, kAttnThreads, pl.smem, nb);
   if (st != PKV_OK) return st;
 
-  AttnParams p;
+  AttnParams p = {};
+  if (pl.swz) {
+    // tensor-copy row coordinates are 32-bit signed
+    const uint64_t rows = (uint64_t)cache->num_pages * cache->num_kv_heads * cache->page_size;
+    if (rows >= (1ull << 31)) return PKV_ERR_UNSUPPORTED;
+    st = pool_tensor_map(cache->k_pages, rows, p.tmap_k);
+    if (st == PKV_OK) st = pool_tensor_map(cache->v_pages, rows, p.tmap_v);
+    if (st != PKV_OK) return st;
+  }
   p.k_pages = static_cast<const uint8_t*>(cache->k_pages);
   p.v_pages = static_cast<const uint8_t*>(cache->v_pages);
   p.kv_sz = cache->kv_sz;

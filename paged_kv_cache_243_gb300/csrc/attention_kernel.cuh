@@ -59,6 +59,11 @@ constexpr int kQStageBytes = 2048;   // shared-memory copy of q for a block's fi
 constexpr int kMiscAbort = 24;   // misc slot: some consumer warp timed out
 
 struct AttnParams {
+  // K and V pools as 2-D tensors [num_pages * Hkv * page_size rows][128 bytes]
+  // with 128-byte swizzle, for the tensor-core INT8 variant at head_dim 128
+  // (which copies each chunk as two 16-row tiles); unused by the others
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   const uint8_t* k_pages;
   const uint8_t* v_pages;
   const float* kv_sz;
@@ -108,6 +113,7 @@ struct ChunkInfo {
   int valid;
   int fresh;  // overlaps rows the preceding kernel may still be writing
   int last;   // the unit's last chunk (holds position seq_len - 1), dense only
+  int row;    // pool row of the chunk's first token (tensor-copy coordinate)
 };
 
 template <int D, int KV>
@@ -119,7 +125,21 @@ struct AttnGeom {
   static constexpr int STAGE = ((2 * KB + SZB) + 127) / 128 * 128;
   static constexpr int QD = D / 8;                 // channels per lane in the score layout
   static constexpr int PD = D / 32;                // channels per lane in the value layout
+  // The tensor-core variant of INT8 caches at head_dim 128 stages K and V as
+  // tiles of 16 rows x 128 bytes with the 128-byte swizzle (16-byte block j of
+  // row r lands at block j ^ (r % 8)), which makes its fragment loads free of
+  // bank conflicts; its ring stages hold the two tiles (1024-byte aligned) and
+  // the scales sit in a separate array.
+  static constexpr bool SWZ_OK = ESZ == 1 && D == 128;
+  static constexpr int TILE_STAGE = 2 * KB;
 };
+
+// Bytes of shared memory per ring stage, and extra alignment slack, of a
+// kernel variant (swz: the swizzled tensor-core INT8 variant).
+__host__ __device__ constexpr int stage_bytes_of(int kb, int szb, bool swz) {
+  return swz ? 2 * kb + szb : ((2 * kb + szb) + 127) / 128 * 128;
+}
+constexpr int kSwizzleAlign = 1024;
 
 template <int GE>
 struct AttnSmem {
@@ -272,19 +292,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // Two bytes of a sign-flipped INT8 word (selected by sel: 0x4140 -> bytes 0, 1;
-// 0x4342 -> bytes 2, 3) as the fp16 pair (u0, u1): 0x64xx is the fp16 value
-// 1024 + xx, and subtracting 1024 is exact.
-__device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t wflip, uint32_t sel) {
+// 0x4342 -> bytes 2, 3) as the centred codes (u0 - 128, u1 - 128) in fp16:
+// 0x64xx is the fp16 value 1024 + xx, and subtracting 1152 is exact.
+__device__ __forceinline__ uint32_t u8x2_to_h2c(uint32_t wflip, uint32_t sel) {
   const uint32_t h = __byte_perm(wflip, 0x64646464u, sel);
   uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64006400u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
   return r;
-}
-
-// The same pair left as 1024 + u (no subtraction): for the values of P.V,
-// where the 1024 offset is removed through the zero-point sum instead.
-__device__ __forceinline__ uint32_t u8x2_to_h2_biased(uint32_t wflip, uint32_t sel) {
-  return __byte_perm(wflip, 0x64646464u, sel);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -406,17 +420,25 @@ __device__ __forceinline__ void append_token_row(const AttnParams& p, int u, int
 // The tensor-core variant is held to 3 resident blocks per SM (<= 136 registers)
 // so that 12 consumer warps hide its per-chunk latency.
 template <int D, int GE, int KV, bool MMA>
-__global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
+    paged_attention_kernel(const __grid_constant__ AttnParams p) {
   using Geo = AttnGeom<D, KV>;
-  constexpr int QD = Geo::QD, PD = Geo::PD, KB = Geo::KB, SZB = Geo::SZB, STAGE = Geo::STAGE;
+  constexpr int QD = Geo::QD, PD = Geo::PD, KB = Geo::KB, SZB = Geo::SZB;
+  // swizzled K/V tiles (tensor copies), scales in their own array
+  constexpr bool SWZ = MMA && Geo::SWZ_OK;
+  constexpr int STAGE = SWZ ? Geo::TILE_STAGE : Geo::STAGE;   // ring stride
   constexpr int PBUF = AttnSmem<GE>::PBUF;
   constexpr int DUP = 8 / GE;  // lanes (per token) that hold the same head after the scatter
   constexpr int NW = kConsumerWarps;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.stages;
-  uint8_t* ring = smem;
-  int4* hdr = reinterpret_cast<int4*>(smem + (size_t)S * STAGE);
+  // the swizzle pattern follows shared-memory address bits 7-9, so swizzled
+  // tiles start on a 1024-byte boundary (the host adds that much slack)
+  uint8_t* ring = SWZ ? smem + ((kSwizzleAlign - (smem_u32(smem) & (kSwizzleAlign - 1))) & (kSwizzleAlign - 1))
+                      : smem;
+  uint8_t* szring = ring + (size_t)S * STAGE;               // swizzled variant: S x SZB scale bytes
+  int4* hdr = reinterpret_cast<int4*>(szring + (SWZ ? (size_t)S * SZB : 0));
   uint64_t* full = reinterpret_cast<uint64_t*>(hdr + S);
   uint64_t* empty = full + S;
   float* pbuf_all = reinterpret_cast<float*>(empty + S);
@@ -567,7 +589,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     };
     auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
       ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
-      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0; ci.last = 0;
+      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0; ci.last = 0; ci.row = 0;
       if (r.u < 0) return;
       const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
       const int L = lens[b];
@@ -594,6 +616,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       const size_t row0 = ((size_t)phys * p.num_kv_heads + g) * ps + off;
       ci.k = p.k_pages + row0 * Geo::ROW;
       ci.v = p.v_pages + row0 * Geo::ROW;
+      ci.row = (int)row0;   // the host keeps pool rows below 2^31 for tensor copies
       if constexpr (KV == KV_I8T) ci.sz = p.kv_sz + row0 * 4;
       if constexpr (KV == KV_I8G)
         ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
@@ -663,9 +686,15 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
             if (e.valid) {
               uint8_t* st = ring + (size_t)s * STAGE;
               mbar_arrive_expect_tx(fb, 2 * KB + SZB);
-              bulk_g2s(smem_u32(st), e.k, KB, fb, pol);
-              bulk_g2s(smem_u32(st + KB), e.v, KB, fb, pol);
-              if constexpr (SZB > 0) bulk_g2s(smem_u32(st + 2 * KB), e.sz, SZB, fb, pol);
+              if constexpr (SWZ) {
+                tma_load_2d(smem_u32(st), &p.tmap_k, 0, e.row, fb, pol);
+                tma_load_2d(smem_u32(st + KB), &p.tmap_v, 0, e.row, fb, pol);
+                bulk_g2s(smem_u32(szring + (size_t)s * SZB), e.sz, SZB, fb, pol);
+              } else {
+                bulk_g2s(smem_u32(st), e.k, KB, fb, pol);
+                bulk_g2s(smem_u32(st + KB), e.v, KB, fb, pol);
+                if constexpr (SZB > 0) bulk_g2s(smem_u32(st + 2 * KB), e.sz, SZB, fb, pol);
+              }
             } else {
               mbar_arrive(fb);
             }
@@ -986,10 +1015,19 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   // ============================================== consumers, tensor-core path
   // Thread (g = lane / 4, t = lane % 4). Scores: C fragment of the [16 tok] x
   // [8 head] product, i.e. tokens g and g + 8, heads 2t and 2t + 1. The channel
-  // axis is permuted so that thread t reads whole 16-byte blocks t, t + 4, ...
-  // of a row. Values: O^T [16 channels] x [8 heads] per m-tile; thread (g, t)
-  // owns channels [g D/8, (g + 1) D/8) of every output head 2t, 2t + 1, and
-  // tokens 4t .. 4t + 3 of the chunk enter the product's k slots.
+  // axis is permuted so that thread t reads whole 16-byte blocks of a row:
+  // blocks t, t + 4, ... or, with swizzled tiles, blocks 2t and 2t + 1.
+  // Values: O^T [16 channels] x [8 heads] per m-tile; thread (g, t) owns
+  // channels [g D/8, (g + 1) D/8) of every output head 2t, 2t + 1, and tokens
+  // 4t .. 4t + 3 (swizzled tiles: 2t, 2t + 1, 2t + 8, 2t + 9) of the chunk
+  // enter the product's k slots. With swizzled tiles every quarter-warp of a
+  // fragment load touches 8 distinct 16-byte blocks: no bank conflicts.
+  // INT8 K codes enter q.K^T centred (c = u - 128, exact in fp16).
+  //
+  // Each chunk's P.V goes into a zeroed MMA accumulator, and the running state
+  // takes it with one fp32 fma (acc = acc * alpha + chunk): the tensor cores'
+  // fp32 accumulation is not IEEE round-to-nearest, and a running sum kept in
+  // the MMA accumulator drifts with the number of chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
   constexpr int ESZ = Geo::ESZ;
   constexpr int E = 16 / ESZ;                 // channels per 16-byte block
@@ -1003,7 +1041,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
   constexpr bool PACK = GE <= 4;
   const int g = lane >> 2, t = lane & 3;
   float* pb = pbuf_all + warp * PBUF;
-  auto chan = [&](int i) { return (t + 4 * (i / E)) * E + (i % E); };
+  // logical 16-byte block m (of NB) of a row that thread t reads, and where a
+  // logical block of row r sits in shared memory
+  auto kblock = [&](int m) { return SWZ ? 2 * t + m : t + 4 * m; };
+  auto phys_block = [&](int r, int blk) { return SWZ ? (blk ^ (r & 7)) : blk; };
+  auto chan = [&](int i) { return kblock(i / E) * E + (i % E); };
+  // V rows (tokens) of k slots 2t, 2t + 1, 2t + 8, 2t + 9 of this thread
+  auto vtok = [&](int jr) { return SWZ ? 2 * t + (jr & 1) + 8 * (jr >> 1) : 4 * t + jr; };
 
   uint32_t qb[KS][2];
   float qs[2];
@@ -1109,7 +1153,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
     }
     if (h4.z) {
       const int nvalid = h4.y;
-      const float* sz = reinterpret_cast<const float*>(st + 2 * KB);
+      const float* sz = reinterpret_cast<const float*>(SWZ ? szring + (size_t)s * SZB : st + 2 * KB);
       // ---- q.K^T on the tensor cores (even and odd k-steps in two
       // accumulators: two dependent MMA chains of half the length)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1118,8 +1162,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         uint4 k0[NB], k1[NB];
 #pragma unroll
         for (int m = 0; m < NB; ++m) {
-          k0[m] = *reinterpret_cast<const uint4*>(st + g * Geo::ROW + (t + 4 * m) * 16);
-          k1[m] = *reinterpret_cast<const uint4*>(st + (g + 8) * Geo::ROW + (t + 4 * m) * 16);
+          k0[m] = *reinterpret_cast<const uint4*>(st + g * Geo::ROW + phys_block(g, kblock(m)) * 16);
+          k1[m] = *reinterpret_cast<const uint4*>(st + (g + 8) * Geo::ROW + phys_block(g + 8, kblock(m)) * 16);
         }
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
@@ -1129,10 +1173,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
           if constexpr (ESZ == 1) {
             const uint32_t w0 = word_of(k0[m], wi) ^ 0x80808080u;
             const uint32_t w1 = word_of(k1[m], wi) ^ 0x80808080u;
-            a0 = u8x2_to_h2(w0, 0x4140u);
-            a2 = u8x2_to_h2(w0, 0x4342u);
-            a1 = u8x2_to_h2(w1, 0x4140u);
-            a3 = u8x2_to_h2(w1, 0x4342u);
+            a0 = u8x2_to_h2c(w0, 0x4140u);
+            a2 = u8x2_to_h2c(w0, 0x4342u);
+            a1 = u8x2_to_h2c(w1, 0x4140u);
+            a3 = u8x2_to_h2c(w1, 0x4342u);
           } else {
             a0 = word_of(k0[m], wi);
             a2 = word_of(k0[m], wi + 1);
@@ -1152,20 +1196,23 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       if constexpr (KV == KV_I8T) {
         const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
         const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
-        sc[0] = fmaf(z0.x, sc[0], z0.y * qs[0]);
-        sc[1] = fmaf(z0.x, sc[1], z0.y * qs[1]);
-        sc[2] = fmaf(z1.x, sc[2], z1.y * qs[0]);
-        sc[3] = fmaf(z1.x, sc[3], z1.y * qs[1]);
-        // V codes enter P.V as 1024 + u: vs (1024 + u) + (vz - 1024 vs) = vs u + vz
-        vs0 = z0.z; vz0 = fmaf(-1024.f, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(-1024.f, z1.z, z1.w);
+        // centred codes: s (u - 128) + (z + 128 s) = s u + z
+        const float kc0 = fmaf(128.f, z0.x, z0.y), kc1 = fmaf(128.f, z1.x, z1.y);
+        sc[0] = fmaf(z0.x, sc[0], kc0 * qs[0]);
+        sc[1] = fmaf(z0.x, sc[1], kc0 * qs[1]);
+        sc[2] = fmaf(z1.x, sc[2], kc1 * qs[0]);
+        sc[3] = fmaf(z1.x, sc[3], kc1 * qs[1]);
+        // V codes enter P.V centred: vs (u - 128) + (vz + 128 vs) = vs u + vz
+        vs0 = z0.z; vz0 = fmaf(128.f, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(128.f, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
         const float4 z = *reinterpret_cast<const float4*>(sz);
-        sc[0] = fmaf(z.x, sc[0], z.y * qs[0]);
-        sc[1] = fmaf(z.x, sc[1], z.y * qs[1]);
-        sc[2] = fmaf(z.x, sc[2], z.y * qs[0]);
-        sc[3] = fmaf(z.x, sc[3], z.y * qs[1]);
+        const float kc = fmaf(128.f, z.x, z.y);   // centred codes, as for per-token scales
+        sc[0] = fmaf(z.x, sc[0], kc * qs[0]);
+        sc[1] = fmaf(z.x, sc[1], kc * qs[1]);
+        sc[2] = fmaf(z.x, sc[2], kc * qs[0]);
+        sc[3] = fmaf(z.x, sc[3], kc * qs[1]);
         vs0 = vs1 = z.z;
-        vz0 = vz1 = fmaf(-1024.f, z.z, z.w);   // as for per-token scales
+        vz0 = vz1 = fmaf(128.f, z.z, z.w);   // centred codes, as for per-token scales
       }
       const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
 #pragma unroll
@@ -1207,42 +1254,53 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
       pb[(2 * t) * kChunk + g + 8] = pw[2];
       pb[(2 * t + 1) * kChunk + g + 8] = pw[3];
       __syncwarp();
-      // B column g: head g (hi part), or with PACK the lo part of head g - GE
+      // B column g: head g (hi part), or with PACK the lo part of head g - GE;
+      // its k slots are the tokens vtok(0 .. 3)
       const int hb = (PACK && g >= GE) ? g - GE : g;
-      float4 pv4 = *reinterpret_cast<const float4*>(pb + (hb < GE ? hb : 0) * kChunk + 4 * t);   // tokens 4t..4t+3
+      const float* pbh = pb + (hb < GE ? hb : 0) * kChunk;
+      float2 pv01, pv23;
+      if constexpr (SWZ) {
+        pv01 = *reinterpret_cast<const float2*>(pbh + 2 * t);
+        pv23 = *reinterpret_cast<const float2*>(pbh + 2 * t + 8);
+      } else {
+        const float4 pv4 = *reinterpret_cast<const float4*>(pbh + 4 * t);
+        pv01 = make_float2(pv4.x, pv4.y);
+        pv23 = make_float2(pv4.z, pv4.w);
+      }
       __syncwarp();
-      if (g >= (PACK ? 2 * GE : GE)) pv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g >= (PACK ? 2 * GE : GE)) {
+        pv01 = make_float2(0.f, 0.f);
+        pv23 = make_float2(0.f, 0.f);
+      }
       uint32_t bh0, bl0, bh1, bl1;
-      split_hi_lo<BF>(pv4.x, pv4.y, bh0, bl0);
-      split_hi_lo<BF>(pv4.z, pv4.w, bh1, bl1);
+      split_hi_lo<BF>(pv01.x, pv01.y, bh0, bl0);
+      split_hi_lo<BF>(pv23.x, pv23.y, bh1, bl1);
       if (PACK && g >= GE) {
         bh0 = bl0;
         bh1 = bl1;
       }
-      // ---- P.V on the tensor cores. The accumulator is rescaled only when
-      // the running max of some head of the warp grew on this chunk.
-      if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
-        float a0 = al[0], a1 = al[1];
-        if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
-          const int src = t >= GE / 2 ? lane - GE / 2 : lane;
-          a0 = __shfl_sync(0xffffffffu, al[0], src);
-          a1 = __shfl_sync(0xffffffffu, al[1], src);
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          acc[mt][0] *= a0;
-          acc[mt][2] *= a0;
-          acc[mt][1] *= a1;
-          acc[mt][3] *= a1;
-        }
+      // ---- P.V on the tensor cores, into a zeroed accumulator per m-tile;
+      // the running state takes it as acc = acc * alpha + chunk (fp32 fma)
+      float a0s = al[0], a1s = al[1];
+      if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
+        const int src = t >= GE / 2 ? lane - GE / 2 : lane;
+        a0s = __shfl_sync(0xffffffffu, al[0], src);
+        a1s = __shfl_sync(0xffffffffu, al[1], src);
       }
+      auto fold = [&](int mt, const float (&d)[4]) {
+        acc[mt][0] = fmaf(acc[mt][0], a0s, d[0]);
+        acc[mt][1] = fmaf(acc[mt][1], a1s, d[1]);
+        acc[mt][2] = fmaf(acc[mt][2], a0s, d[2]);
+        acc[mt][3] = fmaf(acc[mt][3], a1s, d[3]);
+      };
       const uint8_t* vrow = st + KB;
       if constexpr (ESZ == 1) {
-        // int8: dims [g DPT, (g+1) DPT) of tokens 4t .. 4t+3 (DPT bytes per row)
+        // int8: dims [g DPT, (g+1) DPT) of tokens vtok(0 .. 3) (DPT bytes per row)
         uint32_t rw[4][DPT / 4];
 #pragma unroll
         for (int jr = 0; jr < 4; ++jr) {
-          const uint8_t* src = vrow + (4 * t + jr) * Geo::ROW + g * DPT;
+          const int r = vtok(jr);
+          const uint8_t* src = vrow + r * Geo::ROW + phys_block(r, g) * DPT;
           if constexpr (DPT == 16) {
             const uint4 v = *reinterpret_cast<const uint4*>(src);
             rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
@@ -1253,24 +1311,30 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
           }
         }
         // Masked tokens (stale codes) need no clearing: every code is a
-        // finite 1024 + u and their weights are exactly 0.
+        // finite u - 128 and their weights are exactly 0. The codes enter
+        // centred, not as 1024 + u, because weights p * vs below fp16's range
+        // are lost in the hi/lo split: with a 1024 offset each lost weight
+        // would drop 1024 p vs from the product while the fp32 zero-point sum
+        // still removes it, a bias that grows with the tokens a warp streams.
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int wi = mt / 2;
           const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
           const uint32_t t01 = __byte_perm(rw[0][wi], rw[1][wi], sel);
           const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
-          const uint32_t a0 = u8x2_to_h2_biased(t01, 0x4140u), a1 = u8x2_to_h2_biased(t01, 0x4342u);
-          const uint32_t a2 = u8x2_to_h2_biased(t23, 0x4140u), a3 = u8x2_to_h2_biased(t23, 0x4342u);
-          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
-          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+          const uint32_t a0 = u8x2_to_h2c(t01, 0x4140u), a1 = u8x2_to_h2c(t01, 0x4342u);
+          const uint32_t a2 = u8x2_to_h2c(t23, 0x4140u), a3 = u8x2_to_h2c(t23, 0x4342u);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
+          fold(mt, d);
         }
       } else {
-        // fp16 / bf16: dims [g DPT, (g+1) DPT) of tokens 4t .. 4t+3 (2 DPT bytes per row)
+        // fp16 / bf16: dims [g DPT, (g+1) DPT) of tokens vtok(0 .. 3) (2 DPT bytes per row)
         uint32_t rw[4][DPT / 2];
 #pragma unroll
         for (int jr = 0; jr < 4; ++jr) {
-          const uint8_t* src = vrow + (4 * t + jr) * Geo::ROW + g * DPT * 2;
+          const uint8_t* src = vrow + vtok(jr) * Geo::ROW + g * DPT * 2;
 #pragma unroll
           for (int q4 = 0; q4 < DPT / 8; ++q4) {
             const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
@@ -1281,7 +1345,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
         if (nvalid < kChunk) {   // masked tokens may hold NaN; weight 0 would not clear it
 #pragma unroll
           for (int jr = 0; jr < 4; ++jr)
-            if (4 * t + jr >= nvalid)
+            if (vtok(jr) >= nvalid)
 #pragma unroll
               for (int i = 0; i < DPT / 2; ++i) rw[jr][i] = 0u;
         }
@@ -1291,8 +1355,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1) paged_attention_ker
           const uint32_t a1 = __byte_perm(rw[0][mt], rw[1][mt], 0x7632u);
           const uint32_t a2 = __byte_perm(rw[2][mt], rw[3][mt], 0x5410u);
           const uint32_t a3 = __byte_perm(rw[2][mt], rw[3][mt], 0x7632u);
-          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
-          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
+          fold(mt, d);
         }
       }
     }

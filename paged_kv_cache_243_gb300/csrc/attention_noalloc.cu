@@ -9,11 +9,15 @@
 // buffers by a framework that owns the allocator. This entry point takes its
 // workspace from a fixed array in the library's own device memory instead.
 //
-// The array is a file-scope __device__ array of kNoallocScratchBytes; every GPU
-// that loads the library holds it until the process exits. Its device address
-// is looked up once per device, on the first call made with that device
-// current. All calls share the one array, so calls that can overlap on the GPU
+// The array is a file-scope __device__ array of kNoallocScratchBytes. CUDA
+// loads the module that holds it lazily by default: its memory is taken on a
+// device by the first call made with that device current (the call that looks
+// up the array's device address), or when the context is created if the
+// process runs with CUDA_MODULE_LOADING=EAGER, and held until the process
+// exits. All calls share the one array, so calls that can overlap on the GPU
 // (different streams, or different host threads) race and must not be issued.
+// The looked-up address is kept per device; after cudaDeviceReset on a device
+// it is stale, so no call may follow a reset.
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -57,14 +61,13 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache* cache, int32_t ba
                                               int32_t sel_stride, int32_t sel_shared, void* out,
                                               pkv_dtype out_dtype, int32_t num_splits,
                                               int32_t* dev_status, void* stream) {
-  const int32_t mode = sel_pages == nullptr ? 0 : (sel_shared ? 2 : 1);
-  const size_t need = pkv_attention_workspace_bytes(cache, batch, num_q_heads, mode, num_splits);
-  if (need == 0) return PKV_ERR_INVALID_ARG;
-  if (need > pkv::kNoallocScratchBytes) return PKV_ERR_WORKSPACE;
   void* scratch = nullptr;
   const pkv_status st = pkv::scratch_address(&scratch);
   if (st != PKV_OK) return st;
-  // The workspace needs no initial contents, so nothing is cleared here.
+  // The attention call checks the workspace its own plan needs against the
+  // array's size and returns PKV_ERR_WORKSPACE, before launching anything, for
+  // a call that needs more. The workspace needs no initial contents, so
+  // nothing is cleared here.
   return pkv_paged_decode_attention(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table,
                                     max_pages, seq_lens, sel_pages, sel_count, sel_stride, sel_shared,
                                     out, out_dtype, num_splits, -1, scratch,

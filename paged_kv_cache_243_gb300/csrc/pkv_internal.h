@@ -47,7 +47,7 @@ const void* attn_kernel_i8t(int D, int GE, bool mma);
 const void* attn_kernel_i8g(int D, int GE, bool mma);
 
 // Bytes of one shared-memory stage (a 16-token chunk of K and V plus its INT8
-// scales), by KV kind and head_dim.
-int attn_stage_bytes(int kv_kind, int D);
+// scales), by KV kind and head_dim; swz: the swizzled tensor-copy staging.
+int attn_stage_bytes(int kv_kind, int D, bool swz);
 
 }  // namespace pkv

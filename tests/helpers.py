@@ -21,6 +21,16 @@ from oracle.quant import (per_group_bbox_values, per_group_dequant, per_token_bb
 TOL = {"bf16": 2e-3, "f16": 1e-3, "int8": 1e-3}
 
 
+def set_knobs(monkeypatch, **env) -> None:
+    """Set PKV_ATTN_* tuning variables for one test and make the library re-read
+    them (it reads them once per process otherwise); the conftest fixture
+    re-reads them after the test, once monkeypatch has restored the environment."""
+    from paged_kv_cache_243_gb300 import binding as B
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    B.tuning_reload()
+
+
 def torch_dtype(name: str):
     return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
 
@@ -157,3 +167,36 @@ def oracle_dense(ld: Loaded, qf: np.ndarray, units=None) -> dict:
 
 def max_abs_err(gpu_out: np.ndarray, ref: dict) -> float:
     return max(float(np.abs(gpu_out[b, h].astype(np.float64) - o).max()) for (b, h), o in ref.items())
+
+
+def pools(ld):
+    c = ld.cache
+    return (c.k_pages.cpu().numpy(), c.v_pages.cpu().numpy(), c.kv_sz.cpu().numpy())
+
+
+def check_per_token_codes(ld):
+    kp, vp, sz = pools(ld)
+    ps = ld.w.page_size
+    for b in range(ld.w.batch):
+        L = int(ld.lens[b])
+        for x, pool, col in ((ld.seqs[b].k, kp, 0), (ld.seqs[b].v, vp, 2)):
+            c, s, z = oracle.quantize_per_token(x)
+            assert np.array_equal(gather(pool, ld.bt[b], L, ps), c)
+            g = gather(sz, ld.bt[b], L, ps)             # [L][Hkv][4]
+            assert np.array_equal(g[:, :, col].view(np.uint32), s.view(np.uint32))
+            assert np.array_equal(g[:, :, col + 1].view(np.uint32), z.view(np.uint32))
+
+
+def check_per_group_codes(ld):
+    kp, vp, sz = pools(ld)
+    ps = ld.w.page_size
+    for b in range(ld.w.batch):
+        L = int(ld.lens[b])
+        for x, pool, col in ((ld.seqs[b].k, kp, 0), (ld.seqs[b].v, vp, 2)):
+            c, s, z = oracle.quantize_per_group(x)
+            assert np.array_equal(gather(pool, ld.bt[b], L, ps), c)
+            ng = s.shape[0]
+            t0 = np.arange(ng) * 64
+            gs = sz[ld.bt[b][t0 // ps], :, (t0 % ps) // 64]   # [ng][Hkv][4]
+            assert np.array_equal(gs[:, :, col].view(np.uint32), s.view(np.uint32))
+            assert np.array_equal(gs[:, :, col + 1].view(np.uint32), z.view(np.uint32))

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from helpers import TOL, bits_to_torch, gather, load_workload, queries_dev
+from helpers import TOL, bits_to_torch, gather, load_workload, queries_dev, set_knobs
 from oracle.quant import per_token_dequant
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,7 @@ CASES = [
 @pytest.mark.parametrize("splits", [0, 3])
 @pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps,mma", CASES)
 def test_append_attention_steps(monkeypatch, name, dt, quant, d, Hq, Hkv, ps, mma, splits):
-    monkeypatch.setenv("PKV_ATTN_MMA", mma)
+    set_knobs(monkeypatch, PKV_ATTN_MMA=mma)
     w = synth.Workload(name="fa-" + name, seed=660 + d + Hq + ps, batch=4, layers=1, num_q_heads=Hq,
                        num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt, quant=quant, seq_len=None,
                        seq_len_range=(1, 300), outlier_channels=4 if quant != "none" else 0,

@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import synth
-from helpers import TOL, bits_to_torch, gather, load_workload, max_abs_err, oracle_dense, queries_dev
+from helpers import (TOL, bits_to_torch, gather, load_workload, max_abs_err, oracle_dense, queries_dev,
+                     set_knobs)
 
 pytestmark = pytest.mark.gpu
 
@@ -78,8 +79,7 @@ def test_alternating_batch_sizes_on_one_kernel():
 def test_ring_depth_and_blocks_per_sm(monkeypatch, stages, per_sm):
     # the stage count is rounded to a multiple of the consumer warps, so every
     # ring slot has a single reader; results must not depend on these knobs
-    monkeypatch.setenv("PKV_ATTN_STAGES", stages)
-    monkeypatch.setenv("PKV_ATTN_CTAS_PER_SM", per_sm)
+    set_knobs(monkeypatch, PKV_ATTN_STAGES=stages, PKV_ATTN_CTAS_PER_SM=per_sm)
     w = dataclasses.replace(synth.WORKLOADS["w2_llama7b_bf16"], batch=2, layers=1)
     ld = load_workload(w, lens=np.array([700, 333], dtype=np.int32))
     q, qf = queries_dev(w)
@@ -95,7 +95,7 @@ def test_ring_depth_and_blocks_per_sm(monkeypatch, stages, per_sm):
     (128, 32, 4, 16, "bf16"),
 ])
 def test_shapes_ragged_lengths(monkeypatch, d, Hq, Hkv, ps, dt, mma):
-    monkeypatch.setenv("PKV_ATTN_MMA", mma)
+    set_knobs(monkeypatch, PKV_ATTN_MMA=mma)
     w = synth.Workload(name="t", seed=77 + d + Hq + ps, batch=5, layers=1, num_q_heads=Hq,
                        num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt, quant="none",
                        seq_len=None, seq_len_range=(1, 300))
@@ -171,3 +171,57 @@ def test_host_side_errors():
         B.paged_decode_attention(desc, 1, 4, q.data_ptr(), B.F16, 0.125, ld.bt_dev.data_ptr(), 2,
                                  ld.lens_dev.data_ptr(), 0, 0, 0, q.data_ptr(), B.F32, 0, 0, 0, 0, 0)
     assert e.value.status == B.ERR_WORKSPACE
+
+
+def _dense_ref_all(ld, qf, k_last=None, v_last=None):
+    """Oracle outputs of every (sequence, query head), optionally with the last
+    token of each sequence replaced by (k_last[b], v_last[b]) [Hkv][d]."""
+    w = ld.w
+    res = {}
+    for b in range(w.batch):
+        k = ld.seqs[b].k
+        v = ld.seqs[b].v
+        if k_last is not None:
+            k = k.copy()
+            v = v.copy()
+            k[-1] = k_last[b]
+            v[-1] = v_last[b]
+        for h in range(w.num_q_heads):
+            g = h // w.group
+            res[(b, h)] = oracle.decode_attention_tokens(qf[b, h], k[:, g, :], v[:, g, :], w.sm_scale)
+    return res
+
+
+@pytest.mark.slow
+def test_dense_32k_bf16_all_outputs():
+    # The 32K dense bf16 workload (4 sequences x 32768 tokens, 32 = 32 heads,
+    # d = 128, page 16) in the launch configuration of the benchmark: automatic
+    # split count, early start after the previous call (fresh_rows = 0), and the
+    # one-call decode step that writes the token at position 32767 itself.
+    # Every one of the 128 outputs is compared with the oracle.
+    w = synth.WORKLOADS["dense_32k_bf16"]
+    ld = load_workload(w)
+    q, qf = queries_dev(w)
+    ref = _dense_ref_all(ld, qf)
+    for fresh in (-1, 0):
+        out = run_attention(ld, q, fresh_rows=fresh).cpu().numpy()
+        assert max_abs_err(out, ref) <= TOL["bf16"], fresh
+    assert int(ld.status.item()) == 0
+    # decode step: the token at position L - 1 is overwritten by the new one
+    toks = [synth.append_tokens(w, b, 0) for b in range(w.batch)]
+    kb = np.stack([t.k_bits[0] for t in toks])
+    vb = np.stack([t.v_bits[0] for t in toks])
+    q2, qf2 = queries_dev(w, step=1)
+    out = ld.cache.append_attention(bits_to_torch(kb, "bf16").cuda(), bits_to_torch(vb, "bf16").cuda(), q2,
+                                    ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, dev_status=ld.status,
+                                    fresh_rows=0)
+    torch.cuda.synchronize()
+    ref2 = _dense_ref_all(ld, qf2, [t.k[0] for t in toks], [t.v[0] for t in toks])
+    assert max_abs_err(out.cpu().numpy(), ref2) <= TOL["bf16"]
+    # the stored row is the new token's bits
+    kp = ld.cache.k_pages.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(w.batch):
+        L = int(ld.lens[b])
+        t = L - 1
+        assert np.array_equal(kp[ld.bt[b][t // w.page_size], :, t % w.page_size], kb[b])
+    assert int(ld.status.item()) == 0

@@ -106,8 +106,7 @@ def test_w5_full_size_30pct_and_all_pages():
     assert K == 308
     sel, cnt, scores, out = run_sparse(ld, q, K)
     chosen = check_selection(ld, qf, K, sel, cnt, scores)
-    rng = np.random.default_rng(5)
-    units = sorted({(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, 24), rng.integers(0, 16, 24))})
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]   # every output
     assert max_abs_err(out, oracle_sparse(ld, qf, chosen, units)) <= TOL["f16"]
     # top-K = all pages reproduces dense attention
     sel2, cnt2, scores2, out_all = run_sparse(ld, q, P)
@@ -153,29 +152,15 @@ def test_bad_selected_page_is_reported():
         assert np.abs(out[0, h] - o).max() <= TOL["f16"]
 
 
-@pytest.mark.parametrize("mode", ["sum", "max"])
-@pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("none", 64, 8, 2, 16, 4), ("per_token", 128, 16, 4, 16, 5),
-                                                     ("none", 128, 8, 1, 32, 3), ("none", 64, 16, 2, 64, 2)])
-def test_group_shared_selection(mode, quant, d, Hq, Hkv, ps, top_k):
-    # one page list per kv head, from the sum or max of its group's scores;
-    # each query head of the group attends over that list
+def check_group_selection(ld, qf, top_k, mode, sel, cnt, scores, out):
+    """One page list per kv head from the sum or max of its group's scores: scores
+    within fp32 slack, kept pages bit-exact (ties within 1e-4 relative excepted), and
+    every query head's output over its group's list against the oracle."""
     from helpers import oracle_kv
-    from paged_kv_cache_243_gb300 import binding as B
-    G = Hq // Hkv
-    w = synth.Workload(name="spg", seed=970 + d + Hq + ps, batch=4, layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
-                       head_dim=d, page_size=ps, dtype="f16", quant=quant, seq_len=None,
-                       seq_len_range=(1, 400), outlier_channels=4 if quant != "none" else 0,
-                       outlier_scale=15.0, page_offset_std=0.5)
-    ld = load_workload(w, lens=np.array([400, 1, 37, 200], dtype=np.int32), with_meta=True)
-    q, qf = queries_dev(w)
-    gm = B.SELECT_GROUP_SUM if mode == "sum" else B.SELECT_GROUP_MAX
-    sel, cnt, scores = ld.cache.score_topk(q, ld.bt_dev, ld.lens_dev, top_k, want_scores=True,
-                                           dev_status=ld.status, group_mode=gm)
-    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, sel=sel, sel_count=cnt,
-                             sel_shared=True, dev_status=ld.status)
-    torch.cuda.synchronize()
-    sel, cnt, scores, out = sel.cpu().numpy(), cnt.cpu().numpy(), scores.cpu().numpy(), out.cpu().numpy()
+    w = ld.w
+    G, Hkv, ps = w.group, w.num_kv_heads, w.page_size
     assert sel.shape == (w.batch, Hkv, top_k)
+    tol = TOL["int8"] if w.quant != "none" else TOL[w.dtype]
     for b in range(w.batch):
         L = int(ld.lens[b])
         P = -(-L // ps)
@@ -202,8 +187,104 @@ def test_group_shared_selection(mode, quant, d, Hq, Hkv, ps, top_k):
             for h in range(g * G, (g + 1) * G):
                 o = oracle.sparse_decode_attention(qf[b, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], w.sm_scale,
                                                    [got], ps)[0]
-                tol = TOL["int8"] if quant != "none" else TOL["f16"]
                 assert np.abs(out[b, h] - o).max() <= tol, (b, h)
+
+
+def run_group_sparse(ld, q, top_k, mode):
+    from paged_kv_cache_243_gb300 import binding as B
+    gm = B.SELECT_GROUP_SUM if mode == "sum" else B.SELECT_GROUP_MAX
+    sel, cnt, scores = ld.cache.score_topk(q, ld.bt_dev, ld.lens_dev, top_k, want_scores=True,
+                                           dev_status=ld.status, group_mode=gm)
+    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=ld.w.sm_scale, sel=sel, sel_count=cnt,
+                             sel_shared=True, dev_status=ld.status)
+    torch.cuda.synchronize()
+    return sel.cpu().numpy(), cnt.cpu().numpy(), scores.cpu().numpy(), out.cpu().numpy()
+
+
+@pytest.mark.parametrize("mode", ["sum", "max"])
+@pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("none", 64, 8, 2, 16, 4), ("per_token", 128, 16, 4, 16, 5),
+                                                     ("none", 128, 8, 1, 32, 3), ("none", 64, 16, 2, 64, 2)])
+def test_group_shared_selection(mode, quant, d, Hq, Hkv, ps, top_k):
+    # one page list per kv head, from the sum or max of its group's scores;
+    # each query head of the group attends over that list
+    w = synth.Workload(name="spg", seed=970 + d + Hq + ps, batch=4, layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_dim=d, page_size=ps, dtype="f16", quant=quant, seq_len=None,
+                       seq_len_range=(1, 400), outlier_channels=4 if quant != "none" else 0,
+                       outlier_scale=15.0, page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([400, 1, 37, 200], dtype=np.int32), with_meta=True)
+    q, qf = queries_dev(w)
+    sel, cnt, scores, out = run_group_sparse(ld, q, top_k, mode)
+    check_group_selection(ld, qf, top_k, mode, sel, cnt, scores, out)
+    assert int(ld.status.item()) == 0
+
+
+@pytest.mark.slow
+def test_w6_full_size_group_sum():
+    # GQA 32/8 per-token INT8 with page boxes, B = 8, L = 16384, page 16: one
+    # list of 308 pages (30 %) per kv head from the group's summed scores;
+    # boxes bit-exact, scores, selections and every output against the oracle
+    w = synth.WORKLOADS["w6_gqa_sparse_int8"]
+    ld = load_workload(w, with_meta=True)
+    check_meta(ld)
+    q, qf = queries_dev(w)
+    P = w.seq_len // w.page_size
+    K = oracle.top_k_count(w.top_k_ratio, P)
+    sel, cnt, scores, out = run_group_sparse(ld, q, K, "sum")
+    check_group_selection(ld, qf, K, "sum", sel, cnt, scores, out)
+    assert int(ld.status.item()) == 0
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,ps", [(128, 16, 4, 128), (64, 8, 2, 64), (128, 32, 8, 256)])
+def test_per_group_int8_boxes_and_sparse(d, Hq, Hkv, ps):
+    # Per-64-token-group INT8 with page boxes. Every append re-quantises the
+    # open group, which changes the restored values of its earlier tokens, so
+    # the box of the page holding it must be rebuilt: after chunked prefill and
+    # after each of several single-token appends that close a group and open
+    # the next, the boxes must equal the oracle's over the restored keys, bit
+    # for bit. Then page scoring and sparse attention (lists per query head,
+    # and per kv head from group sums and maxima) run over that cache.
+    w = synth.Workload(name="spg8", seed=990 + d + Hq + ps, batch=4, layers=1, num_q_heads=Hq,
+                       num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype="f16", quant="per_group64",
+                       seq_len=None, seq_len_range=(1, 400), outlier_channels=4, outlier_scale=15.0,
+                       page_offset_std=0.5)
+    lens = np.array([190, 62, 127, 1], dtype=np.int32)
+    ld = load_workload(w, lens=lens, with_meta=True, extra_pages=1, chunks=[100, 27, 1, 1, 36, 100])
+    check_meta(ld)
+    from helpers import bits_to_torch
+    from helpers import check_per_group_codes
+    K = [s.k for s in ld.seqs]
+    V = [s.v for s in ld.seqs]
+    cur = lens.copy()
+    for step in range(4):       # 190 -> 194 closes group 2; 62 -> 66 closes group 0; 127 -> 131
+        toks = [synth.append_tokens(w, b, step) for b in range(w.batch)]
+        kb = np.stack([t.k_bits for t in toks])
+        vb = np.stack([t.v_bits for t in toks])
+        ld.cache.append(bits_to_torch(kb, "f16").cuda(), bits_to_torch(vb, "f16").cuda(), ld.bt_dev,
+                        torch.from_numpy(cur.copy()).cuda(), dev_status=ld.status)
+        torch.cuda.synchronize()
+        cur = cur + 1
+        for b in range(w.batch):
+            K[b] = np.concatenate([K[b], toks[b].k])
+            V[b] = np.concatenate([V[b], toks[b].v])
+            ld.seqs[b] = synth.SeqData(None, None, K[b], V[b])
+        ld.lens = cur.copy()
+        check_meta(ld)
+    check_per_group_codes(ld)
+    ld.lens_dev = torch.from_numpy(cur.copy()).cuda()
+    q, qf = queries_dev(w)
+    top_k = 2
+    sel, cnt, scores, out = run_sparse(ld, q, top_k)
+    chosen = check_selection(ld, qf, top_k, sel, cnt, scores)
+    from helpers import oracle_kv
+    for (b, h), pages in chosen.items():
+        k, v = oracle_kv(ld, b)
+        g = h // w.group
+        o = oracle.sparse_decode_attention(qf[b, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], w.sm_scale,
+                                           [pages], ps)[0]
+        assert np.abs(out[b, h] - o).max() <= TOL["int8"], (b, h)
+    for mode in ("sum", "max"):
+        sel, cnt, scores, out = run_group_sparse(ld, q, top_k, mode)
+        check_group_selection(ld, qf, top_k, mode, sel, cnt, scores, out)
     assert int(ld.status.item()) == 0
 
 
