@@ -323,9 +323,9 @@ class Replica:
         if attention:
             # early start: after this step's append, the kernel before the
             # attention writes only the new token's rows (fresh_rows = 1); after
-            # another layer's attention it writes nothing the call reads (0).
-            # Scoring writes the page lists, so sparse calls wait (-1).
-            fresh = -1 if (sparse or not EARLY_START) else (1 if append else 0)
+            # another layer's attention it writes nothing the call reads (0);
+            # after the page scoring it writes only the page lists (0).
+            fresh = -1 if not EARLY_START else (1 if (append and not sparse) else 0)
             c.attention(self.qs[i], self.bts[i], self.len_list[s], sm_scale=self.w.sm_scale,
                         sel=self.sel[i] if sparse else None, sel_count=self.cnt[i] if sparse else None,
                         sel_shared=sparse and self.group_mode != 0,
@@ -537,115 +537,168 @@ def sweep(peak: float) -> Dict:
 
 
 # -------------------------------------------------------------- CPU baseline
+# The oracle (fp64 NumPy, test infrastructure) timed on the host cores, per
+# workload, on bounded samples. A unit is one (layer, sequence, query head):
+# the oracle restores that query head's K/V from the stored form (INT8 codes,
+# scales and zero-points precomputed with the oracle's quantiser, as the cache
+# holds them), and runs its attention; for the sparse workload it also scores
+# the pages from their boxes (precomputed, as the cache keeps them), selects
+# the top-K and attends over them. Only that arithmetic is timed; seeded input
+# generation and the stored-form preparation are not.
+CPU_BASELINE_WORKLOADS = ("w1_tiny_f16", "w2_llama7b_bf16", "w3_gqa_int8_token",
+                          "w4_long_int8_group", "w5_sparse_f16", "dense_32k_bf16")
 _SEQ_CACHE: Dict = {}
 
 
-def _oracle_units(args):
-    """Oracle attention of (layer, sequence, query head) units in this worker.
+def _stored_kv(name: str, layer: int, b: int, g: int):
+    """(what the oracle restores from, K/V of kv head g of sequence b) kept per
+    worker for the sequences it samples."""
+    import oracle
+    key = (name, layer, b, g)
+    if key in _SEQ_CACHE:
+        return _SEQ_CACHE[key]
+    if len(_SEQ_CACHE) > 8:
+        _SEQ_CACHE.clear()
+    w = synth.WORKLOADS[name]
+    L = int(synth.seq_lens(w)[b])
+    sd = synth.seq_tokens(w, b, layer, L)
+    k, v = sd.k[:, g:g + 1].copy(), sd.v[:, g:g + 1].copy()
+    del sd
+    if w.quant == "per_token":
+        stored = (oracle.quantize_per_token(k), oracle.quantize_per_token(v))
+    elif w.quant == "per_group64":
+        stored = (oracle.quantize_per_group(k), oracle.quantize_per_group(v))
+    else:
+        stored = (k, v)
+    meta = oracle.page_bounding_boxes(k, w.page_size) if w.top_k_ratio else None
+    _SEQ_CACHE[key] = (stored, meta, synth.queries(w, layer)[1])
+    return _SEQ_CACHE[key]
 
-    Returns (seconds spent in the oracle's arithmetic, KV bytes those units read).
-    The seeded input generation is not timed and is cached per (layer, sequence).
-    """
+
+def _oracle_units(args):
+    """Oracle arithmetic of the given (layer, sequence, query head) units in this
+    worker; returns (seconds of oracle arithmetic, units)."""
     name, units = args
     import oracle
     from oracle.quant import per_group_dequant, per_token_dequant
     w = synth.WORKLOADS[name]
-    lens = synth.seq_lens(w)
-    t_total, byts = 0.0, 0
+    t_total = 0.0
     for layer, b, h in units:
-        key = (name, layer, b)
-        if key not in _SEQ_CACHE:
-            if len(_SEQ_CACHE) > 4:
-                _SEQ_CACHE.clear()
-            _SEQ_CACHE[key] = (synth.seq_tokens(w, b, layer, int(lens[b])), synth.queries(w, layer)[1])
-        sd, qf = _SEQ_CACHE[key]
         g = h // w.group
+        stored, meta, qf = _stored_kv(name, layer, b, g)
         t0 = time.perf_counter()
-        if w.quant == "none":
-            k, v = sd.k[:, g].astype(np.float64), sd.v[:, g].astype(np.float64)
-        elif w.quant == "per_token":
-            kc, ks, kz = oracle.quantize_per_token(sd.k[:, g:g + 1])
-            vc, vs, vz = oracle.quantize_per_token(sd.v[:, g:g + 1])
-            k = per_token_dequant(kc, ks, kz)[:, 0]
-            v = per_token_dequant(vc, vs, vz)[:, 0]
+        if w.quant == "per_token":
+            k = per_token_dequant(*stored[0])[:, 0]
+            v = per_token_dequant(*stored[1])[:, 0]
+        elif w.quant == "per_group64":
+            k = per_group_dequant(*stored[0])[:, 0]
+            v = per_group_dequant(*stored[1])[:, 0]
         else:
-            kc, ks, kz = oracle.quantize_per_group(sd.k[:, g:g + 1])
-            vc, vs, vz = oracle.quantize_per_group(sd.v[:, g:g + 1])
-            k = per_group_dequant(kc, ks, kz)[:, 0]
-            v = per_group_dequant(vc, vs, vz)[:, 0]
-        oracle.decode_attention_tokens(qf[b, h], k, v, w.sm_scale)
+            k, v = stored[0][:, 0], stored[1][:, 0]
+        if meta is None:
+            oracle.decode_attention_tokens(qf[b, h], k, v, w.sm_scale)
+        else:
+            mn, mx = meta
+            r = oracle.page_scores(qf[b, h:h + 1], mn, mx, 1)[0]
+            K = oracle.top_k_count(w.top_k_ratio, r.shape[0])
+            pages = oracle.select_top_k(r, K)
+            oracle.sparse_decode_attention(qf[b, h:h + 1], k[:, None], v[:, None], w.sm_scale, [pages],
+                                           w.page_size)
         t_total += time.perf_counter() - t0
-        byts += int(lens[b]) * w.head_dim * 2 * (1 if w.quant != "none" else 2)
-    return t_total, byts
+    return t_total, len(units)
 
 
-class OracleRunner:
-    """The oracle, as it stands, on all host cores: one single-threaded spawn
-    worker per core, each timing its own units."""
+def _oracle_pool(workers: int):
+    """Spawned single-threaded workers (BLAS threads pinned to one)."""
+    import multiprocessing as mp
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    old = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"
+    try:
+        return mp.get_context("spawn").Pool(workers)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
-    def __init__(self, name: str):
-        import multiprocessing as mp
-        self.name = name
-        self.cores = os.cpu_count() or 1
-        keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
-        old = {k: os.environ.get(k) for k in keys}
-        for k in keys:
-            os.environ[k] = "1"
-        try:
-            self.pool = mp.get_context("spawn").Pool(self.cores)
-        finally:
-            for k, v in old.items():
-                if v is None:
-                    os.environ.pop(k, None)
-                else:
-                    os.environ[k] = v
+
+def step_bytes_of(w: synth.Workload) -> int:
+    """Algorithmic bytes of one step of the workload (as the GPU arm counts them)."""
+    lens = synth.seq_lens(w)
+    if w.top_k_ratio:
+        K = int(math.ceil(w.top_k_ratio * -(-int(lens.max()) // w.page_size)))
+        return algorithmic_bytes(w, lens, append_tokens=0, sparse_pages=K)["total"] * w.layers
+    return algorithmic_bytes(w, lens, append_tokens=1 if w.append_steps else 0)["total"] * w.layers
+
+
+class OracleSampler:
+    """Times oracle units of one workload on a pool of spawned single-threaded
+    workers. Worker c takes units of one sequence (the first or the last of the
+    batch, alternating) and of one kv head's query heads, so it restores one
+    kv head's K/V (generated once per worker)."""
+
+    def __init__(self, name: str, pool, workers: int):
+        self.name, self.pool, self.workers = name, pool, workers
         w = synth.WORKLOADS[name]
-        self.units = [(l, b, h) for l in range(w.layers) for b in range(w.batch) for h in range(w.num_q_heads)]
+        self.units_per_step = w.layers * w.batch * w.num_q_heads
+        self.step_bytes = step_bytes_of(w)
 
-    def run(self, units_per_core: int, seed: int):
-        """One sample: units_per_core units per core from a few sequences; returns
-        (bytes, seconds) with seconds = the slowest worker's arithmetic time."""
-        rng = np.random.default_rng(seed)
+    def run(self, units_per_worker: int, seed: int):
+        """One sample; returns (units, seconds) where seconds is the slowest
+        worker's oracle time (the workers run at once)."""
         w = synth.WORKLOADS[self.name]
-        # two fixed sequences (generated once per worker), random query heads
+        rng = np.random.default_rng(seed)
         seqs = [(0, 0), (w.layers - 1, w.batch - 1)]
         jobs = []
-        for c in range(self.cores):
+        for c in range(self.workers):
             layer, b = seqs[c % 2]
-            hs = rng.integers(0, w.num_q_heads, size=units_per_core)
+            g = (c // 2) % w.num_kv_heads
+            hs = g * w.group + rng.integers(0, w.group, size=units_per_worker)
             jobs.append((self.name, [(layer, b, int(h)) for h in hs]))
         res = self.pool.map(_oracle_units, jobs, chunksize=1)
-        self.cpu_seconds = sum(r[0] for r in res)
         return sum(r[1] for r in res), max(r[0] for r in res)
 
-    def close(self):
-        self.pool.close()
-        self.pool.join()
+    def measure(self, budget_s: float) -> Dict:
+        """About budget_s of oracle time per worker; GB/s of the workload's
+        algorithmic bytes at the sampled rate of units."""
+        self.run(1, 0)                                   # warm: imports, inputs
+        n, t = self.run(1, 0)
+        per_unit = max(t, 1e-6)
+        upw = int(max(1, min(4000, budget_s / per_unit)))
+        units, secs = self.run(upw, 2)
+        rate = units / secs                               # units per second
+        ms_step = self.units_per_step / rate * 1e3
+        return {"gb_s": round(self.step_bytes / (ms_step * 1e-3) / 1e9, 4), "cores": self.workers,
+                "est_ms_per_step": round(ms_step, 3), "units_timed": units, "seconds": round(secs, 3)}
 
 
-def cpu_baseline(name: str, budget_s: float = 15.0) -> Dict:
-    """Oracle throughput on the host cores over a bounded sample of the workload."""
-    runner = OracleRunner(name)
+def cpu_baseline(name: str, budget_s: float = 1.5) -> Dict:
+    """The oracle on the host cores, single core and all cores, for the headline
+    workload (top-level keys) and for every workload of the pages (per_config)."""
+    cores = os.cpu_count() or 1
+    single, multi = _oracle_pool(1), _oracle_pool(cores)
+    per = {}
     try:
-        for _ in range(2):
-            runner.run(2, 0)                           # warm: imports + generation
-        t0 = time.perf_counter()
-        byts, secs, cpu, n = 0, 0.0, 0.0, 0
-        upc = 4
-        # about budget_s of CPU work in total (all cores), bounded in wall time
-        while cpu < budget_s and time.perf_counter() - t0 < 3 * budget_s and n < 10000:
-            bb, ss = runner.run(upc, 1 + n)
-            byts += bb
-            secs += ss
-            cpu += runner.cpu_seconds
-            n += 1
+        for wname in CPU_BASELINE_WORKLOADS:
+            per[wname] = {"single_core": OracleSampler(wname, single, 1).measure(budget_s),
+                          "all_cores": OracleSampler(wname, multi, cores).measure(budget_s)}
     finally:
-        runner.close()
-    return {"value": round(byts / secs / 1e9, 4), "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
-            "sample": f"{n} rounds x {upc} (layer, sequence, query head) units per core of {name} "
-                      f"({n * upc * runner.cores} units); fp64 numpy oracle, one single-threaded "
-                      f"spawn worker per core; oracle arithmetic timed, seeded input generation not",
-            "seconds": round(secs, 3), "cpu_seconds": round(cpu, 2)}
+        for pool in (single, multi):
+            pool.close()
+            pool.join()
+    head = per.get(name) or per["w2_llama7b_bf16"]
+    return {"value": head["all_cores"]["gb_s"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_core": {"value": head["single_core"]["gb_s"], "cores": 1},
+            "sample": f"per workload, about {budget_s} s of oracle arithmetic per worker on one "
+                      f"single-threaded spawned worker (single_core) and on {cores} (all_cores); a unit "
+                      f"is one (layer, sequence, query head): restore its K/V from the stored form and "
+                      f"attend (sparse: score the page boxes, select the top-K, attend); GB/s = the "
+                      f"workload's algorithmic bytes per step / (units per step / units per second); "
+                      f"seeded input generation and the stored-form preparation are not timed",
+            "per_config": per}
 
 
 # ------------------------------------------------------------------- arms
@@ -785,35 +838,44 @@ def run_ours(args) -> None:
 
 def run_reference(args) -> None:
     """The oracle as the reference arm: each step is a bounded sample of the
-    workload (one unit per host core), sized so the whole run takes minutes."""
+    workload (a few (layer, sequence, query head) units per host core), sized so
+    the whole run takes minutes; ms_per_step is the measured time of one such
+    sample step, and the value is the GB/s of the workload's algorithmic bytes
+    at the sampled rate of units."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
-    lens = synth.seq_lens(w)
-    step_bytes = algorithmic_bytes(w, lens)["total"] * w.layers
-    runner = OracleRunner(args.workload)
+    cores = os.cpu_count() or 1
+    pool = _oracle_pool(cores)
+    smp = OracleSampler(args.workload, pool, cores)
     try:
-        for _ in range(2):
-            runner.run(1, 0)
-        byts, secs = 0, 0.0
+        smp.run(1, 0)
+        upw = 8
+        units, secs = 0, 0.0
         for i in range(args.warmup + args.steps):
-            bb, ss = runner.run(1, 1 + i)
+            n, t = smp.run(upw, 1 + i)
             if i >= args.warmup:
-                byts += bb
-                secs += ss
+                units += n
+                secs += t
     finally:
-        runner.close()
-    value = byts / secs / 1e9 if secs > 0 else 0.0
-    ms = step_bytes / (value * 1e9) * 1e3 if value > 0 else None
-    cb = {"value": round(value, 4), "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
-          "sample": f"per step one (layer, sequence, query head) unit per core ({runner.cores} units) "
-                    f"of {args.workload}; fp64 numpy oracle; {args.steps} timed steps"}
+        pool.close()
+        pool.join()
+    rate = units / secs if secs > 0 else 0.0
+    value = smp.step_bytes * rate / smp.units_per_step / 1e9 if rate > 0 else 0.0
+    ms_sample = secs / max(1, args.steps) * 1e3
+    cb = {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+          "sample": f"per step {upw} (layer, sequence, query head) units on each of {cores} single-threaded "
+                    f"spawned workers ({upw * cores} units) of {args.workload}; fp64 numpy oracle; "
+                    f"{args.steps} timed steps"}
     line = {"impl": "reference", "metric": "paged decode-attention KV GB/s", "value": round(value, 4),
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded numpy generators)",
-            "config": {"workload": w.name, "description": w.description},
+            "ms_per_step": round(ms_sample, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy generators)",
+            "config": {"workload": w.name, "description": w.description,
+                       "step": f"a sample of {upw * cores} units of the workload (its "
+                               f"{smp.units_per_step} units take {smp.units_per_step / max(rate, 1e-9) * 1e3:.1f} ms "
+                               f"at the sampled rate)"},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -224,9 +224,15 @@ size_t pkv_attention_workspace_bytes(const pkv_cache* cache, int32_t batch, int3
  *                 fresh_rows tokens of each sequence writes, i.e. positions
  *                 >= seq_lens[b] - fresh_rows (per-group INT8: from the
  *                 start of the 64-token group holding that position, which
- *                 the append re-quantises). Typical use: the call right after
- *                 this step's pkv_kv_append (fresh_rows = its t_new), or
- *                 right after another attention call (fresh_rows = 0). The
+ *                 the append re-quantises), and, in sparse mode, the page
+ *                 lists sel_pages / sel_count. Typical use: the call right
+ *                 after this step's pkv_kv_append (fresh_rows = its t_new),
+ *                 right after another attention call (fresh_rows = 0), or a
+ *                 sparse call right after the pkv_page_score_topk that wrote
+ *                 its lists (fresh_rows = 0). A sparse call that starts early
+ *                 plans its work from the lengths alone (every row of
+ *                 sequence b is given min(sel_stride, pages of b) pages) and
+ *                 reads at most that many entries of a list. The
  *                 call then reads q, the tables, the lengths and all older
  *                 rows at once, and waits for that kernel before copying a
  *                 chunk with fresh rows and before its first write to out or

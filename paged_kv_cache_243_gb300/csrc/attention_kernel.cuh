@@ -57,6 +57,7 @@ constexpr int kMiscInts = 32;
 constexpr int kQStageBytes = 2048;   // shared-memory copy of q for a block's first units (small: it must
                                      // not cost a resident block per SM)
 constexpr int kMiscAbort = 24;   // misc slot: some consumer warp timed out
+constexpr int kSkipSelected = -2;   // producer: a chunk past its unit's page list
 
 struct AttnParams {
   // K and V pools as 2-D tensors [num_pages * Hkv * page_size rows][128 bytes]
@@ -501,6 +502,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
     int n;
     if (!sparse) {
       n = (L + kChunk - 1) / kChunk;
+    } else if (early) {
+      // the page lists may still be being written: every unit of sequence b
+      // gets min(list stride, pages of b) pages' chunks, a bound on any
+      // valid list (distinct pages of the sequence); entries past the
+      // unit's count are skipped once the lists are read
+      const int P = (L + ps - 1) / ps;
+      n = min(p.sel_stride, P) * (ps / kChunk);
     } else {
       int cnt = p.sel_count[b * p.units_per_b + hu];
       cnt = cnt < 0 ? 0 : (cnt > p.sel_stride ? p.sel_stride : cnt);
@@ -584,7 +592,12 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         const int lp = (r.k * kChunk) / ps;
         if (r.k * kChunk < lens[b]) r.phys = p.block_table[(size_t)b * p.max_pages + lp];
       } else {
-        r.sp = p.sel_pages[(size_t)(b * p.units_per_b + hu) * p.sel_stride + r.k / cpp];
+        const size_t row = (size_t)b * p.units_per_b + hu;
+        if (early && r.k / cpp >= min(max(p.sel_count[row], 0), p.sel_stride)) {
+          r.sp = kSkipSelected;   // past the unit's list: no page, no error
+          return;
+        }
+        r.sp = p.sel_pages[row * p.sel_stride + r.k / cpp];
       }
     };
     auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
@@ -598,6 +611,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         t0 = r.k * kChunk;
         g = hu;
       } else {
+        if (r.sp == kSkipSelected) return;
         g = p.unit_is_q ? hu / p.group : hu;
         if (r.sp < 0 || (long long)r.sp * ps >= L) {
           flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
@@ -641,6 +655,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       pdl_launch_dependents();
       waited = true;
     };
+    // early sparse calls: the page lists are the preceding kernel's output
+    if (sparse && !waited) wait_prior();
     Raw cur;
     fetch(lo + lane, cur);
     for (int base = lo; base < hi && !abort; base += 32) {
@@ -1411,18 +1427,25 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
   const int o = blockIdx.y * OB + (tid - grp * OB);   // output of the unit
   const bool active = o < GE * D;
   const bool sparse = p.sel_pages != nullptr;
+  // the unit chunk ranges follow from the lengths alone in dense calls and in
+  // early-start sparse calls (whose units of sequence b all get min(list
+  // stride, pages of b) pages' chunks); other sparse calls read the prefix
+  // the attention kernel's block 0 wrote
+  const bool from_lens = !sparse || p.fresh_rows >= 0;
   const int b = u / p.units_per_b, hu = u - b * p.units_per_b;
   long long W = 0, s0 = 0, s1 = 0;
-  if (!sparse) {
-    // chunks of each kv head of sequence b' = ceil(clamped length / 16), as in
-    // the attention kernel: W = units_per_b * sum_b' n_b', and unit u starts
-    // after all units of sequences b' < b and hu units of sequence b
+  if (from_lens) {
+    // chunks of each unit of sequence b' (n_b', as in the attention kernel):
+    // W = units_per_b * sum_b' n_b', and unit u starts after all units of
+    // sequences b' < b and hu units of sequence b
     const int cap = p.max_pages * p.page_size;
     long long tot = 0, before = 0, nb = 0;
     for (int bb = tid; bb < p.batch; bb += kCombineThreads) {
       int L = p.seq_lens[bb];
       L = L < 0 ? 0 : (L > cap ? cap : L);
-      const long long n = (L + kChunk - 1) / kChunk;
+      const long long n = !sparse ? (L + kChunk - 1) / kChunk
+                                  : (long long)min(p.sel_stride, (L + p.page_size - 1) / p.page_size) *
+                                        (p.page_size / kChunk);
       tot += n;
       if (bb < b) before += n;
       if (bb == b) nb = n;
@@ -1462,14 +1485,14 @@ __global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const 
     R4 = nb1 + (cta_lo(c_last + 1, W, N) <= s1 ? 1 : kConsumerWarps);
   };
   int c_first = 0, nb1 = 0, R4 = 0;
-  if (!sparse && s0 != s1) cover(c_first, nb1, R4);
+  if (from_lens && s0 != s1) cover(c_first, nb1, R4);
   // The next kernel may launch now, before this grid's wait: its own wait
   // covers this grid, which completes only after the attention grid it
   // merges. (Triggering at the very start measured slower: W2 25.4 against
   // 22.9 us per call in a 32-call chain.)
   pdl_launch_dependents();
   pdl_wait();
-  if (sparse) {
+  if (!from_lens) {
     W = __ldcg(p.ws_prefix + p.num_units);
     s0 = __ldcg(p.ws_prefix + u);
     s1 = __ldcg(p.ws_prefix + u + 1);

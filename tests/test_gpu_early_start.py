@@ -152,3 +152,77 @@ def test_fused_steps_enqueued_back_to_back(name, dt, quant, d, Hq, Hkv, ps, laye
                                                        w.sm_scale)
                     tol = TOL["int8"] if quant != "none" else TOL[dt]
                     assert np.abs(got[h] - o).max() <= tol, (l, s, b, h)
+
+
+@pytest.mark.parametrize("group_mode", [0, 1])
+@pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("none", 64, 8, 8, 16, 7), ("per_token", 128, 16, 4, 16, 5),
+                                                     ("none", 128, 8, 2, 32, 3)])
+def test_sparse_attention_overlapping_the_scoring(group_mode, quant, d, Hq, Hkv, ps, top_k):
+    # sparse attention right after the page scoring that writes its lists,
+    # started early (fresh_rows = 0): it plans from the lengths and reads the
+    # lists only after waiting; results equal the call that waits up front
+    import oracle as O
+    from helpers import TOL as T, oracle_kv
+    w = synth.Workload(name="early-sp", seed=680 + d + Hq + ps + group_mode, batch=4, layers=1,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype="f16", quant=quant,
+                       seq_len=None, seq_len_range=(1, 500), outlier_channels=4 if quant != "none" else 0,
+                       outlier_scale=15.0, page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([500, 1, 70, 33], dtype=np.int32), with_meta=True)
+    q, qf = queries_dev(w)
+    shared = group_mode != 0
+    outs = []
+    for fresh in (0, -1):
+        sel, cnt, _ = ld.cache.score_topk(q, ld.bt_dev, ld.lens_dev, top_k, dev_status=ld.status,
+                                          group_mode=group_mode)
+        out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, sel=sel, sel_count=cnt,
+                                 sel_shared=shared, dev_status=ld.status, fresh_rows=fresh)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    assert np.abs(outs[0] - outs[1]).max() <= 1e-6
+    tol = T["int8"] if quant != "none" else T["f16"]
+    for b in range(w.batch):
+        k, v = oracle_kv(ld, b)
+        for h in range(Hq):
+            g = h // w.group
+            r = g if shared else h
+            pages = sel[b, r, :cnt[b, r]]
+            o = O.sparse_decode_attention(qf[b, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], w.sm_scale, [pages], ps)[0]
+            assert np.abs(outs[0][b, h] - o).max() <= tol, (b, h)
+    assert int(ld.status.item()) == 0
+
+
+def test_early_sparse_lists_shorter_than_their_stride():
+    # caller-made lists: counts below min(stride, pages), entries past a count
+    # hold garbage that must not be read; a zero count gives zeros
+    import oracle as O
+    from helpers import TOL as T
+    w = synth.Workload(name="early-sp2", seed=701, batch=3, layers=1, num_q_heads=4, num_kv_heads=4,
+                       head_dim=64, page_size=16, dtype="f16", quant="none", seq_len=None,
+                       seq_len_range=(1, 300))
+    ld = load_workload(w, lens=np.array([300, 100, 40], dtype=np.int32))
+    q, qf = queries_dev(w)
+    stride = 6
+    rng = np.random.default_rng(9)
+    sel = np.full((w.batch, w.num_q_heads, stride), 99999, dtype=np.int32)   # garbage past the counts
+    cnt = np.zeros((w.batch, w.num_q_heads), dtype=np.int32)
+    for b in range(w.batch):
+        P = -(-int(ld.lens[b]) // 16)
+        for h in range(w.num_q_heads):
+            n = int(rng.integers(0, min(stride, P) + 1)) if (b, h) != (0, 0) else 0
+            sel[b, h, :n] = np.sort(rng.choice(P, n, replace=False))
+            cnt[b, h] = n
+    sel_d, cnt_d = torch.from_numpy(sel).cuda(), torch.from_numpy(cnt).cuda()
+    ld.status.zero_()
+    out = ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, sel=sel_d, sel_count=cnt_d,
+                             dev_status=ld.status, fresh_rows=0)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy()
+    assert int(ld.status.item()) == 0
+    assert (out[0, 0] == 0).all()
+    for b in range(w.batch):
+        sd = ld.seqs[b]
+        for h in range(w.num_q_heads):
+            o = O.sparse_decode_attention(qf[b, h:h + 1], sd.k[:, h:h + 1], sd.v[:, h:h + 1], w.sm_scale,
+                                          [sel[b, h, :cnt[b, h]]], 16)[0]
+            assert np.abs(out[b, h] - o).max() <= T["f16"], (b, h)
