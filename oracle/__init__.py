@@ -30,4 +30,8 @@ from .attention import (  # noqa: F401
 from .sparse import (  # noqa: F401
     page_bounding_boxes, page_scores, group_page_scores, select_top_k, top_k_count,
 )
+from .quant4 import (  # noqa: F401
+    quantize_block_u4, quantize_rows_u4, quantize_per_token_u4, pack_u4, unpack_u4, dequantize_u4,
+    per_token_u4_dequant, per_token_u4_bbox_values,
+)
 from .sizes import kv_cache_bytes, blocks_needed  # noqa: F401
