@@ -98,7 +98,6 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
     group_shared: one page list per kv head, read once for its query-head group.
     """
     H, d, Hq = w.num_kv_heads, w.head_dim, w.num_q_heads
-    esz = 1 if w.quant != "none" else 2
     ps = w.page_size
     if sparse_pages is None:
         toks = lens.astype(np.int64)
@@ -107,9 +106,12 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
         # each query head reads its own selected pages (or each group its list)
         toks = np.minimum(lens.astype(np.int64), sparse_pages * ps)
         units = H if group_shared else Hq
-    per_tok = 2 * d * esz
-    if w.quant == "per_token":
-        per_tok += 16
+    if w.quant == "none":
+        per_tok = 2 * d * 2
+    elif w.quant == "per_token_u4":
+        per_tok = 2 * (d // 2) + 16           # two 4-bit codes per byte, K and V, + scales
+    else:
+        per_tok = 2 * d + (16 if w.quant == "per_token" else 0)
     attn = int((toks * units).sum()) * per_tok
     if w.quant == "per_group64":
         attn += int(((toks + 63) // 64 * units).sum()) * 16
@@ -123,6 +125,8 @@ def algorithmic_bytes(w: synth.Workload, lens: np.ndarray, append_tokens: int = 
             dst = src
         elif w.quant == "per_token":
             dst = w.batch * append_tokens * H * 2 * (d + 8)
+        elif w.quant == "per_token_u4":
+            dst = w.batch * append_tokens * H * 2 * (d // 2 + 8)
         else:
             dst = w.batch * H * 2 * (64 * d + 8) + w.batch * H * 2 * 64 * d * 4  # open group + tail
         res["append"] = src + dst
@@ -239,7 +243,7 @@ class Replica:
         gen.manual_seed(seed)
         self.lens = synth.seq_lens(w)
         extra = 1 if w.append_steps else 0
-        kv_name = "int8" if w.quant != "none" else w.dtype
+        kv_name, quant_name = synth.cache_kind(w)
         qdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
         self.qdt = qdt
         B, H, d, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
@@ -258,7 +262,7 @@ class Replica:
         # workloads) or extends the context (append workloads)
         for layer in range(self.layers):
             bt, pool = synth.block_tables(w, layer, extra)
-            cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=w.quant,
+            cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=quant_name,
                                  with_meta=with_meta, tail_rows=B)
             bt_d = torch.from_numpy(bt).to(dev)
             # prefill: T tokens per sequence drawn on the device, written by kv_append
@@ -382,10 +386,10 @@ def prefill_append(w: synth.Workload, with_meta: bool, peak: float) -> Dict:
     from paged_kv_cache_243_gb300.cache import PagedKVCache
     dev = torch.device("cuda")
     B, H, d, T = w.batch, w.num_kv_heads, w.head_dim, int(synth.seq_lens(w).max())
-    kv_name = "int8" if w.quant != "none" else w.dtype
+    kv_name, quant_name = synth.cache_kind(w)
     qdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
     bt, pool = synth.block_tables(w, 0, 1 if w.append_steps else 0)
-    cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=w.quant, with_meta=with_meta,
+    cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=quant_name, with_meta=with_meta,
                          tail_rows=B)
     gen = torch.Generator(device=dev)
     gen.manual_seed(w.seed + 7)
@@ -410,6 +414,8 @@ def prefill_append(w: synth.Workload, with_meta: bool, peak: float) -> Dict:
         dst = src
     elif w.quant == "per_token":
         dst = toks * H * 2 * (d + 8)
+    elif w.quant == "per_token_u4":
+        dst = toks * H * 2 * (d // 2 + 8)
     else:
         dst = toks * H * 2 * d + (toks // 64) * H * 2 * 8
     P = -(-T // w.page_size)
@@ -442,8 +448,9 @@ def extra_workloads(peak: float) -> Dict:
             e.update(extra)
         res[name] = e
 
-    # 32K dense bf16 (the >= 70 % target), W3 per-token INT8, W4 per-group INT8 + append
-    for name in ("dense_32k_bf16", "w3_gqa_int8_token", "w4_long_int8_group"):
+    # 32K dense bf16 (the >= 70 % target), W3 per-token INT8, W4 per-group INT8 +
+    # append, and the W3 shapes with per-token 4-bit codes
+    for name in ("dense_32k_bf16", "w3_gqa_int8_token", "w4_long_int8_group", "w7_gqa_u4_token"):
         w = synth.WORKLOADS[name]
         rep = Replica(w, w.seed)
         g, _ = rep.capture(append=True, attention=True)
@@ -566,6 +573,8 @@ def _stored_kv(name: str, layer: int, b: int, g: int):
     del sd
     if w.quant == "per_token":
         stored = (oracle.quantize_per_token(k), oracle.quantize_per_token(v))
+    elif w.quant == "per_token_u4":
+        stored = (oracle.quantize_per_token_u4(k), oracle.quantize_per_token_u4(v))
     elif w.quant == "per_group64":
         stored = (oracle.quantize_per_group(k), oracle.quantize_per_group(v))
     else:
@@ -590,6 +599,9 @@ def _oracle_units(args):
         if w.quant == "per_token":
             k = per_token_dequant(*stored[0])[:, 0]
             v = per_token_dequant(*stored[1])[:, 0]
+        elif w.quant == "per_token_u4":
+            k = oracle.per_token_u4_dequant(*stored[0])[:, 0]
+            v = oracle.per_token_u4_dequant(*stored[1])[:, 0]
         elif w.quant == "per_group64":
             k = per_group_dequant(*stored[0])[:, 0]
             v = per_group_dequant(*stored[1])[:, 0]

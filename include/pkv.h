@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 3
+#define PKV_ABI_VERSION 4
 
 typedef enum {
   PKV_OK = 0,
@@ -58,7 +58,9 @@ typedef enum {
 #define PKV_DEV_TIMEOUT 8       /* a bounded wait inside a kernel gave up */
 #define PKV_DEV_BAD_CONFIG 16   /* launch parameters a kernel refuses to run with */
 
-typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2, PKV_I8 = 3 } pkv_dtype;
+/* PKV_U4: unsigned 4-bit codes, two per byte (the even channel in the low
+ * nibble), for KV pools only. */
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2, PKV_I8 = 3, PKV_U4 = 4 } pkv_dtype;
 
 /* Who selects pages in pkv_page_score_topk. The pages score one query per page;
  * the group modes are this library's readings for query-head groups (GQA). */
@@ -70,8 +72,9 @@ typedef enum {
 
 typedef enum {
   PKV_QUANT_NONE = 0,       /* kv_dtype F16 or BF16: values stored as is */
-  PKV_QUANT_PER_TOKEN = 1,  /* kv_dtype I8: one (scale, zero) per token and kv head
-                               [HBM-layout page, section 二] */
+  PKV_QUANT_PER_TOKEN = 1,  /* kv_dtype I8 or U4: one (scale, zero) per token and kv head
+                               [HBM-layout page, section 二; 4-bit: KV-practice page,
+                               section 3.2] */
   PKV_QUANT_PER_GROUP64 = 2 /* kv_dtype I8: one (scale, zero) per 64 tokens and kv head
                                [Gemini page, 第一章] */
 } pkv_quant;
@@ -82,13 +85,15 @@ typedef enum {
  * physical page id [HBM-layout page, sections 二 (layout C) and 三].
  *
  * Layouts (all row-major, device memory, caller-owned):
- *   k_pages, v_pages : [num_pages][num_kv_heads][page_size][head_dim] of kv_dtype.
- *                      Token slot s of logical page i of a sequence holds its
- *                      token i * page_size + s.
- *   kv_sz            : I8 only, fp32 [num_pages][num_kv_heads][page_size / gran][4]
- *                      with gran = 1 (per token) or 64 (per group); the 4 floats
- *                      are (k_scale, k_zero, v_scale, v_zero). Restoration:
- *                      x = (code + 128) * scale + zero.
+ *   k_pages, v_pages : [num_pages][num_kv_heads][page_size][head_dim] of kv_dtype
+ *                      (U4: [..][head_dim / 2] bytes, channel 2i in the low
+ *                      nibble of byte i). Token slot s of logical page i of a
+ *                      sequence holds its token i * page_size + s.
+ *   kv_sz            : I8 and U4 only, fp32 [num_pages][num_kv_heads][page_size / gran][4]
+ *                      with gran = 1 (per token) or 64 (per group, I8 only); the
+ *                      4 floats are (k_scale, k_zero, v_scale, v_zero).
+ *                      Restoration: x = (code + 128) * scale + zero for I8
+ *                      (signed codes), x = u * scale + zero for U4 (u in [0, 15]).
  *   tail             : PER_GROUP64 only, fp32
  *                      [tail_rows][num_kv_heads][2 (K, V)][2 (group parity)][64][head_dim]:
  *                      original values of each sequence's open (partially filled)
@@ -100,14 +105,15 @@ typedef enum {
  *                      minimum (row 0) and maximum (row 1) of the page's valid
  *                      keys [TinyServe page, section 2.1]; kept in fp32
  *                      [TinyServe page, section 5.2]. For INT8 keys the box is
- *                      built from fl32(fl32((c + 128) * s) + z).
+ *                      built from fl32(fl32((c + 128) * s) + z), for 4-bit keys
+ *                      from fl32(fl32(u * s) + z).
  */
 typedef struct {
   int32_t num_pages;
   int32_t page_size;     /* multiple of 16; multiple of 64 for PER_GROUP64 */
   int32_t num_kv_heads;
   int32_t head_dim;      /* 64 or 128 */
-  pkv_dtype kv_dtype;    /* F16, BF16 (with QUANT_NONE) or I8 */
+  pkv_dtype kv_dtype;    /* F16, BF16 (with QUANT_NONE), I8, or U4 (with QUANT_PER_TOKEN) */
   pkv_quant quant;
   void* k_pages;
   void* v_pages;
@@ -149,8 +155,10 @@ void pkv_tuning_reload(void);
  * (closed groups never change). If page_meta is set, the bounding box of every
  * page the append touched is recomputed from the stored keys.
  * Quantiser (bit-exact definition, fp32 ops, ties to even):
- *   s = (max - min) / 255; z = min; code = clamp(rint((x - z) / s), 0, 255) - 128;
- *   a constant block stores s = 0 and codes -128.
+ *   I8: s = (max - min) / 255; z = min; code = clamp(rint((x - z) / s), 0, 255) - 128;
+ *       a constant block stores s = 0 and codes -128.
+ *   U4: s = (max - min) / 15; z = min; u = clamp(rint((x - z) / s), 0, 15);
+ *       a constant row stores s = 0 and codes 0.
  * Device errors: PKV_DEV_BAD_POSITION (slot beyond max_pages * page_size or
  * negative position / length), PKV_DEV_BAD_PAGE; the token is skipped.
  */
@@ -282,7 +290,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
  *   Other arguments as pkv_paged_decode_attention in dense mode; with
  *   fresh_rows >= 0 the work before the call must also leave the new rows
  *   alone (the kernel writes them before it waits for that work).
- * Caches: fp16/bf16 and per-token INT8 without page metadata; per-group INT8
+ * Caches: fp16/bf16, per-token INT8 and 4-bit without page metadata; per-group INT8
  * (which re-quantises the whole open group) and caches with page boxes return
  * PKV_ERR_UNSUPPORTED (use pkv_kv_append and pkv_paged_decode_attention).
  * Sequences with seq_lens[b] = 0 get no token.

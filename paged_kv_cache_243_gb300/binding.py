@@ -15,7 +15,7 @@ from typing import Optional
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpkv.so")
 
 # pkv_dtype / pkv_quant / status values of include/pkv.h
-F16, BF16, F32, I8 = 0, 1, 2, 3
+F16, BF16, F32, I8, U4 = 0, 1, 2, 3, 4
 QUANT_NONE, QUANT_PER_TOKEN, QUANT_PER_GROUP64 = 0, 1, 2
 SELECT_PER_HEAD, SELECT_GROUP_SUM, SELECT_GROUP_MAX = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_PAGES, ERR_CUDA, ERR_WORKSPACE = range(6)

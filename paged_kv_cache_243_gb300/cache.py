@@ -15,8 +15,9 @@ import torch
 from . import binding as B
 
 _TORCH_TO_PKV = {torch.float16: B.F16, torch.bfloat16: B.BF16, torch.float32: B.F32}
-_NAME_TO_PKV = {"f16": B.F16, "bf16": B.BF16, "int8": B.I8}
-_PKV_TO_TORCH = {B.F16: torch.float16, B.BF16: torch.bfloat16, B.F32: torch.float32, B.I8: torch.int8}
+_NAME_TO_PKV = {"f16": B.F16, "bf16": B.BF16, "int8": B.I8, "u4": B.U4}
+_PKV_TO_TORCH = {B.F16: torch.float16, B.BF16: torch.bfloat16, B.F32: torch.float32, B.I8: torch.int8,
+                 B.U4: torch.uint8}
 _QUANT = {"none": B.QUANT_NONE, "per_token": B.QUANT_PER_TOKEN, "per_group64": B.QUANT_PER_GROUP64}
 
 
@@ -56,13 +57,14 @@ class PagedKVCache:
         self.kv_dtype, self.quant = _NAME_TO_PKV[kv_dtype], _QUANT[quant]
         self.device = torch.device(device)
         tdt = _PKV_TO_TORCH[self.kv_dtype]
-        shape = (num_pages, num_kv_heads, page_size, head_dim)
+        # 4-bit codes: two per byte
+        shape = (num_pages, num_kv_heads, page_size, head_dim // 2 if self.kv_dtype == B.U4 else head_dim)
         self.k_pages = torch.empty(shape, dtype=tdt, device=self.device)
         self.v_pages = torch.empty(shape, dtype=tdt, device=self.device)
         self.device = self.k_pages.device      # concrete index (cuda:N)
         self.kv_sz = None
         self.tail = None
-        if self.kv_dtype == B.I8:
+        if self.kv_dtype in (B.I8, B.U4):
             gran = 1 if self.quant == B.QUANT_PER_TOKEN else 64
             self.kv_sz = torch.empty((num_pages, num_kv_heads, page_size // gran, 4),
                                      dtype=torch.float32, device=self.device)
@@ -74,7 +76,7 @@ class PagedKVCache:
                                       device=self.device) if with_meta else None)
         if poison:
             # unwritten slots read as NaN (float) / NaN scales (INT8): a stray read shows
-            if self.kv_dtype == B.I8:
+            if self.kv_dtype in (B.I8, B.U4):
                 self.k_pages.fill_(0)
                 self.v_pages.fill_(0)
                 self.kv_sz.fill_(float("nan"))

@@ -14,9 +14,9 @@
 namespace pkv {
 
 int attn_stage_bytes(int kv_kind, int D, bool swz) {
-  const int esz = (kv_kind == KV_I8T || kv_kind == KV_I8G) ? 1 : 2;
-  const int kb = kChunk * D * esz;
-  const int szb = kv_kind == KV_I8T ? kChunk * 16 : (kv_kind == KV_I8G ? 16 : 0);
+  const int row = kv_kind == KV_U4T ? D / 2 : ((kv_kind == KV_I8T || kv_kind == KV_I8G) ? D : 2 * D);
+  const int kb = kChunk * row;
+  const int szb = (kv_kind == KV_I8T || kv_kind == KV_U4T) ? kChunk * 16 : (kv_kind == KV_I8G ? 16 : 0);
   return stage_bytes_of(kb, szb, swz);
 }
 
@@ -146,6 +146,10 @@ pkv_status check_cache(const pkv_cache* c, bool need_pools) {
     if (c->quant != PKV_QUANT_PER_TOKEN && c->quant != PKV_QUANT_PER_GROUP64) return PKV_ERR_INVALID_ARG;
     if (c->quant == PKV_QUANT_PER_GROUP64 && c->page_size % 64 != 0) return PKV_ERR_UNSUPPORTED;
     if (need_pools && (!c->kv_sz || !aligned16(c->kv_sz))) return PKV_ERR_INVALID_ARG;
+  } else if (c->kv_dtype == PKV_U4) {
+    if (c->quant == PKV_QUANT_PER_GROUP64) return PKV_ERR_UNSUPPORTED;
+    if (c->quant != PKV_QUANT_PER_TOKEN) return PKV_ERR_INVALID_ARG;
+    if (need_pools && (!c->kv_sz || !aligned16(c->kv_sz))) return PKV_ERR_INVALID_ARG;
   } else {
     return PKV_ERR_INVALID_ARG;
   }
@@ -160,6 +164,7 @@ pkv_status check_cache(const pkv_cache* c, bool need_pools) {
 int kv_kind(const pkv_cache* c) {
   if (c->kv_dtype == PKV_F16) return KV_F16;
   if (c->kv_dtype == PKV_BF16) return KV_BF16;
+  if (c->kv_dtype == PKV_U4) return KV_U4T;
   return c->quant == PKV_QUANT_PER_TOKEN ? KV_I8T : KV_I8G;
 }
 
@@ -177,15 +182,17 @@ const void* attn_kernel(int kind, int D, int ge, bool mma) {
     case KV_F16: return attn_kernel_f16(D, ge, mma);
     case KV_BF16: return attn_kernel_bf16(D, ge, mma);
     case KV_I8T: return attn_kernel_i8t(D, ge, mma);
+    case KV_U4T: return attn_kernel_u4t(D, ge, mma);
     default: return attn_kernel_i8g(D, ge, mma);
   }
 }
 
 // The tensor-core variant serves dense query-head groups (G >= 2) when q has
 // the dtype of the products' operands: fp16 for fp16 and INT8 caches (codes
-// enter as exact fp16 integers), bf16 for bf16 caches.
+// enter as exact fp16 integers), bf16 for bf16 caches. 4-bit caches always
+// use the CUDA-core consumers.
 bool use_mma(int kind, int ge, int q_dtype, const Tuning& tn) {
-  if (ge < 2 || tn.mma == 0) return false;
+  if (ge < 2 || tn.mma == 0 || kind == KV_U4T) return false;
   return kind == KV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16;
 }
 
@@ -533,7 +540,8 @@ pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, in
   if (st != PKV_OK) return st;
   if (cache->quant == PKV_QUANT_PER_GROUP64 || cache->page_meta) return PKV_ERR_UNSUPPORTED;
   if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-  if (cache->kv_dtype != PKV_I8 && src_dtype != cache->kv_dtype) return PKV_ERR_UNSUPPORTED;
+  if ((cache->kv_dtype == PKV_F16 || cache->kv_dtype == PKV_BF16) && src_dtype != cache->kv_dtype)
+    return PKV_ERR_UNSUPPORTED;
   if (batch > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
                         nullptr, nullptr, 0, 0, out, out_dtype, num_splits, fresh_rows, k_new, v_new,

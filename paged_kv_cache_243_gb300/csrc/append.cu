@@ -2,13 +2,15 @@
 // section 三 append_kv: block = pos / block_size, slot = pos % block_size,
 // through the block table], quantising to INT8 when the cache is INT8
 // [HBM-layout page, section 二 per-token; Gemini page, 第一章 per-64-token
-// group], and refreshing the per-page channel bounding boxes of the keys
-// [TinyServe page, section 2.1].
+// group] or to 4-bit codes [KV-practice page, section 3.2; per token], and
+// refreshing the per-page channel bounding boxes of the keys [TinyServe page,
+// section 2.1].
 //
-// The quantiser is an exact fp32 operation sequence (correctly rounded
+// The quantisers are exact fp32 operation sequences (correctly rounded
 // subtract and divide, round half to even), so codes, scales and zero-points
 // are bit-identical to any other IEEE implementation of the same sequence:
-//   s = (max - min) / 255, z = min, code = clamp(rint((x - z) / s), 0, 255) - 128.
+//   INT8: s = (max - min) / 255, z = min, code = clamp(rint((x - z) / s), 0, 255) - 128;
+//   4-bit: s = (max - min) / 15, z = min, u = clamp(rint((x - z) / s), 0, 15).
 #include "pkv_internal.h"
 #include "quant.cuh"
 
@@ -103,13 +105,13 @@ __global__ void append_copy_kernel(const AppendParams p) {
   }
 }
 
-// Per-token INT8: 8 lanes per (row, token, kv head, K|V), each quantising D/8
-// consecutive values, so a warp serves 4 consecutive tokens of one (row, kv
-// head, K|V) and the per-token work (min/max across lanes, scale, reciprocal)
-// is shared by 8 lanes, not 32. The source values are loaded before the
-// position and block-table lookups.
+// Per-token INT8 (U4: per-token 4-bit codes, two per byte): 8 lanes per (row,
+// token, kv head, K|V), each quantising D/8 consecutive values, so a warp
+// serves 4 consecutive tokens of one (row, kv head, K|V) and the per-token work
+// (min/max across lanes, scale, reciprocal) is shared by 8 lanes, not 32. The
+// source values are loaded before the position and block-table lookups.
 constexpr int kTokPerWarp = 4;
-template <int D>
+template <int D, bool U4>
 __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -155,17 +157,27 @@ __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParam
     if (part == 0) flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
     return;
   }
-  const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), U4 ? 15.f : 255.f);
   const float z = mn;
   const float rs = quant_recip(s);
-  uint32_t w[EPL / 4];
-  quant_words<EPL>(x, s, z, rs, w);
   const size_t row = ((size_t)phys * H + g) * p.page_size + tp % p.page_size;
-  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
-  if constexpr (EPL == 16)
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-  else
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  if constexpr (U4) {
+    uint32_t w[EPL / 8];
+    quant_nibbles<EPL>(x, s, z, rs, w);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? p.v_pages : p.k_pages) + row * (D / 2) + part * (EPL / 2);
+    if constexpr (EPL == 16)
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = w[0];
+  } else {
+    uint32_t w[EPL / 4];
+    quant_words<EPL>(x, s, z, rs, w);
+    int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
+    if constexpr (EPL == 16)
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  }
   if (part == 0) {
     p.kv_sz[row * 4 + kv * 2 + 0] = s;
     p.kv_sz[row * 4 + kv * 2 + 1] = z;
@@ -319,6 +331,11 @@ __global__ void append_meta_kernel(const AppendParams p) {
                               ? p.kv_sz + (row0 + s) * 4
                               : p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + s / 64) * 4;
         x[k] = __fadd_rn(__fmul_rn((float)(code + 128), sz[0]), sz[1]);
+      } else if (p.kv_dtype == PKV_U4) {
+        const uint32_t byte = reinterpret_cast<const uint8_t*>(p.k_pages)[(row0 + s) * (D / 2) + i / 2];
+        const float u = (float)((i & 1) ? byte >> 4 : byte & 0xFu);
+        const float* sz = p.kv_sz + (row0 + s) * 4;
+        x[k] = __fadd_rn(__fmul_rn(u, sz[0]), sz[1]);
       } else {
         x[k] = load_src(p.k_pages, p.kv_dtype, (row0 + s) * D + i);
       }
@@ -341,14 +358,18 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
   AppendParams pc = p;
   void* args1[] = {&pc};
   cudaError_t e = cudaSuccess;
-  if (p.kv_dtype != PKV_I8) {
+  if (p.kv_dtype == PKV_F16 || p.kv_dtype == PKV_BF16) {
     e = launch_pdl(reinterpret_cast<const void*>(&append_copy_kernel), dim3(p.t_new, p.batch), dim3(256), 0,
                    st, args1);
   } else if (p.quant == PKV_QUANT_PER_TOKEN) {
     const long long warps = (long long)p.batch * ((p.t_new + kTokPerWarp - 1) / kTokPerWarp) * H * 2;
     const long long blocks = (warps * 32 + 255) / 256;
-    const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&append_per_token_kernel<128>)
-                                       : reinterpret_cast<const void*>(&append_per_token_kernel<64>);
+    const bool u4 = p.kv_dtype == PKV_U4;
+    const void* fn = p.head_dim == 128
+                         ? (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<128, true>)
+                               : reinterpret_cast<const void*>(&append_per_token_kernel<128, false>))
+                         : (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<64, true>)
+                               : reinterpret_cast<const void*>(&append_per_token_kernel<64, false>));
     e = launch_pdl(fn, dim3((unsigned)blocks), dim3(256), 0, st, args1);
   } else {
     const int groups = (p.t_new + 63) / 64 + 1;

@@ -119,10 +119,11 @@ struct ChunkInfo {
 
 template <int D, int KV>
 struct AttnGeom {
-  static constexpr int ESZ = (KV == KV_I8T || KV == KV_I8G) ? 1 : 2;
-  static constexpr int ROW = D * ESZ;              // bytes of one token row
+  static constexpr int ESZ = (KV == KV_I8T || KV == KV_I8G || KV == KV_U4T) ? 1 : 2;
+  static constexpr bool PTOK = KV == KV_I8T || KV == KV_U4T;   // per-token scales
+  static constexpr int ROW = KV == KV_U4T ? D / 2 : D * ESZ;  // bytes of one token row
   static constexpr int KB = kChunk * ROW;          // bytes of one chunk of K (or V)
-  static constexpr int SZB = KV == KV_I8T ? kChunk * 16 : (KV == KV_I8G ? 16 : 0);
+  static constexpr int SZB = PTOK ? kChunk * 16 : (KV == KV_I8G ? 16 : 0);
   static constexpr int STAGE = ((2 * KB + SZB) + 127) / 128 * 128;
   static constexpr int QD = D / 8;                 // channels per lane in the score layout
   static constexpr int PD = D / 32;                // channels per lane in the value layout
@@ -131,7 +132,7 @@ struct AttnGeom {
   // row r lands at block j ^ (r % 8)), which makes its fragment loads free of
   // bank conflicts; its ring stages hold the two tiles (1024-byte aligned) and
   // the scales sit in a separate array.
-  static constexpr bool SWZ_OK = ESZ == 1 && D == 128;
+  static constexpr bool SWZ_OK = ESZ == 1 && D == 128 && KV != KV_U4T;
   static constexpr int TILE_STAGE = 2 * KB;
 };
 
@@ -174,7 +175,7 @@ __device__ __forceinline__ int qk_dim(int j, int e) {
 }
 
 // Load this lane's D/8 channels of token row `row` (score layout) as packed
-// fp32 pairs (INT8: u = code + 128).
+// fp32 pairs (INT8: u = code + 128; 4-bit: u = the code).
 template <int D, int KV>
 __device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, uint64_t (&k2)[D / 16]) {
   if constexpr (KV == KV_F16 || KV == KV_BF16) {
@@ -186,6 +187,24 @@ __device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, uint64_t
     } else {
       const uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
       k2[0] = widen2<KV>(a.x); k2[1] = widen2<KV>(a.y); k2[2] = widen2<KV>(a.z); k2[3] = widen2<KV>(a.w);
+    }
+  } else if constexpr (KV == KV_U4T) {
+    // D / 8 channels = D / 16 bytes per lane; pair i = the two nibbles of byte i
+    if constexpr (D == 128) {
+      const uint2 a = *reinterpret_cast<const uint2*>(row + j * 8);
+      uint32_t lo0, hi0, lo1, hi1;
+      split_nibbles(a.x, lo0, hi0);
+      split_nibbles(a.y, lo1, hi1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) k2[i] = u4pair(lo0, hi0, i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) k2[4 + i] = u4pair(lo1, hi1, i);
+    } else {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(row + j * 4);
+      uint32_t lo, hi;
+      split_nibbles(a, lo, hi);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) k2[i] = u4pair(lo, hi, i);
     }
   } else {
     if constexpr (D == 128) {
@@ -212,6 +231,17 @@ __device__ __forceinline__ void load_v_slice(const uint8_t* row, int lane, uint6
       v2[1] = widen2<KV>(a.y);
     } else {
       v2[0] = widen2<KV>(*reinterpret_cast<const uint32_t*>(row + lane * 4));
+    }
+  } else if constexpr (KV == KV_U4T) {
+    // D / 32 channels = D / 64 bytes per lane
+    uint32_t lo, hi;
+    if constexpr (D == 128) {
+      split_nibbles((uint32_t)*reinterpret_cast<const uint16_t*>(row + lane * 2), lo, hi);
+      v2[0] = u4pair(lo, hi, 0);
+      v2[1] = u4pair(lo, hi, 1);
+    } else {
+      split_nibbles((uint32_t)row[lane], lo, hi);
+      v2[0] = u4pair(lo, hi, 0);
     }
   } else {
     if constexpr (D == 128) {
@@ -355,15 +385,16 @@ __device__ __forceinline__ int cta_of(long long x, long long W, long long N) {
 // Fused append of one token row (K and V of one kv head) at row r of the
 // chunk whose K, V (and per-token scale) rows start at ck, cv (csz), by the 32
 // lanes of a warp: a copy for fp16/bf16 caches (source dtype = cache dtype),
-// the per-token quantiser of kv_append for INT8 caches [HBM-layout page,
-// section 二].
+// the per-token quantiser of kv_append for INT8 [HBM-layout page, section 二]
+// and 4-bit caches.
 template <int D, int KV>
 __device__ __forceinline__ void append_token_row(const AttnParams& p, int u, int r, uint8_t* ck, uint8_t* cv,
                                                  float* csz, int lane) {
   const int b = u / p.units_per_b, g = u - b * p.units_per_b;
   const size_t src = ((size_t)b * p.num_kv_heads + g) * D;
   constexpr int PL = D / 32;   // values per lane
-  if constexpr (KV == KV_I8T) {
+  if constexpr (KV == KV_I8T || KV == KV_U4T) {
+    constexpr bool U4 = KV == KV_U4T;
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
       const void* sp = kv ? p.v_new : p.k_new;
@@ -386,15 +417,25 @@ __device__ __forceinline__ void append_token_row(const AttnParams& p, int u, int
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       }
-      const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
+      const float s = __fdiv_rn(__fsub_rn(mx, mn), U4 ? 15.f : 255.f);
       const float z = mn;
       uint32_t w[1];
-      quant_words<4>(x, s, z, quant_recip(s), w);
-      uint8_t* dst = (kv ? cv : ck) + (size_t)r * D + lane * PL;
-      if constexpr (PL == 4)
-        *reinterpret_cast<uint32_t*>(dst) = w[0];
-      else
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+      if constexpr (U4) {
+        // 4 values (D = 64: the lane's 2 values twice) -> 2 bytes of nibbles
+        quant_nibbles<4>(x, s, z, quant_recip(s), w);
+        uint8_t* dst = (kv ? cv : ck) + (size_t)r * (D / 2) + lane * (PL / 2);
+        if constexpr (PL == 4)
+          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+        else
+          *dst = (uint8_t)w[0];
+      } else {
+        quant_words<4>(x, s, z, quant_recip(s), w);
+        uint8_t* dst = (kv ? cv : ck) + (size_t)r * D + lane * PL;
+        if constexpr (PL == 4)
+          *reinterpret_cast<uint32_t*>(dst) = w[0];
+        else
+          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+      }
       if (lane == 0) {
         csz[r * 4 + kv * 2 + 0] = s;
         csz[r * 4 + kv * 2 + 1] = z;
@@ -631,7 +672,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       ci.k = p.k_pages + row0 * Geo::ROW;
       ci.v = p.v_pages + row0 * Geo::ROW;
       ci.row = (int)row0;   // the host keeps pool rows below 2^31 for tensor copies
-      if constexpr (KV == KV_I8T) ci.sz = p.kv_sz + row0 * 4;
+      if constexpr (Geo::PTOK) ci.sz = p.kv_sz + row0 * 4;
       if constexpr (KV == KV_I8G)
         ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
       ci.nvalid = nv;
@@ -667,7 +708,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       for (int k0 = 0; k0 < cnt; k0 += S) {
         const bool mine = lane >= k0 && lane < min(cnt, k0 + S);
         if (!waited && __any_sync(0xffffffffu, mine && e.fresh)) wait_prior();
-        if constexpr (KV == KV_F16 || KV == KV_BF16 || KV == KV_I8T) {
+        if constexpr (KV != KV_I8G) {
           unsigned todo = p.k_new ? __ballot_sync(0xffffffffu, mine && e.valid && e.last) : 0u;
           if (todo) {
             // the new token of each of these units, written by the whole warp;
@@ -941,7 +982,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
           part[h] = hsum2(a);
         }
         float sv = reduce_scatter8<GE>(part, j);
-        if constexpr (KV == KV_I8T) sv = fmaf(sz[t * 4 + 0], sv, sz[t * 4 + 1] * qsum);
+        if constexpr (Geo::PTOK) sv = fmaf(sz[t * 4 + 0], sv, sz[t * 4 + 1] * qsum);
         if constexpr (KV == KV_I8G) sv = fmaf(ks, sv, kz * qsum);
         sc[it] = t < nvalid ? sv : -INFINITY;
       }
@@ -957,7 +998,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       for (int it = 0; it < 4; ++it) {
         const float pe = exp2f(sc[it] - m_new);
         psum += pe;
-        if constexpr (KV == KV_I8T) {
+        if constexpr (Geo::PTOK) {
           const int t = 4 * it + r;
           if (t < nvalid) {
             pz = fmaf(pe, sz[t * 4 + 3], pz);
@@ -974,7 +1015,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       psum += __shfl_xor_sync(0xffffffffu, psum, 8);
       psum += __shfl_xor_sync(0xffffffffu, psum, 16);
       l_h = fmaf(l_h, alpha, psum);
-      if constexpr (KV == KV_I8T) {
+      if constexpr (Geo::PTOK) {
         pz += __shfl_xor_sync(0xffffffffu, pz, 8);
         pz += __shfl_xor_sync(0xffffffffu, pz, 16);
         zs = fmaf(zs, alpha, pz);

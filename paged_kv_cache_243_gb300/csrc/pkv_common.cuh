@@ -15,7 +15,8 @@ namespace pkv {
 // one (page, kv head) is one contiguous run of 16 * head_dim elements.
 constexpr int kChunk = 16;
 
-enum KvKind : int { KV_F16 = 0, KV_BF16 = 1, KV_I8T = 2, KV_I8G = 3 };
+// KV_U4T: per-token 4-bit codes, two per byte (even channel in the low nibble).
+enum KvKind : int { KV_F16 = 0, KV_BF16 = 1, KV_I8T = 2, KV_I8G = 3, KV_U4T = 4 };
 
 // ---------------------------------------------------------------- conversions
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -65,6 +66,13 @@ __device__ __forceinline__ void flag_status(int32_t* st, int bit) {
   if (st) atomicOr(st, bit);
 }
 
+// 4-bit codes of the four bytes of w (channels 2i in the low nibble, 2i + 1
+// in the high one): lo = the low nibbles, hi = the high nibbles, one per byte.
+__device__ __forceinline__ void split_nibbles(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = w & 0x0F0F0F0Fu;
+  hi = (w >> 4) & 0x0F0F0F0Fu;
+}
+
 // ------------------------------------------------- packed fp32 pairs (f32x2)
 // Two fp32 values in one 64-bit register pair; the .f32x2 forms of fma / add /
 // sub / mul issue both lanes in one instruction (sm_100 and later).
@@ -103,6 +111,14 @@ __device__ __forceinline__ uint64_t widen2(uint32_t w) {
   float a, b;
   unpack2<KV>(w, a, b);
   return pack2f(a, b);
+}
+
+// Byte i of the low-nibble word and of the high-nibble word (split_nibbles) as
+// the pair (u_2i, u_2i+1) of 4-bit codes.
+__device__ __forceinline__ uint64_t u4pair(uint32_t lo, uint32_t hi, int i) {
+  const float a = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + (uint32_t)i));
+  const float b = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + (uint32_t)i));
+  return fsub2(pack2f(a, b), pack2f(8388608.0f, 8388608.0f));
 }
 
 // Bytes i, i+1 of a sign-flipped INT8 word as the pair (u_i, u_i+1), u = code + 128.

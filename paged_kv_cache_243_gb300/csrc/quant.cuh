@@ -54,6 +54,36 @@ __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float 
   }
 }
 
+// 4-bit codes [per-token 4-bit reading of the KV-practice page, section 3.2]:
+// s = (max - min) / 15, z = min, u = clamp(rint((x - z) / s), 0, 15), each
+// step a correctly rounded fp32 operation, as quant_words: rint through the
+// reciprocal rs unless a product lies within 1e-3 of a half-integer (then the
+// quotient itself). N values (N even) -> N / 2 bytes, value 2i in the low
+// nibble of byte i; w[k] holds bytes 4k .. 4k + 3.
+template <int N>
+__device__ __forceinline__ void quant_nibbles(const float (&x)[N], float s, float z, float rs,
+                                              uint32_t (&w)[(N + 7) / 8]) {
+#pragma unroll
+  for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
+  if (s == 0.f) return;   // constant row: every code 0
+  float d[N], m[N];
+  bool near = rs == 0.f;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    d[e] = __fsub_rn(x[e], z);
+    const float q = __fmul_rn(d[e], rs);
+    m[e] = __fadd_rn(q, kRoundMagic);
+    const float diff = __fsub_rn(q, __fsub_rn(m[e], kRoundMagic));
+    near |= fabsf(diff) > 0.499f;
+  }
+  if (__any_sync(__activemask(), near)) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) m[e] = __fadd_rn(__fdiv_rn(d[e], s), kRoundMagic);
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e) w[e / 8] |= (__float_as_uint(m[e]) & 0xFu) << (4 * (e % 8));
+}
+
 // Four consecutive source values (f16/bf16) widened to fp32; i is a multiple of 4.
 __device__ __forceinline__ float4 load_src4(const void* p, int dtype, size_t i) {
   const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p) + i);

@@ -7,5 +7,5 @@ oracle take their inputs from here, so neither ever feeds the other.
 from .workloads import (  # noqa: F401
     WORKLOADS, Workload, SeqData, f32_to_bf16_bits, bf16_bits_to_f32,
     round_to_dtype, make_workload, seq_tokens, queries, block_tables,
-    append_tokens, seq_lens, outlier_channels, scaled,
+    append_tokens, seq_lens, outlier_channels, scaled, cache_kind,
 )

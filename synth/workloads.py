@@ -56,7 +56,7 @@ class Workload:
     head_dim: int
     page_size: int
     dtype: str                      # source dtype of q and of the K/V tokens
-    quant: str                      # "none" | "per_token" | "per_group64"
+    quant: str                      # "none" | "per_token" | "per_group64" | "per_token_u4"
     seq_len: Optional[int]          # fixed context length, or None for a drawn mix
     seq_len_range: Optional[Tuple[int, int]] = None
     pool_pages: Optional[int] = None   # physical pages per layer (None: as needed)
@@ -112,6 +112,12 @@ WORKLOADS: Dict[str, Workload] = {
         outlier_channels=4, outlier_scale=15.0, page_offset_std=0.5, top_k_ratio=0.3,
         description="GQA 32/8 per-token INT8 sparse: B=8, d=128, L=16384, page 16, per-page K "
                     "offset ~ N(0, 0.5^2), top-K 30 % per kv head from the group's summed scores"),
+    "w7_gqa_u4_token": Workload(
+        name="w7_gqa_u4_token", seed=1242, batch=16, layers=1, num_q_heads=32, num_kv_heads=8,
+        head_dim=128, page_size=16, dtype="f16", quant="per_token_u4", seq_len=None,
+        seq_len_range=(1024, 32768), outlier_channels=4, outlier_scale=15.0,
+        description="GQA 32/8 per-token 4-bit KV: B=16, d=128, L ~ U[1024, 32768], page 16, "
+                    "4 of 128 K channels per kv head x15 (the GQA INT8 workload's shapes)"),
     "dense_32k_bf16": Workload(
         name="dense_32k_bf16", seed=1240, batch=4, layers=1, num_q_heads=32, num_kv_heads=32,
         head_dim=128, page_size=16, dtype="bf16", quant="none", seq_len=32768,
@@ -232,3 +238,12 @@ def make_workload(name: str) -> Workload:
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of a workload with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)
+
+
+def cache_kind(w: Workload) -> Tuple[str, str]:
+    """(storage dtype name, quantisation name) of a workload's cache."""
+    if w.quant == "none":
+        return w.dtype, "none"
+    if w.quant == "per_token_u4":
+        return "u4", "per_token"
+    return "int8", w.quant

@@ -16,6 +16,7 @@ import oracle
 import synth
 from oracle.quant import (per_group_bbox_values, per_group_dequant, per_token_bbox_values,
                           per_token_dequant)
+from oracle.quant4 import per_token_u4_bbox_values, per_token_u4_dequant
 
 # Tolerances on attention outputs (max-abs, fp32 outputs), per input precision.
 TOL = {"bf16": 2e-3, "f16": 1e-3, "int8": 1e-3}
@@ -66,9 +67,9 @@ def load_workload(w: synth.Workload, layer: int = 0, lens: Optional[np.ndarray] 
         lens = np.asarray(lens, dtype=np.int32)
         bt, pool = _block_tables(w, lens, layer, extra_pages)
     lens = np.asarray(lens, dtype=np.int32)
-    kv_name = "int8" if w.quant != "none" else w.dtype
+    kv_name, quant_name = synth.cache_kind(w)
     cache = PagedKVCache(pool, w.page_size, w.num_kv_heads, w.head_dim, kv_dtype=kv_name,
-                         quant=w.quant, with_meta=with_meta, tail_rows=w.batch, poison=poison)
+                         quant=quant_name, with_meta=with_meta, tail_rows=w.batch, poison=poison)
     seqs = [synth.seq_tokens(w, b, layer, int(lens[b])) for b in range(w.batch)]
     bt_dev = torch.from_numpy(bt).cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -127,6 +128,9 @@ def oracle_kv(ld: Loaded, b: int):
         kc, ks, kz = oracle.quantize_per_token(sd.k)
         vc, vs, vz = oracle.quantize_per_token(sd.v)
         return per_token_dequant(kc, ks, kz), per_token_dequant(vc, vs, vz)
+    if w.quant == "per_token_u4":
+        return (per_token_u4_dequant(*oracle.quantize_per_token_u4(sd.k)),
+                per_token_u4_dequant(*oracle.quantize_per_token_u4(sd.v)))
     kc, ks, kz = oracle.quantize_per_group(sd.k)
     vc, vs, vz = oracle.quantize_per_group(sd.v)
     return per_group_dequant(kc, ks, kz), per_group_dequant(vc, vs, vz)
@@ -139,6 +143,8 @@ def oracle_bbox_keys(w, sd: synth.SeqData) -> np.ndarray:
     if w.quant == "per_token":
         kc, ks, kz = oracle.quantize_per_token(sd.k)
         return per_token_bbox_values(kc, ks, kz)
+    if w.quant == "per_token_u4":
+        return per_token_u4_bbox_values(*oracle.quantize_per_token_u4(sd.k))
     kc, ks, kz = oracle.quantize_per_group(sd.k)
     return per_group_bbox_values(kc, ks, kz)
 
@@ -200,3 +206,18 @@ def check_per_group_codes(ld):
             gs = sz[ld.bt[b][t0 // ps], :, (t0 % ps) // 64]   # [ng][Hkv][4]
             assert np.array_equal(gs[:, :, col].view(np.uint32), s.view(np.uint32))
             assert np.array_equal(gs[:, :, col + 1].view(np.uint32), z.view(np.uint32))
+
+
+def check_per_token_u4_codes(ld):
+    """Packed 4-bit codes, scales and zero-points bit-exact against the oracle's
+    quantiser, gathered through the block table."""
+    kp, vp, sz = pools(ld)
+    ps = ld.w.page_size
+    for b in range(ld.w.batch):
+        L = int(ld.lens[b])
+        for x, pool, col in ((ld.seqs[b].k, kp, 0), (ld.seqs[b].v, vp, 2)):
+            c, s, z = oracle.quantize_per_token_u4(x)
+            assert np.array_equal(gather(pool, ld.bt[b], L, ps), oracle.pack_u4(c))
+            g = gather(sz, ld.bt[b], L, ps)
+            assert np.array_equal(g[:, :, col].view(np.uint32), s.view(np.uint32))
+            assert np.array_equal(g[:, :, col + 1].view(np.uint32), z.view(np.uint32))

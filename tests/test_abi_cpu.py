@@ -35,7 +35,8 @@ def test_exports_every_declared_symbol(B):
 
 
 def test_status_strings_and_version(B):
-    assert B.abi_version() == 3
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    assert B.abi_version() == int(re.search(r"#define PKV_ABI_VERSION (\d+)", src).group(1))
     assert B.status_string(B.OK) == "ok"
     assert B.status_string(B.ERR_OUT_OF_PAGES) == "out of pages"
 
@@ -55,6 +56,9 @@ def test_argument_checks_before_cuda(B):
         (_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000, page_size=32), B.ERR_UNSUPPORTED),
         (_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_TOKEN, kv_sz=0), B.ERR_INVALID_ARG),
         (_desc(B, kv_dtype=B.F16, quant=B.QUANT_PER_TOKEN), B.ERR_INVALID_ARG),
+        (_desc(B, kv_dtype=B.U4, quant=B.QUANT_PER_TOKEN, kv_sz=0), B.ERR_INVALID_ARG),
+        (_desc(B, kv_dtype=B.U4, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000, page_size=64), B.ERR_UNSUPPORTED),
+        (_desc(B, kv_dtype=B.U4, quant=B.QUANT_NONE, kv_sz=0x3000), B.ERR_INVALID_ARG),
         (_desc(B, k_pages=0x1001), B.ERR_INVALID_ARG),
         (_desc(B, num_pages=0), B.ERR_INVALID_ARG),
     ]

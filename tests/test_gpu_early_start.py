@@ -22,6 +22,8 @@ def _restored(w, k):
         return k.astype(np.float64)
     if w.quant == "per_token":
         return per_token_dequant(*oracle.quantize_per_token(k))
+    if w.quant == "per_token_u4":
+        return oracle.per_token_u4_dequant(*oracle.quantize_per_token_u4(k))
     return per_group_dequant(*oracle.quantize_per_group(k))
 
 
@@ -31,6 +33,7 @@ CASES = [
     ("f16-mha", "f16", "none", 64, 4, 4, 32),
     ("i8-token", "f16", "per_token", 128, 8, 2, 16),
     ("i8-group", "f16", "per_group64", 128, 16, 4, 64),
+    ("u4-token", "f16", "per_token_u4", 128, 8, 2, 16),
 ]
 
 
