@@ -397,18 +397,20 @@ def prefill_append(w: synth.Workload, with_meta: bool, peak: float) -> Dict:
     v = torch.randn((B, T, H, d), generator=gen, device=dev).to(qdt)
     bt_d = torch.from_numpy(bt).to(dev)
     pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    lens = synth.seq_lens(w)
+    new_lens = torch.from_numpy(lens.astype(np.int32)).to(dev)   # each sequence's own length
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        cache.append(k, v, bt_d, pos, dev_status=status, stream=s)
+        cache.append(k, v, bt_d, pos, new_lens, dev_status=status, stream=s)
     s.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        cache.append(k, v, bt_d, pos, dev_status=status, stream=torch.cuda.current_stream())
+        cache.append(k, v, bt_d, pos, new_lens, dev_status=status, stream=torch.cuda.current_stream())
     torch.cuda.synchronize()
     ms = time_graph(g, 10, 3)
-    toks = B * T
+    toks = int(lens.sum())
     src = toks * H * d * 2 * 2
     if w.quant == "none":
         dst = src
@@ -418,9 +420,8 @@ def prefill_append(w: synth.Workload, with_meta: bool, peak: float) -> Dict:
         dst = toks * H * 2 * (d // 2 + 8)
     else:
         dst = toks * H * 2 * d + (toks // 64) * H * 2 * 8
-    P = -(-T // w.page_size)
     if with_meta:
-        dst += B * P * H * 2 * d * 4
+        dst += int(((lens + w.page_size - 1) // w.page_size).sum()) * H * 2 * d * 4
     byts = src + dst
     gbs = byts / (ms * 1e-3) / 1e9
     out = {"tokens": toks, "ms": round(ms, 4), "bytes": int(byts), "gb_s": round(gbs, 1),

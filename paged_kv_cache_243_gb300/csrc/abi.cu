@@ -563,6 +563,7 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
       (!cache->tail || !aligned16(cache->tail) || cache->tail_rows < batch))
     return PKV_ERR_INVALID_ARG;
   if ((long long)t_new > (long long)max_pages * cache->page_size) return PKV_ERR_INVALID_ARG;
+  if (batch > 65535 || cache->num_kv_heads > 32767) return PKV_ERR_UNSUPPORTED;   // grid y / z limits
   AppendParams p;
   p.k_pages = cache->k_pages;
   p.v_pages = cache->v_pages;

@@ -105,82 +105,94 @@ __global__ void append_copy_kernel(const AppendParams p) {
   }
 }
 
-// Per-token INT8 (U4: per-token 4-bit codes, two per byte): 8 lanes per (row,
-// token, kv head, K|V), each quantising D/8 consecutive values, so a warp
-// serves 4 consecutive tokens of one (row, kv head, K|V) and the per-token work
-// (min/max across lanes, scale, reciprocal) is shared by 8 lanes, not 32. The
-// source values are loaded before the position and block-table lookups.
-constexpr int kTokPerWarp = 4;
+// Per-token INT8 (U4: per-token 4-bit codes, two per byte): 8 lanes per
+// token, each quantising D/8 consecutive values, so the per-token work
+// (min/max across lanes, scale, reciprocal) is shared by 8 lanes, not 32.
+// grid (token blocks, kv head * 2 + K|V, row), up to 8 warps per block (fewer
+// for short appends): warp w of a block serves tokens 8w .. 8w + 7 of the
+// block's as two groups of 4, whose source rows are all loaded before either
+// is processed (and before the position and block-table lookups), so a warp
+// keeps 2 KB of loads in flight.
+constexpr int kTokPerWarp = 8;
 template <int D, bool U4>
 __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParams p) {
   pdl_wait();
   pdl_launch_dependents();
   constexpr int EPL = D / 8;   // values per lane: 16 (D = 128) or 8 (D = 64)
-  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, sub = lane >> 3, part = lane & 7;
   const int H = p.num_kv_heads;
-  const int tblocks = (p.t_new + kTokPerWarp - 1) / kTokPerWarp;
-  const long long total = (long long)p.batch * tblocks * H * 2;
-  if (wid >= total) return;
-  const int kv = (int)(wid & 1);
-  const int g = (int)((wid >> 1) % H);
-  const long long rest = (wid >> 1) / H;
-  const int t = (int)(rest % tblocks) * kTokPerWarp + sub, b = (int)(rest / tblocks);
-  const void* sp = kv ? p.v_new : p.k_new;
-  float x[EPL];
-  {
-    const size_t src = (((size_t)b * p.t_new + (t < p.t_new ? t : 0)) * H + g) * D + part * EPL;
+  const int kv = blockIdx.y & 1, g = blockIdx.y >> 1, b = blockIdx.z;
+  const int tpb = (blockDim.x >> 5) * kTokPerWarp;
+  const int wt = blockIdx.x * tpb + (threadIdx.x >> 5) * kTokPerWarp;   // the warp's first token
+  if (wt >= p.t_new) return;   // warp-uniform
+  const uint16_t* sp = reinterpret_cast<const uint16_t*>(kv ? p.v_new : p.k_new);
+  uint2 raw[2][EPL / 4];
 #pragma unroll
-    for (int e = 0; e < EPL; e += 4) {
-      const float4 f = load_src4(sp, p.src_dtype, src + e);
-      x[e] = f.x; x[e + 1] = f.y; x[e + 2] = f.z; x[e + 3] = f.w;
-    }
+  for (int gi = 0; gi < 2; ++gi) {
+    const int t = wt + 4 * gi + sub;
+    const uint16_t* src = sp + (((size_t)b * p.t_new + (t < p.t_new ? t : 0)) * H + g) * D + part * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL / 4; ++e) raw[gi][e] = reinterpret_cast<const uint2*>(src)[e];
   }
   int pos, n;
   if (!row_window(p, b, pos, n)) return;
-  const bool live = t < n;
-  const int tp = pos + t;
-  const int phys = live ? p.block_table[(size_t)b * p.max_pages + tp / p.page_size] : -1;
-  float mn = x[0], mx = x[0];
+  int phys[2];
 #pragma unroll
-  for (int e = 1; e < EPL; ++e) {
-    mn = fminf(mn, x[e]);
-    mx = fmaxf(mx, x[e]);
+  for (int gi = 0; gi < 2; ++gi) {
+    const int t = wt + 4 * gi + sub;
+    phys[gi] = t < n ? p.block_table[(size_t)b * p.max_pages + (pos + t) / p.page_size] : -1;
   }
 #pragma unroll
-  for (int off = 4; off > 0; off >>= 1) {   // the token's 8 lanes
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
-  if (!live) return;
-  if (phys < 0 || phys >= p.num_pages) {
-    if (part == 0) flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
-    return;
-  }
-  const float s = __fdiv_rn(__fsub_rn(mx, mn), U4 ? 15.f : 255.f);
-  const float z = mn;
-  const float rs = quant_recip(s);
-  const size_t row = ((size_t)phys * H + g) * p.page_size + tp % p.page_size;
-  if constexpr (U4) {
-    uint32_t w[EPL / 8];
-    quant_nibbles<EPL>(x, s, z, rs, w);
-    uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? p.v_pages : p.k_pages) + row * (D / 2) + part * (EPL / 2);
-    if constexpr (EPL == 16)
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    else
-      *reinterpret_cast<uint32_t*>(dst) = w[0];
-  } else {
-    uint32_t w[EPL / 4];
-    quant_words<EPL>(x, s, z, rs, w);
-    int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
-    if constexpr (EPL == 16)
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    else
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-  }
-  if (part == 0) {
-    p.kv_sz[row * 4 + kv * 2 + 0] = s;
-    p.kv_sz[row * 4 + kv * 2 + 1] = z;
+  for (int gi = 0; gi < 2; ++gi) {
+    const int t = wt + 4 * gi + sub;
+    float x[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL / 4; ++e) {
+      const float4 f = widen4(raw[gi][e], p.src_dtype);
+      x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int e = 1; e < EPL; ++e) {
+      mn = fminf(mn, x[e]);
+      mx = fmaxf(mx, x[e]);
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {   // the token's 8 lanes
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (t >= n) continue;
+    const int ph = phys[gi];
+    if (ph < 0 || ph >= p.num_pages) {
+      if (part == 0) flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+      continue;
+    }
+    const float s = __fdiv_rn(__fsub_rn(mx, mn), U4 ? 15.f : 255.f);
+    const float z = mn;
+    const float rs = quant_recip(s);
+    const size_t row = ((size_t)ph * H + g) * p.page_size + (pos + t) % p.page_size;
+    if constexpr (U4) {
+      uint32_t w[EPL / 8];
+      quant_nibbles<EPL>(x, s, z, rs, w);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? p.v_pages : p.k_pages) + row * (D / 2) + part * (EPL / 2);
+      if constexpr (EPL == 16)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      else
+        *reinterpret_cast<uint32_t*>(dst) = w[0];
+    } else {
+      uint32_t w[EPL / 4];
+      quant_words<EPL>(x, s, z, rs, w);
+      int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
+      if constexpr (EPL == 16)
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      else
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    }
+    if (part == 0) {
+      p.kv_sz[row * 4 + kv * 2 + 0] = s;
+      p.kv_sz[row * 4 + kv * 2 + 1] = z;
+    }
   }
 }
 
@@ -196,14 +208,15 @@ __device__ __forceinline__ float* tail_row(const AppendParams& p, int b, int g, 
 // of its loads (tail and new tokens) are issued before the first use, and
 // before the block-table lookup, so the block pays about one memory latency.
 constexpr int kGroupThreads = 256;
-constexpr int kGroupVec4 = 64 * 128 / 4 / kGroupThreads;   // head_dim <= 128
+template <int D>
 __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(const AppendParams p, int write_tail) {
+  constexpr int kGroupVec4 = 64 * D / 4 / kGroupThreads;   // float4s of a full group per thread
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red_mn[kGroupThreads / 32], red_mx[kGroupThreads / 32];
   __shared__ int ok_s;
   const int b = blockIdx.z, g = blockIdx.y >> 1, kv = blockIdx.y & 1;
-  const int D = p.head_dim, H = p.num_kv_heads;
+  const int H = p.num_kv_heads;
   int pos, n;
   if (!row_window(p, b, pos, n)) return;
   const int gi = pos / 64 + blockIdx.x;
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(cons
     const int f = threadIdx.x + k * kGroupThreads;
     if (f < nf) {
       const int i = 4 * f, tt = i / D, e = i - tt * D, tok = t0 + tt;
-      x[k] = tok < pos ? *reinterpret_cast<const float4*>(tl + (size_t)tt * D + e)
+      x[k] = tok < pos ? *reinterpret_cast<const float4*>(tl + i)
                        : load_src4(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
     }
   }
@@ -303,52 +316,89 @@ __global__ void append_tail_kernel(const AppendParams p) {
 }
 
 // Recompute the key bounding box of every page the append touched, over the
-// page's valid tokens, from the stored keys. grid (page slot, kv head, row),
-// one thread per channel.
-__global__ void append_meta_kernel(const AppendParams p) {
+// page's valid tokens, from the stored keys (INT8 and 4-bit codes restored as
+// fl32(fl32(u * s) + z)). One warp per (page, kv head): grid (page slot, kv
+// head block of 4, row), 128 threads; lane l covers channels [l C, l C + C),
+// C = D / 32, reading its part of each token row in one load (a warp reads a
+// row coalesced), 8 rows per pass with their loads issued together.
+template <int D, int KV>
+__global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) {
+  constexpr int C = D / 32;
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.z, g = blockIdx.y, i = threadIdx.x;
-  const int D = p.head_dim, H = p.num_kv_heads, ps = p.page_size;
+  const int b = blockIdx.z, g = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int H = p.num_kv_heads, ps = p.page_size;
+  if (g >= H) return;
   int pos, n;
   if (!row_window(p, b, pos, n)) return;
   const int lp = pos / ps + blockIdx.x;
   if (lp > (pos + n - 1) / ps) return;
   const int phys = page_of(p, b, lp);
-  if (phys < 0 || i >= D) return;
+  if (phys < 0) return;
   const int nv = min(ps, pos + n - lp * ps);
   const size_t row0 = ((size_t)phys * H + g) * ps;
-  float mn = INFINITY, mx = -INFINITY;
-  // 8 rows per pass, their loads issued together
+  float mn[C], mx[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    mn[c] = INFINITY;
+    mx[c] = -INFINITY;
+  }
   for (int s0 = 0; s0 < nv; s0 += 8) {
-    float x[8];
+    uint64_t raw[8];
+    float2 sc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int s = min(s0 + k, nv - 1);     // a repeated row leaves min/max unchanged
-      if (p.kv_dtype == PKV_I8) {
-        const int code = reinterpret_cast<const int8_t*>(p.k_pages)[(row0 + s) * D + i];
-        const float* sz = p.quant == PKV_QUANT_PER_TOKEN
-                              ? p.kv_sz + (row0 + s) * 4
-                              : p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + s / 64) * 4;
-        x[k] = __fadd_rn(__fmul_rn((float)(code + 128), sz[0]), sz[1]);
-      } else if (p.kv_dtype == PKV_U4) {
-        const uint32_t byte = reinterpret_cast<const uint8_t*>(p.k_pages)[(row0 + s) * (D / 2) + i / 2];
-        const float u = (float)((i & 1) ? byte >> 4 : byte & 0xFu);
-        const float* sz = p.kv_sz + (row0 + s) * 4;
-        x[k] = __fadd_rn(__fmul_rn(u, sz[0]), sz[1]);
+      const int t = min(s0 + k, nv - 1);     // a repeated row leaves min/max unchanged
+      const size_t r = row0 + t;
+      if constexpr (KV == KV_I8T || KV == KV_I8G) {
+        if constexpr (C == 4)
+          raw[k] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * D + lane * 4);
+        else
+          raw[k] = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * D + lane * 2);
+        sc[k] = KV == KV_I8T
+                    ? *reinterpret_cast<const float2*>(p.kv_sz + r * 4)
+                    : *reinterpret_cast<const float2*>(p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + t / 64) * 4);
+      } else if constexpr (KV == KV_U4T) {
+        if constexpr (C == 4)
+          raw[k] = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * (D / 2) + lane * 2);
+        else
+          raw[k] = reinterpret_cast<const uint8_t*>(p.k_pages)[r * (D / 2) + lane];
+        sc[k] = *reinterpret_cast<const float2*>(p.kv_sz + r * 4);
       } else {
-        x[k] = load_src(p.k_pages, p.kv_dtype, (row0 + s) * D + i);
+        if constexpr (C == 4)
+          raw[k] = *reinterpret_cast<const uint64_t*>(reinterpret_cast<const uint16_t*>(p.k_pages) + r * D + lane * 4);
+        else
+          raw[k] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.k_pages) + r * D + lane * 2);
       }
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      mn = fminf(mn, x[k]);
-      mx = fmaxf(mx, x[k]);
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        float x;
+        if constexpr (KV == KV_I8T || KV == KV_I8G) {
+          const int code = (int)(int8_t)((raw[k] >> (8 * c)) & 0xFFu);
+          x = __fadd_rn(__fmul_rn((float)(code + 128), sc[k].x), sc[k].y);
+        } else if constexpr (KV == KV_U4T) {
+          const float u = (float)((raw[k] >> (4 * c)) & 0xFu);
+          x = __fadd_rn(__fmul_rn(u, sc[k].x), sc[k].y);
+        } else {
+          const unsigned short h = (unsigned short)((raw[k] >> (16 * c)) & 0xFFFFu);
+          x = p.kv_dtype == PKV_BF16 ? __uint_as_float((uint32_t)h << 16) : __half2float(__ushort_as_half(h));
+        }
+        mn[c] = fminf(mn[c], x);
+        mx[c] = fmaxf(mx[c], x);
+      }
     }
   }
-  float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D;
-  meta[i] = mn;
-  meta[D + i] = mx;
+  float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D + lane * C;
+  if constexpr (C == 4) {
+    *reinterpret_cast<float4*>(meta) = make_float4(mn[0], mn[1], mn[2], mn[3]);
+    *reinterpret_cast<float4*>(meta + D) = make_float4(mx[0], mx[1], mx[2], mx[3]);
+  } else {
+    *reinterpret_cast<float2*>(meta) = make_float2(mn[0], mn[1]);
+    *reinterpret_cast<float2*>(meta + D) = make_float2(mx[0], mx[1]);
+  }
 }
 
 }  // namespace
@@ -362,20 +412,22 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
     e = launch_pdl(reinterpret_cast<const void*>(&append_copy_kernel), dim3(p.t_new, p.batch), dim3(256), 0,
                    st, args1);
   } else if (p.quant == PKV_QUANT_PER_TOKEN) {
-    const long long warps = (long long)p.batch * ((p.t_new + kTokPerWarp - 1) / kTokPerWarp) * H * 2;
-    const long long blocks = (warps * 32 + 255) / 256;
+    const int warps = min(8, (p.t_new + kTokPerWarp - 1) / kTokPerWarp);
+    const dim3 grid((p.t_new + warps * kTokPerWarp - 1) / (warps * kTokPerWarp), H * 2, p.batch);
     const bool u4 = p.kv_dtype == PKV_U4;
     const void* fn = p.head_dim == 128
                          ? (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<128, true>)
                                : reinterpret_cast<const void*>(&append_per_token_kernel<128, false>))
                          : (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<64, true>)
                                : reinterpret_cast<const void*>(&append_per_token_kernel<64, false>));
-    e = launch_pdl(fn, dim3((unsigned)blocks), dim3(256), 0, st, args1);
+    e = launch_pdl(fn, grid, dim3(32 * warps), 0, st, args1);
   } else {
     const int groups = (p.t_new + 63) / 64 + 1;
     int inline_tail = p.t_new <= 64;
     void* args2[] = {&pc, &inline_tail};
-    e = launch_pdl(reinterpret_cast<const void*>(&append_per_group_kernel), dim3(groups, H * 2, p.batch),
+    const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&append_per_group_kernel<128>)
+                                       : reinterpret_cast<const void*>(&append_per_group_kernel<64>);
+    e = launch_pdl(fn, dim3(groups, H * 2, p.batch),
                    dim3(kGroupThreads), 0, st, args2);
     if (e == cudaSuccess && !inline_tail)
       e = launch_pdl(reinterpret_cast<const void*>(&append_tail_kernel), dim3(H * 2, p.batch), dim3(256), 0,
@@ -383,8 +435,17 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
   }
   if (e == cudaSuccess && p.page_meta) {
     const int pages = (p.t_new + p.page_size - 1) / p.page_size + 1;
-    e = launch_pdl(reinterpret_cast<const void*>(&append_meta_kernel), dim3(pages, H, p.batch),
-                   dim3(p.head_dim), 0, st, args1);
+    const int kind = p.kv_dtype == PKV_U4 ? KV_U4T
+                   : p.kv_dtype == PKV_I8 ? (p.quant == PKV_QUANT_PER_TOKEN ? KV_I8T : KV_I8G)
+                                          : KV_F16;   // fp16 or bf16 (converted by dtype)
+    const void* fn = nullptr;
+#define PKV_META(d, k) \
+    if (p.head_dim == d && kind == k) fn = reinterpret_cast<const void*>(&append_meta_kernel<d, k>);
+    PKV_META(64, KV_F16) PKV_META(64, KV_I8T) PKV_META(64, KV_I8G) PKV_META(64, KV_U4T)
+    PKV_META(128, KV_F16) PKV_META(128, KV_I8T) PKV_META(128, KV_I8G) PKV_META(128, KV_U4T)
+#undef PKV_META
+    if (!fn) return PKV_ERR_UNSUPPORTED;
+    e = launch_pdl(fn, dim3(pages, (H + 3) / 4, p.batch), dim3(128), 0, st, args1);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
