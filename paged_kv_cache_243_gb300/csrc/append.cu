@@ -291,6 +291,103 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(cons
   }
 }
 
+// Bulk per-64-token-group INT8 for groups made of new tokens only: group
+// slots 1, 2, ... of an append longer than one group (slot 0, which may hold
+// earlier members of the open group, and the tail copy go to the kernels
+// above and below). grid (group slot - 1, kv head, row); one block quantises
+// K and V of one group together, holding the source values as 16-bit words
+// (2 registers per 4 values), so it keeps 32 KB of loads in flight; both
+// tensors' min/max meet in one block reduction.
+template <int D>
+__global__ void __launch_bounds__(kGroupThreads, 4) append_group_bulk_kernel(const AppendParams p) {
+  constexpr int NV = 64 * D / 4 / kGroupThreads;   // 4-value elements per thread and tensor
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float red[4][kGroupThreads / 32];
+  __shared__ int phys_s;
+  const int b = blockIdx.z, g = blockIdx.y, H = p.num_kv_heads;
+  int pos, n;
+  if (!row_window(p, b, pos, n)) return;
+  const int gi = pos / 64 + 1 + blockIdx.x;
+  if (gi > (pos + n - 1) / 64) return;
+  const int t0 = gi * 64;   // > pos: every member is a new token
+  const int t_end = min(t0 + 64, pos + n);
+  const int nf = (t_end - t0) * D / 4;
+  const uint16_t* ks = reinterpret_cast<const uint16_t*>(p.k_new);
+  const uint16_t* vs = reinterpret_cast<const uint16_t*>(p.v_new);
+  uint2 kr[NV], vr[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int f = threadIdx.x + k * kGroupThreads;
+    if (f < nf) {
+      const int i = 4 * f, tt = i / D, e = i - tt * D;
+      const size_t idx = (((size_t)b * p.t_new + (t0 + tt - pos)) * H + g) * D + e;
+      kr[k] = *reinterpret_cast<const uint2*>(ks + idx);
+      vr[k] = *reinterpret_cast<const uint2*>(vs + idx);
+    }
+  }
+  if (threadIdx.x == 0) phys_s = page_of(p, b, t0 / p.page_size);
+  float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (threadIdx.x + k * kGroupThreads < nf) {
+      const float4 a = widen4(kr[k], p.src_dtype), c = widen4(vr[k], p.src_dtype);
+      kmn = fminf(fminf(kmn, a.x), fminf(a.y, fminf(a.z, a.w)));
+      kmx = fmaxf(fmaxf(kmx, a.x), fmaxf(a.y, fmaxf(a.z, a.w)));
+      vmn = fminf(fminf(vmn, c.x), fminf(c.y, fminf(c.z, c.w)));
+      vmx = fmaxf(fmaxf(vmx, c.x), fmaxf(c.y, fmaxf(c.z, c.w)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, off));
+    kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, off));
+    vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, off));
+    vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[0][warp] = kmn;
+    red[1][warp] = kmx;
+    red[2][warp] = vmn;
+    red[3][warp] = vmx;
+  }
+  __syncthreads();
+  const int phys = phys_s;
+  if (phys < 0) return;
+  kmn = red[0][0]; kmx = red[1][0]; vmn = red[2][0]; vmx = red[3][0];
+#pragma unroll
+  for (int w = 1; w < kGroupThreads / 32; ++w) {
+    kmn = fminf(kmn, red[0][w]);
+    kmx = fmaxf(kmx, red[1][w]);
+    vmn = fminf(vmn, red[2][w]);
+    vmx = fmaxf(vmx, red[3][w]);
+  }
+  const float sk = __fdiv_rn(__fsub_rn(kmx, kmn), 255.f), sv = __fdiv_rn(__fsub_rn(vmx, vmn), 255.f);
+  const float rk = quant_recip(sk), rv = quant_recip(sv);
+  const int off0 = t0 % p.page_size;
+  const size_t base = (((size_t)phys * H + g) * p.page_size + off0) * D;
+  int8_t* kd = reinterpret_cast<int8_t*>(p.k_pages) + base;
+  int8_t* vd = reinterpret_cast<int8_t*>(p.v_pages) + base;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int f = threadIdx.x + k * kGroupThreads;
+    if (f < nf) {
+      const float4 a = widen4(kr[k], p.src_dtype), c = widen4(vr[k], p.src_dtype);
+      const float xa[4] = {a.x, a.y, a.z, a.w}, xc[4] = {c.x, c.y, c.z, c.w};
+      uint32_t wa[1], wc[1];
+      quant_words<4>(xa, sk, kmn, rk, wa);
+      quant_words<4>(xc, sv, vmn, rv, wc);
+      *reinterpret_cast<uint32_t*>(kd + 4 * f) = wa[0];
+      *reinterpret_cast<uint32_t*>(vd + 4 * f) = wc[0];
+    }
+  }
+  if (threadIdx.x == 0) {
+    float* szp = p.kv_sz + (((size_t)phys * H + g) * (p.page_size / 64) + off0 / 64) * 4;
+    *reinterpret_cast<float4*>(szp) = make_float4(sk, kmn, sv, vmn);
+  }
+}
+
 // Keeps the new members of each row's open group (appends longer than one
 // group, run after the quantise kernel so no block reads a tail row another
 // block rewrites). grid (kv head * 2 + kv, row).
@@ -427,8 +524,16 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
     void* args2[] = {&pc, &inline_tail};
     const void* fn = p.head_dim == 128 ? reinterpret_cast<const void*>(&append_per_group_kernel<128>)
                                        : reinterpret_cast<const void*>(&append_per_group_kernel<64>);
-    e = launch_pdl(fn, dim3(groups, H * 2, p.batch),
+    // appends longer than a group: the first group slot (which may hold
+    // earlier members of the open group) here, the others, all new tokens,
+    // in the bulk kernel; the tail kernel then keeps the open group's members
+    e = launch_pdl(fn, dim3(inline_tail ? groups : 1, H * 2, p.batch),
                    dim3(kGroupThreads), 0, st, args2);
+    if (e == cudaSuccess && !inline_tail) {
+      const void* fb = p.head_dim == 128 ? reinterpret_cast<const void*>(&append_group_bulk_kernel<128>)
+                                         : reinterpret_cast<const void*>(&append_group_bulk_kernel<64>);
+      e = launch_pdl(fb, dim3(groups - 1, H, p.batch), dim3(kGroupThreads), 0, st, args1);
+    }
     if (e == cudaSuccess && !inline_tail)
       e = launch_pdl(reinterpret_cast<const void*>(&append_tail_kernel), dim3(H * 2, p.batch), dim3(256), 0,
                      st, args1);

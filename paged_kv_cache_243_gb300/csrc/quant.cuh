@@ -62,6 +62,17 @@ __device__ __forceinline__ void quant_rint(const float (&x)[N], float s, float z
 // Codes of N values as bytes (code + 128 = u in [0, 255], stored as the int8
 // u - 128, i.e. u ^ 0x80), packed 4 per word: w[k] holds values 4k .. 4k+3.
 // The quotient q lies in [0, 255 (1 + 2^-22)], so rint(q) needs no clamp.
+// Packs quant_rint's results as INT8 codes (byte u ^ 0x80 per value).
+template <int N>
+__device__ __forceinline__ void pack_words(const float (&m)[N], uint32_t (&w)[N / 4]) {
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) {
+    const uint32_t lo = __byte_perm(__float_as_uint(m[4 * k]), __float_as_uint(m[4 * k + 1]), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(m[4 * k + 2]), __float_as_uint(m[4 * k + 3]), 0x0040);
+    w[k] = __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float z, float rs,
                                             uint32_t (&w)[N / 4]) {
@@ -72,12 +83,7 @@ __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float 
   }
   float m[N];
   quant_rint<N>(x, s, z, rs, m);
-#pragma unroll
-  for (int k = 0; k < N / 4; ++k) {
-    const uint32_t lo = __byte_perm(__float_as_uint(m[4 * k]), __float_as_uint(m[4 * k + 1]), 0x0040);
-    const uint32_t hi = __byte_perm(__float_as_uint(m[4 * k + 2]), __float_as_uint(m[4 * k + 3]), 0x0040);
-    w[k] = __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
-  }
+  pack_words<N>(m, w);
 }
 
 // 4-bit codes [per-token 4-bit reading of the KV-practice page, section 3.2]:
@@ -87,16 +93,26 @@ __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float 
 // quotient itself; the bound of quant_words holds a fortiori for quotients of
 // at most 15). N values (N even) -> N / 2 bytes, value 2i in the low
 // nibble of byte i; w[k] holds bytes 4k .. 4k + 3.
+// Packs quant_rint's results as 4-bit codes, value 2i in the low nibble of byte i.
+template <int N>
+__device__ __forceinline__ void pack_nibbles(const float (&m)[N], uint32_t (&w)[(N + 7) / 8]) {
+#pragma unroll
+  for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
+#pragma unroll
+  for (int e = 0; e < N; ++e) w[e / 8] |= (__float_as_uint(m[e]) & 0xFu) << (4 * (e % 8));
+}
+
 template <int N>
 __device__ __forceinline__ void quant_nibbles(const float (&x)[N], float s, float z, float rs,
                                               uint32_t (&w)[(N + 7) / 8]) {
+  if (s == 0.f) {   // constant row: every code 0
 #pragma unroll
-  for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
-  if (s == 0.f) return;   // constant row: every code 0
+    for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
+    return;
+  }
   float m[N];
   quant_rint<N>(x, s, z, rs, m);
-#pragma unroll
-  for (int e = 0; e < N; ++e) w[e / 8] |= (__float_as_uint(m[e]) & 0xFu) << (4 * (e % 8));
+  pack_nibbles<N>(m, w);
 }
 
 // Four 16-bit source values (f16/bf16, as loaded) widened to fp32.
