@@ -188,11 +188,10 @@ const void* attn_kernel(int kind, int D, int ge, bool mma) {
 }
 
 // The tensor-core variant serves dense query-head groups (G >= 2) when q has
-// the dtype of the products' operands: fp16 for fp16 and INT8 caches (codes
-// enter as exact fp16 integers), bf16 for bf16 caches. 4-bit caches always
-// use the CUDA-core consumers.
+// the dtype of the products' operands: fp16 for fp16, INT8 and 4-bit caches
+// (codes enter as exact fp16 integers), bf16 for bf16 caches.
 bool use_mma(int kind, int ge, int q_dtype, const Tuning& tn) {
-  if (ge < 2 || tn.mma == 0 || kind == KV_U4T) return false;
+  if (ge < 2 || tn.mma == 0) return false;
   return kind == KV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16;
 }
 

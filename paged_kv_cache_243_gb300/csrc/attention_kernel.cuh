@@ -332,6 +332,16 @@ __device__ __forceinline__ uint32_t u8x2_to_h2c(uint32_t wflip, uint32_t sel) {
   return r;
 }
 
+// Two 4-bit codes of a word as centred fp16 (u - 8): the nibbles at bit
+// offsets 4s and 4s + 16 (mask 0x000F000F after the shift) placed in the low
+// mantissa bits of fp16 1024 (0x6400), minus 1032, exact.
+__device__ __forceinline__ uint32_t nib2h(uint32_t w, int s) {
+  const uint32_t h = ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -1080,12 +1090,21 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // enter the product's k slots. With swizzled tiles every quarter-warp of a
   // fragment load touches 8 distinct 16-byte blocks: no bank conflicts.
   // INT8 K codes enter q.K^T centred (c = u - 128, exact in fp16).
+  // 4-bit codes (64-byte rows at D = 128, whose 16-byte fragment loads are
+  // already free of conflicts): thread t reads block t of a K row, 32
+  // channels; a register pairs channels c and c + 4 of one word (k slots
+  // 2t, 2t + 1 of a k-step), so a nibble pair becomes fp16 with a shift, a
+  // mask and an or; V tokens 4 jr + t enter k slots (2t, 2t + 1, 2t + 8,
+  // 2t + 9) for jr = 0 .. 3, and a register pairs two tokens' nibbles of one
+  // channel (a byte permute and a mask). Both enter centred (u - 8).
   //
   // Each chunk's P.V goes into a zeroed MMA accumulator, and the running state
   // takes it with one fp32 fma (acc = acc * alpha + chunk): the tensor cores'
   // fp32 accumulation is not IEEE round-to-nearest, and a running sum kept in
   // the MMA accumulator drifts with the number of chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
+  constexpr bool U4 = (KV == KV_U4T);
+  constexpr float KCEN = U4 ? 8.f : 128.f;    // code centre: u - KCEN enters the products
   constexpr int ESZ = Geo::ESZ;
   constexpr int E = 16 / ESZ;                 // channels per 16-byte block
   constexpr int NB = (D / 4) / E;             // 16-byte blocks per thread per row
@@ -1104,7 +1123,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   auto phys_block = [&](int r, int blk) { return SWZ ? (blk ^ (r & 7)) : blk; };
   auto chan = [&](int i) { return kblock(i / E) * E + (i % E); };
   // V rows (tokens) of k slots 2t, 2t + 1, 2t + 8, 2t + 9 of this thread
-  auto vtok = [&](int jr) { return SWZ ? 2 * t + (jr & 1) + 8 * (jr >> 1) : 4 * t + jr; };
+  auto vtok = [&](int jr) {
+    return U4 ? 4 * jr + t : (SWZ ? 2 * t + (jr & 1) + 8 * (jr >> 1) : 4 * t + jr);
+  };
 
   uint32_t qb[KS][2];
   float qs[2];
@@ -1135,7 +1156,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         l2[jj] += __shfl_xor_sync(0xffffffffu, l2[jj], off);
-        if constexpr (KV == KV_I8T || KV == KV_I8G) zs2[jj] += __shfl_xor_sync(0xffffffffu, zs2[jj], off);
+        if constexpr (KV != KV_F16 && KV != KV_BF16) zs2[jj] += __shfl_xor_sync(0xffffffffu, zs2[jj], off);
       }
     }
 #pragma unroll
@@ -1166,11 +1187,21 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         static_cast<const uint16_t*>(q_of(u)) + (g < GE ? g : 0) * D);
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      const int ch = chan(4 * kk);
       uint32_t w0 = 0u, w1 = 0u;
-      if (g < GE) {
-        w0 = qrow[ch / 2];
-        w1 = qrow[ch / 2 + 1];
+      if constexpr (U4) {
+        // k slots (2t, 2t + 1) = channels (c, c + 4), (2t + 8, 2t + 9) = (c + 1, c + 5)
+        const uint16_t* qh = reinterpret_cast<const uint16_t*>(qrow);
+        const int c = t * (D / 4) + 8 * (kk >> 1) + 2 * (kk & 1);
+        if (g < GE) {
+          w0 = (uint32_t)qh[c] | ((uint32_t)qh[c + 4] << 16);
+          w1 = (uint32_t)qh[c + 1] | ((uint32_t)qh[c + 5] << 16);
+        }
+      } else {
+        const int ch = chan(4 * kk);
+        if (g < GE) {
+          w0 = qrow[ch / 2];
+          w1 = qrow[ch / 2 + 1];
+        }
       }
       qb[kk][0] = w0;
       qb[kk][1] = w1;
@@ -1215,7 +1246,34 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       // accumulators: two dependent MMA chains of half the length)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       float sco[4] = {0.f, 0.f, 0.f, 0.f};
-      {
+      if constexpr (U4) {
+        // block t (D / 8 bytes: D / 4 channels) of rows g and g + 8
+        constexpr int NWD = D / 32;   // words per block
+        uint32_t kw0[NWD], kw1[NWD];
+        if constexpr (NWD == 4) {
+          const uint4 a = *reinterpret_cast<const uint4*>(st + g * Geo::ROW + t * 16);
+          const uint4 b = *reinterpret_cast<const uint4*>(st + (g + 8) * Geo::ROW + t * 16);
+          kw0[0] = a.x; kw0[1] = a.y; kw0[2] = a.z; kw0[3] = a.w;
+          kw1[0] = b.x; kw1[1] = b.y; kw1[2] = b.z; kw1[3] = b.w;
+        } else {
+          const uint2 a = *reinterpret_cast<const uint2*>(st + g * Geo::ROW + t * 8);
+          const uint2 b = *reinterpret_cast<const uint2*>(st + (g + 8) * Geo::ROW + t * 8);
+          kw0[0] = a.x; kw0[1] = a.y;
+          kw1[0] = b.x; kw1[1] = b.y;
+        }
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int w = kk >> 1, h = kk & 1;
+          const uint32_t a0 = nib2h(kw0[w], 2 * h), a2 = nib2h(kw0[w], 2 * h + 1);
+          const uint32_t a1 = nib2h(kw1[w], 2 * h), a3 = nib2h(kw1[w], 2 * h + 1);
+          if (kk & 1)
+            mma16816<BF>(sco, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          else
+            mma16816<BF>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] += sco[e];
+      } else {
         uint4 k0[NB], k1[NB];
 #pragma unroll
         for (int m = 0; m < NB; ++m) {
@@ -1250,17 +1308,17 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       }
       // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
       float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
-      if constexpr (KV == KV_I8T) {
+      if constexpr (Geo::PTOK) {
         const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
         const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
-        // centred codes: s (u - 128) + (z + 128 s) = s u + z
-        const float kc0 = fmaf(128.f, z0.x, z0.y), kc1 = fmaf(128.f, z1.x, z1.y);
+        // centred codes: s (u - KCEN) + (z + KCEN s) = s u + z
+        const float kc0 = fmaf(KCEN, z0.x, z0.y), kc1 = fmaf(KCEN, z1.x, z1.y);
         sc[0] = fmaf(z0.x, sc[0], kc0 * qs[0]);
         sc[1] = fmaf(z0.x, sc[1], kc0 * qs[1]);
         sc[2] = fmaf(z1.x, sc[2], kc1 * qs[0]);
         sc[3] = fmaf(z1.x, sc[3], kc1 * qs[1]);
-        // V codes enter P.V centred: vs (u - 128) + (vz + 128 vs) = vs u + vz
-        vs0 = z0.z; vz0 = fmaf(128.f, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(128.f, z1.z, z1.w);
+        // V codes enter P.V centred: vs (u - KCEN) + (vz + KCEN vs) = vs u + vz
+        vs0 = z0.z; vz0 = fmaf(KCEN, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
         const float4 z = *reinterpret_cast<const float4*>(sz);
         const float kc = fmaf(128.f, z.x, z.y);   // centred codes, as for per-token scales
@@ -1290,7 +1348,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         // lane-local running sums (rescaled like the accumulator; the lanes
         // of a head are summed at flush)
         l2[jj] = fmaf(l2[jj], al[jj], p0 + p1);
-        if constexpr (KV == KV_I8T) {
+        if constexpr (Geo::PTOK) {
           const float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
           zs2[jj] = fmaf(zs2[jj], al[jj], pz);
           pw[jj] = ok0 ? p0 * vs0 : 0.f;
@@ -1316,7 +1374,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       const int hb = (PACK && g >= GE) ? g - GE : g;
       const float* pbh = pb + (hb < GE ? hb : 0) * kChunk;
       float2 pv01, pv23;
-      if constexpr (SWZ) {
+      if constexpr (U4) {
+        pv01 = make_float2(pbh[t], pbh[t + 4]);
+        pv23 = make_float2(pbh[t + 8], pbh[t + 12]);
+      } else if constexpr (SWZ) {
         pv01 = *reinterpret_cast<const float2*>(pbh + 2 * t);
         pv23 = *reinterpret_cast<const float2*>(pbh + 2 * t + 8);
       } else {
@@ -1351,7 +1412,38 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         acc[mt][3] = fmaf(acc[mt][3], a1s, d[3]);
       };
       const uint8_t* vrow = st + KB;
-      if constexpr (ESZ == 1) {
+      if constexpr (U4) {
+        // 4-bit: channels [g DPT, (g+1) DPT) = DPT / 2 bytes of tokens vtok(0 .. 3)
+        constexpr int NWV = DPT / 8;   // words per token (2 at D = 128, 1 at 64)
+        uint32_t rw[4][NWV];
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) {
+          const uint8_t* src = vrow + vtok(jr) * Geo::ROW + g * (DPT / 2);
+          if constexpr (NWV == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            rw[jr][0] = v.x;
+            rw[jr][1] = v.y;
+          } else {
+            rw[jr][0] = *reinterpret_cast<const uint32_t*>(src);
+          }
+        }
+        // m-tile mt: byte mt of the thread's bytes; rows g / g + 8 = its low /
+        // high nibble (channels 16 g + 2 mt, + 1); the permute puts the byte
+        // of two tokens at bytes 0 and 2
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int wi = mt >> 2, bsel = mt & 3;
+          const uint32_t sel = (uint32_t)(bsel | (bsel << 4) | ((bsel + 4) << 8) | ((bsel + 4) << 12));
+          const uint32_t t01 = __byte_perm(rw[0][wi], rw[1][wi], sel);
+          const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
+          const uint32_t a0 = nib2h(t01, 0), a1 = nib2h(t01, 1);
+          const uint32_t a2 = nib2h(t23, 0), a3 = nib2h(t23, 1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
+          fold(mt, d);
+        }
+      } else if constexpr (ESZ == 1) {
         // int8: dims [g DPT, (g+1) DPT) of tokens vtok(0 .. 3) (DPT bytes per row)
         uint32_t rw[4][DPT / 4];
 #pragma unroll

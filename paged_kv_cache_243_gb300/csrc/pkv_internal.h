@@ -45,7 +45,7 @@ const void* attn_kernel_f16(int D, int GE, bool mma);
 const void* attn_kernel_bf16(int D, int GE, bool mma);
 const void* attn_kernel_i8t(int D, int GE, bool mma);
 const void* attn_kernel_i8g(int D, int GE, bool mma);
-const void* attn_kernel_u4t(int D, int GE, bool mma);   // no tensor-core variant (nullptr)
+const void* attn_kernel_u4t(int D, int GE, bool mma);
 
 // Bytes of one shared-memory stage (a 16-token chunk of K and V plus its INT8
 // scales), by KV kind and head_dim; swz: the swizzled tensor-copy staging.

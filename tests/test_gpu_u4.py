@@ -9,7 +9,7 @@ import torch
 import oracle
 import synth
 from helpers import (TOL, bits_to_torch, check_per_token_u4_codes, gather, load_workload, max_abs_err,
-                     oracle_dense, oracle_kv, queries_dev)
+                     oracle_dense, oracle_kv, queries_dev, set_knobs)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,9 +21,12 @@ def small_u4(seed, d=128, Hq=8, Hkv=2, ps=16, batch=4, offsets=0.0):
                           page_offset_std=offsets)
 
 
+@pytest.mark.parametrize("mma", ["1", "0"])
 @pytest.mark.parametrize("d,Hq,Hkv,ps", [(128, 8, 2, 16), (64, 4, 4, 16), (64, 16, 2, 32), (128, 32, 8, 64),
-                                          (128, 8, 8, 16)])
-def test_u4_small_all_outputs(d, Hq, Hkv, ps):
+                                          (128, 8, 8, 16), (64, 8, 4, 16)])
+def test_u4_small_all_outputs(monkeypatch, d, Hq, Hkv, ps, mma):
+    # mma = 1: query-head groups use the tensor-core kernel; 0: the CUDA-core one
+    set_knobs(monkeypatch, PKV_ATTN_MMA=mma)
     w = small_u4(800 + d + Hq + ps, d, Hq, Hkv, ps)
     ld = load_workload(w, lens=np.array([1, 400, 17, 250], dtype=np.int32))
     check_per_token_u4_codes(ld)
