@@ -544,6 +544,89 @@ def sweep(peak: float) -> Dict:
             "peak_gbs": peak, "points": res}
 
 
+def prefill_once() -> None:
+    """One bulk kv_append of the whole context, no timing (a short command for
+    profilers): per-token INT8 with page boxes at the sparse GQA INT8
+    workload's shapes, then per-64-token-group INT8 at the long-context ones."""
+    import torch
+    from paged_kv_cache_243_gb300.cache import PagedKVCache
+    for name, meta in (("w6_gqa_sparse_int8", True), ("w4_long_int8_group", False)):
+        w = synth.WORKLOADS[name]
+        B, H, d, T = w.batch, w.num_kv_heads, w.head_dim, int(synth.seq_lens(w).max())
+        kv_name, quant_name = synth.cache_kind(w)
+        bt, pool = synth.block_tables(w, 0, 1 if w.append_steps else 0)
+        cache = PagedKVCache(pool, w.page_size, H, d, kv_dtype=kv_name, quant=quant_name, with_meta=meta,
+                             tail_rows=B)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(w.seed + 7)
+        k = torch.randn((B, T, H, d), generator=gen, device="cuda").half()
+        v = torch.randn((B, T, H, d), generator=gen, device="cuda").half()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cache.append(k, v, torch.from_numpy(bt).cuda(), torch.zeros(B, dtype=torch.int32, device="cuda"),
+                     dev_status=st)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        del cache, k, v
+        torch.cuda.empty_cache()
+
+
+def sparse_breakdown(peak: float) -> List[Dict]:
+    """Where a sparse decode step's time goes: the step (page scoring + top-K +
+    sparse attention) with and without the attention's early start, the scoring
+    alone, the sparse attention alone, and dense attention over all pages, for
+    the fp16 per-head-list and the GQA INT8 group-sum workloads."""
+    import torch
+    global EARLY_START
+    res = []
+    saved = EARLY_START
+    for name, gm in (("w5_sparse_f16", 0), ("w6_gqa_sparse_int8", 1)):
+        w = synth.WORKLOADS[name]
+        P = w.seq_len // w.page_size
+        K = int(math.ceil(w.top_k_ratio * P))
+        rep = Replica(w, w.seed, with_meta=True, top_k=K, group_mode=gm)
+        r = {"workload": name}
+        for early in (False, True):
+            EARLY_START = early
+            g, _ = rep.capture(append=False, attention=True, sparse=True)
+            r[f"step_us_early{int(early)}"] = round(time_graph(g, 50, 5) * 1e3, 2)
+        EARLY_START = saved
+        c = rep.caches[0]
+
+        def score_only():
+            c.score_topk(rep.qs[0], rep.bts[0], rep.len_list[0], K, dev_status=rep.status, sel=rep.sel[0],
+                         count=rep.cnt[0], stream=torch.cuda.current_stream(), group_mode=gm)
+
+        def attention_only():
+            c.attention(rep.qs[0], rep.bts[0], rep.len_list[0], sm_scale=w.sm_scale, sel=rep.sel[0],
+                        sel_count=rep.cnt[0], sel_shared=gm != 0, out=rep.outs[0], dev_status=rep.status,
+                        stream=torch.cuda.current_stream(), fresh_rows=0)
+
+        for label, fn in (("score_us", score_only), ("attention_us", attention_only)):
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                fn()
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(10):
+                    fn()
+            torch.cuda.synchronize()
+            r[label] = round(time_graph(g, 20, 3) / 10 * 1e3, 2)
+        gd, _ = rep.capture(append=False, attention=True, sparse=False)
+        r["dense_us"] = round(time_graph(gd, 50, 5) * 1e3, 2)
+        b = algorithmic_bytes(w, rep.lens, append_tokens=0, sparse_pages=K, group_shared=gm != 0)
+        r["step_frac_early1"] = round(b["total"] / (r["step_us_early1"] * 1e-6) / 1e9 / peak, 4)
+        r["attention_frac"] = round(b["attention"] / (r["attention_us"] * 1e-6) / 1e9 / peak, 4)
+        r["score_frac"] = round(b["score"] / (r["score_us"] * 1e-6) / 1e9 / peak, 4)
+        r["gap_us"] = round(r["step_us_early1"] - r["score_us"] - r["attention_us"], 2)
+        res.append(r)
+        del rep
+        torch.cuda.empty_cache()
+    return res
+
+
 # -------------------------------------------------------------- CPU baseline
 # The oracle (fp64 NumPy, test infrastructure) timed on the host cores, per
 # workload, on bounded samples. A unit is one (layer, sequence, query head):
@@ -910,18 +993,29 @@ def main(argv: Optional[List[str]] = None) -> None:
                     help="the step's append is a separate kv_append launch")
     ap.add_argument("--sweep", action="store_true",
                     help="print attention call times over batch x context instead of the bench line")
+    ap.add_argument("--sparse-breakdown", action="store_true",
+                    help="print where the sparse decode steps' time goes instead of the bench line")
+    ap.add_argument("--prefill-once", action="store_true",
+                    help="run one bulk append of the INT8 GQA shapes, untimed (for profilers)")
     args = ap.parse_args(argv)
     global EARLY_START, FUSED_APPEND
     EARLY_START = not args.no_early_start
     FUSED_APPEND = not args.no_fused_append
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.sweep:
+    if args.sweep or args.sparse_breakdown or args.prefill_once:
         import torch
         from paged_kv_cache_243_gb300 import _build
         _build.build()
         torch.cuda.set_device(0)
-        print(json.dumps(sweep(load_peaks()["hbm_gbs"])), flush=True)
+        if args.sweep:
+            print(json.dumps(sweep(load_peaks()["hbm_gbs"])), flush=True)
+        elif args.sparse_breakdown:
+            for r in sparse_breakdown(load_peaks()["hbm_gbs"]):
+                print(json.dumps(r), flush=True)
+        else:
+            prefill_once()
+            print("ok", flush=True)
         return
     if args.impl == "reference":
         run_reference(args)
