@@ -342,6 +342,13 @@ __device__ __forceinline__ uint32_t nib2h(uint32_t w, int s) {
   return r;
 }
 
+// Two 4-bit codes of a word (nibbles at bit offsets 4s and 4s + 16) as the
+// fp16 pair 16 + u: the nibble goes to mantissa bits 6-9 of fp16 16 (0x4C00).
+__device__ __forceinline__ uint32_t nib16(uint32_t w, int s) {
+  const uint32_t x = s == 0 ? (w << 6) : (s == 1 ? (w << 2) : (s == 2 ? (w >> 2) : (w >> 6)));
+  return (x & 0x03C003C0u) | 0x4C004C00u;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -951,8 +958,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   bool abort = false;
   // S is a multiple of NW (checked by the host), so stage s is only ever read by
   // warp s % NW, which waits on its phases 0, 1, 2, ... in order.
-  for (int n = warp; lo + n < hi; n += NW) {
-    const int s = n % S, use = n / S;
+  // chunk n of the block's range sits in stage n mod S at phase n / S; both
+  // are stepped, not divided (S is a multiple of NW, so s wraps exactly)
+  for (int n = warp, s = warp, use = 0; lo + n < hi; n += NW, s += NW, use += (s >= S), s -= (s >= S) ? S : 0) {
     if (!mbar_wait_bounded(smem_u32(&full[s]), use & 1)) {
       flag_status(p.dev_status, PKV_DEV_TIMEOUT);
       abort = true;
@@ -1001,12 +1009,12 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 8));
       cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 16));
       const float m_new = fmaxf(m_h, cmax);
-      const float alpha = exp2f(m_h - m_new);
+      const float alpha = fast_exp2(m_h - m_new);
       float pw[4];
       float psum = 0.f, pz = 0.f;
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        const float pe = exp2f(sc[it] - m_new);
+        const float pe = fast_exp2(sc[it] - m_new);
         psum += pe;
         if constexpr (Geo::PTOK) {
           const int t = 4 * it + r;
@@ -1089,14 +1097,18 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // 4t .. 4t + 3 (swizzled tiles: 2t, 2t + 1, 2t + 8, 2t + 9) of the chunk
   // enter the product's k slots. With swizzled tiles every quarter-warp of a
   // fragment load touches 8 distinct 16-byte blocks: no bank conflicts.
-  // INT8 K codes enter q.K^T centred (c = u - 128, exact in fp16).
+  // INT8 K codes enter q.K^T centred (c = u - 128, exact in fp16). 4-bit K
+  // codes enter offset, as 16 + u (exact in fp16, one shift and one logic op
+  // per pair, no subtraction); the offset's product (16 x the q sum) leaves
+  // with the zero-point term, and the accumulated magnitude stays within a
+  // few times that of centred codes.
   // 4-bit codes (64-byte rows at D = 128, whose 16-byte fragment loads are
   // already free of conflicts): thread t reads block t of a K row, 32
   // channels; a register pairs channels c and c + 4 of one word (k slots
-  // 2t, 2t + 1 of a k-step), so a nibble pair becomes fp16 with a shift, a
-  // mask and an or; V tokens 4 jr + t enter k slots (2t, 2t + 1, 2t + 8,
-  // 2t + 9) for jr = 0 .. 3, and a register pairs two tokens' nibbles of one
-  // channel (a byte permute and a mask). Both enter centred (u - 8).
+  // 2t, 2t + 1 of a k-step); V tokens 4 jr + t enter k slots (2t, 2t + 1,
+  // 2t + 8, 2t + 9) for jr = 0 .. 3, and a register pairs two tokens' nibbles
+  // of one channel (a byte permute and a mask).
+  // V codes enter P.V centred (u - 128, u - 8); see the P.V step for why.
   //
   // Each chunk's P.V goes into a zeroed MMA accumulator, and the running state
   // takes it with one fp32 fma (acc = acc * alpha + chunk): the tensor cores'
@@ -1104,7 +1116,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // the MMA accumulator drifts with the number of chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
   constexpr bool U4 = (KV == KV_U4T);
-  constexpr float KCEN = U4 ? 8.f : 128.f;    // code centre: u - KCEN enters the products
+  // codes enter q.K^T as u - KCEN_K (4-bit: 16 + u) and P.V as u - KCEN_V
+  // (centred); the scale and zero-point terms take the rest
+  constexpr float KCEN_K = U4 ? -16.f : 128.f;
+  constexpr float KCEN_V = U4 ? 8.f : 128.f;
   constexpr int ESZ = Geo::ESZ;
   constexpr int E = 16 / ESZ;                 // channels per 16-byte block
   constexpr int NB = (D / 4) / E;             // 16-byte blocks per thread per row
@@ -1221,8 +1236,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   };
 
   bool abort = false;
-  for (int n = warp; lo + n < hi; n += NW) {
-    const int s = n % S, use = n / S;
+  // chunk n of the block's range sits in stage n mod S at phase n / S; both
+  // are stepped, not divided (S is a multiple of NW, so s wraps exactly)
+  for (int n = warp, s = warp, use = 0; lo + n < hi; n += NW, s += NW, use += (s >= S), s -= (s >= S) ? S : 0) {
     if (!mbar_wait_bounded(smem_u32(&full[s]), use & 1)) {
       flag_status(p.dev_status, PKV_DEV_TIMEOUT);
       abort = true;
@@ -1264,8 +1280,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           const int w = kk >> 1, h = kk & 1;
-          const uint32_t a0 = nib2h(kw0[w], 2 * h), a2 = nib2h(kw0[w], 2 * h + 1);
-          const uint32_t a1 = nib2h(kw1[w], 2 * h), a3 = nib2h(kw1[w], 2 * h + 1);
+          const uint32_t a0 = nib16(kw0[w], 2 * h), a2 = nib16(kw0[w], 2 * h + 1);
+          const uint32_t a1 = nib16(kw1[w], 2 * h), a3 = nib16(kw1[w], 2 * h + 1);
           if (kk & 1)
             mma16816<BF>(sco, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
           else
@@ -1311,23 +1327,23 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       if constexpr (Geo::PTOK) {
         const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
         const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
-        // centred codes: s (u - KCEN) + (z + KCEN s) = s u + z
-        const float kc0 = fmaf(KCEN, z0.x, z0.y), kc1 = fmaf(KCEN, z1.x, z1.y);
+        // s (u - KCEN_K) + (z + KCEN_K s) = s u + z
+        const float kc0 = fmaf(KCEN_K, z0.x, z0.y), kc1 = fmaf(KCEN_K, z1.x, z1.y);
         sc[0] = fmaf(z0.x, sc[0], kc0 * qs[0]);
         sc[1] = fmaf(z0.x, sc[1], kc0 * qs[1]);
         sc[2] = fmaf(z1.x, sc[2], kc1 * qs[0]);
         sc[3] = fmaf(z1.x, sc[3], kc1 * qs[1]);
-        // V codes enter P.V centred: vs (u - KCEN) + (vz + KCEN vs) = vs u + vz
-        vs0 = z0.z; vz0 = fmaf(KCEN, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN, z1.z, z1.w);
+        // V codes enter P.V centred: vs (u - KCEN_V) + (vz + KCEN_V vs) = vs u + vz
+        vs0 = z0.z; vz0 = fmaf(KCEN_V, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN_V, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
         const float4 z = *reinterpret_cast<const float4*>(sz);
-        const float kc = fmaf(128.f, z.x, z.y);   // centred codes, as for per-token scales
+        const float kc = fmaf(KCEN_K, z.x, z.y);   // centred codes, as for per-token scales
         sc[0] = fmaf(z.x, sc[0], kc * qs[0]);
         sc[1] = fmaf(z.x, sc[1], kc * qs[1]);
         sc[2] = fmaf(z.x, sc[2], kc * qs[0]);
         sc[3] = fmaf(z.x, sc[3], kc * qs[1]);
         vs0 = vs1 = z.z;
-        vz0 = vz1 = fmaf(128.f, z.z, z.w);   // centred codes, as for per-token scales
+        vz0 = vz1 = fmaf(KCEN_V, z.z, z.w);   // centred codes, as for per-token scales
       }
       const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
 #pragma unroll
@@ -1343,8 +1359,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
         cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
         const float mn = fmaxf(m2[jj], cm);
-        al[jj] = exp2f(m2[jj] - mn);
-        const float p0 = exp2f(sc[jj] - mn), p1 = exp2f(sc[2 + jj] - mn);
+        al[jj] = fast_exp2(m2[jj] - mn);
+        const float p0 = fast_exp2(sc[jj] - mn), p1 = fast_exp2(sc[2 + jj] - mn);
         // lane-local running sums (rescaled like the accumulator; the lanes
         // of a head are summed at flush)
         l2[jj] = fmaf(l2[jj], al[jj], p0 + p1);

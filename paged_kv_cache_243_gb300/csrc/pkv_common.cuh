@@ -238,6 +238,15 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
+// error about 2^-22, results below 2^-126 flushed to zero, 2^-inf = 0). The
+// online softmax only takes it of differences x <= 0 from a running maximum.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
