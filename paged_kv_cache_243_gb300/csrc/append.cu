@@ -414,13 +414,22 @@ __global__ void append_tail_kernel(const AppendParams p) {
 
 // Recompute the key bounding box of every page the append touched, over the
 // page's valid tokens, from the stored keys (INT8 and 4-bit codes restored as
-// fl32(fl32(u * s) + z)). One warp per (page, kv head): grid (page slot, kv
-// head block of 4, row), 128 threads; lane l covers channels [l C, l C + C),
-// C = D / 32, reading its part of each token row in one load (a warp reads a
-// row coalesced), 8 rows per pass with their loads issued together.
+// fl32(fl32(u * s) + z): a packed multiply, then the scalar __fadd_rn, which is
+// never fused with it; ptxas may contract a packed mul.rn.f32x2 / add.rn.f32x2
+// pair into one fma, a different rounding). One warp per (page, kv head):
+// grid (page slot, kv head block of 4, row), 128 threads. Lane l covers
+// channel block l mod 16 (D / 16 channels) of rows l / 16, l / 16 + 2, ...:
+// a warp reads two whole rows per load instruction, with sixteen rows' loads
+// in flight per pass, folds each channel over its eight rows in min/max
+// chains, and merges the two row halves with one shuffle at the end.
 template <int D, int KV>
 __global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) {
-  constexpr int C = D / 32;
+  constexpr int C = D / 16;   // channels per lane
+  constexpr bool I8 = KV == KV_I8T || KV == KV_I8G;
+  constexpr int RB = KV == KV_U4T ? C / 2 : (I8 ? C : 2 * C);   // bytes per lane per row
+  constexpr int RW = RB >= 4 ? RB / 4 : 1;                      // 32-bit words per lane per row
+  constexpr int ROWB = KV == KV_U4T ? D / 2 : (I8 ? D : 2 * D); // bytes per row
+  constexpr int RPL = 8;                                        // rows per lane per pass
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.z, g = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -434,67 +443,98 @@ __global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) 
   if (phys < 0) return;
   const int nv = min(ps, pos + n - lp * ps);
   const size_t row0 = ((size_t)phys * H + g) * ps;
+  const int part = lane & 15, ro = lane >> 4;
+  const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k_pages) + row0 * ROWB + part * RB;
   float mn[C], mx[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     mn[c] = INFINITY;
     mx[c] = -INFINITY;
   }
-  for (int s0 = 0; s0 < nv; s0 += 8) {
-    uint64_t raw[8];
-    float2 sc[8];
+  for (int r0 = 0; r0 < nv; r0 += 2 * RPL) {
+    uint32_t w[RPL][RW];
+    float2 sc[RPL];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int t = min(s0 + k, nv - 1);     // a repeated row leaves min/max unchanged
-      const size_t r = row0 + t;
-      if constexpr (KV == KV_I8T || KV == KV_I8G) {
-        if constexpr (C == 4)
-          raw[k] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * D + lane * 4);
-        else
-          raw[k] = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * D + lane * 2);
-        sc[k] = KV == KV_I8T
-                    ? *reinterpret_cast<const float2*>(p.kv_sz + r * 4)
-                    : *reinterpret_cast<const float2*>(p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + t / 64) * 4);
-      } else if constexpr (KV == KV_U4T) {
-        if constexpr (C == 4)
-          raw[k] = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.k_pages) + r * (D / 2) + lane * 2);
-        else
-          raw[k] = reinterpret_cast<const uint8_t*>(p.k_pages)[r * (D / 2) + lane];
-        sc[k] = *reinterpret_cast<const float2*>(p.kv_sz + r * 4);
+    for (int i = 0; i < RPL; ++i) {
+      const int t = min(r0 + ro + 2 * i, nv - 1);   // a repeated row leaves the bounds unchanged
+      const uint8_t* src = kb + (size_t)t * ROWB;
+      if constexpr (RB == 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+      } else if constexpr (RB == 8) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        w[i][0] = v.x; w[i][1] = v.y;
+      } else if constexpr (RB == 4) {
+        w[i][0] = *reinterpret_cast<const uint32_t*>(src);
       } else {
-        if constexpr (C == 4)
-          raw[k] = *reinterpret_cast<const uint64_t*>(reinterpret_cast<const uint16_t*>(p.k_pages) + r * D + lane * 4);
-        else
-          raw[k] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(p.k_pages) + r * D + lane * 2);
+        w[i][0] = *reinterpret_cast<const uint16_t*>(src);
       }
+      if constexpr (KV == KV_I8T || KV == KV_U4T)
+        sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (row0 + t) * 4);
+      else if constexpr (KV == KV_I8G)
+        sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + t / 64) * 4);
+      else
+        sc[i] = make_float2(0.f, 0.f);
     }
+    // channels (c, c + 1) of every row i: values (a[i], b[i]), then the chains
+    auto fold = [&](int c, const float (&a)[RPL], const float (&bb)[RPL]) {
+      float l0 = mn[c], h0 = mx[c], l1 = mn[c + 1], h1 = mx[c + 1];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+      for (int i = 0; i < RPL; i += 2) {
+        l0 = fminf(fminf(l0, a[i]), a[i + 1]);
+        h0 = fmaxf(fmaxf(h0, a[i]), a[i + 1]);
+        l1 = fminf(fminf(l1, bb[i]), bb[i + 1]);
+        h1 = fmaxf(fmaxf(h1, bb[i]), bb[i + 1]);
+      }
+      mn[c] = l0; mx[c] = h0; mn[c + 1] = l1; mx[c + 1] = h1;
+    };
+    auto deq = [&](int i, uint64_t u2, float& a, float& bv) {   // fl32(fl32(u s) + z)
+      float p0, p1;
+      unpack2f(fmul2(u2, pack2f(sc[i].x, sc[i].x)), p0, p1);
+      a = __fadd_rn(p0, sc[i].y);
+      bv = __fadd_rn(p1, sc[i].y);
+    };
 #pragma unroll
-      for (int c = 0; c < C; ++c) {
-        float x;
-        if constexpr (KV == KV_I8T || KV == KV_I8G) {
-          const int code = (int)(int8_t)((raw[k] >> (8 * c)) & 0xFFu);
-          x = __fadd_rn(__fmul_rn((float)(code + 128), sc[k].x), sc[k].y);
-        } else if constexpr (KV == KV_U4T) {
-          const float u = (float)((raw[k] >> (4 * c)) & 0xFu);
-          x = __fadd_rn(__fmul_rn(u, sc[k].x), sc[k].y);
-        } else {
-          const unsigned short h = (unsigned short)((raw[k] >> (16 * c)) & 0xFFFFu);
-          x = p.kv_dtype == PKV_BF16 ? __uint_as_float((uint32_t)h << 16) : __half2float(__ushort_as_half(h));
+    for (int q = 0; q < RW; ++q) {
+      if constexpr (I8) {   // word q: channels 4q .. 4q + 3 of the lane's block
+#pragma unroll
+        for (int jp = 0; jp < 4 && 4 * q + jp < C; jp += 2) {
+          float a[RPL], bv[RPL];
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) deq(i, u8pair(w[i][q] ^ 0x80808080u, jp), a[i], bv[i]);
+          fold(4 * q + jp, a, bv);
         }
-        mn[c] = fminf(mn[c], x);
-        mx[c] = fmaxf(mx[c], x);
+      } else if constexpr (KV == KV_U4T) {   // word q: channels 8q .. 8q + 7
+#pragma unroll
+        for (int j = 0; j < 4 && 8 * q + 2 * j < C; ++j) {
+          float a[RPL], bv[RPL];
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) {
+            uint32_t lo, hi;
+            split_nibbles(w[i][q], lo, hi);
+            deq(i, u4pair(lo, hi, j), a[i], bv[i]);
+          }
+          fold(8 * q + 2 * j, a, bv);
+        }
+      } else {   // word q: channels 2q, 2q + 1
+        float a[RPL], bv[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) unpack2<KV>(w[i][q], a[i], bv[i]);
+        fold(2 * q, a, bv);
       }
     }
   }
-  float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D + lane * C;
-  if constexpr (C == 4) {
-    *reinterpret_cast<float4*>(meta) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-    *reinterpret_cast<float4*>(meta + D) = make_float4(mx[0], mx[1], mx[2], mx[3]);
-  } else {
-    *reinterpret_cast<float2*>(meta) = make_float2(mn[0], mn[1]);
-    *reinterpret_cast<float2*>(meta + D) = make_float2(mx[0], mx[1]);
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    mn[c] = fminf(mn[c], __shfl_xor_sync(0xffffffffu, mn[c], 16));
+    mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+  }
+  if (ro != 0) return;
+  float* meta = p.page_meta + (((size_t)phys * H + g) * 2) * D + part * C;
+#pragma unroll
+  for (int c = 0; c < C; c += 4) {
+    *reinterpret_cast<float4*>(meta + c) = make_float4(mn[c], mn[c + 1], mn[c + 2], mn[c + 3]);
+    *reinterpret_cast<float4*>(meta + D + c) = make_float4(mx[c], mx[c + 1], mx[c + 2], mx[c + 3]);
   }
 }
 
@@ -542,12 +582,13 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
     const int pages = (p.t_new + p.page_size - 1) / p.page_size + 1;
     const int kind = p.kv_dtype == PKV_U4 ? KV_U4T
                    : p.kv_dtype == PKV_I8 ? (p.quant == PKV_QUANT_PER_TOKEN ? KV_I8T : KV_I8G)
-                                          : KV_F16;   // fp16 or bf16 (converted by dtype)
+                   : p.kv_dtype == PKV_BF16 ? KV_BF16 : KV_F16;
     const void* fn = nullptr;
 #define PKV_META(d, k) \
     if (p.head_dim == d && kind == k) fn = reinterpret_cast<const void*>(&append_meta_kernel<d, k>);
-    PKV_META(64, KV_F16) PKV_META(64, KV_I8T) PKV_META(64, KV_I8G) PKV_META(64, KV_U4T)
-    PKV_META(128, KV_F16) PKV_META(128, KV_I8T) PKV_META(128, KV_I8G) PKV_META(128, KV_U4T)
+    PKV_META(64, KV_F16) PKV_META(64, KV_BF16) PKV_META(64, KV_I8T) PKV_META(64, KV_I8G) PKV_META(64, KV_U4T)
+    PKV_META(128, KV_F16) PKV_META(128, KV_BF16) PKV_META(128, KV_I8T) PKV_META(128, KV_I8G)
+    PKV_META(128, KV_U4T)
 #undef PKV_META
     if (!fn) return PKV_ERR_UNSUPPORTED;
     e = launch_pdl(fn, dim3(pages, (H + 3) / 4, p.batch), dim3(128), 0, st, args1);

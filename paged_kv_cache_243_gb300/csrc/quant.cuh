@@ -30,8 +30,11 @@ constexpr float kNearHalf = 0.4999f;         // |p - rint(p)| above this: within
 
 // Shared step of both quantisers: for N values (N even), m[e] = rint(q_e) +
 // 1.5 * 2^23 with q_e = fl(fl(x_e - z) / s), the integer in m's low mantissa
-// bits. Two values per packed fp32x2 instruction (each lane correctly
-// rounded, so the results equal the scalar sequence).
+// bits. Two values per packed fp32x2 instruction. ptxas may contract the
+// packed multiply and the magic add into one fma (it never fuses the scalar
+// __fmul_rn / __fadd_rn); m then holds the rounding of the exact product
+// (x - z) rs, within 255 * 2^-24 of q, and the near-half test covers that
+// case by the same bound.
 template <int N>
 __device__ __forceinline__ void quant_rint(const float (&x)[N], float s, float z, float rs, float (&m)[N]) {
   const uint64_t z2 = pack2f(z, z), rs2 = pack2f(rs, rs), mg2 = pack2f(kRoundMagic, kRoundMagic);
