@@ -40,6 +40,8 @@ struct Tuning {
   int stages = 0;         // PKV_ATTN_STAGES: explicit stage count (rounded to a multiple of 4)
   int ctas_per_sm = 0;    // PKV_ATTN_CTAS_PER_SM: cap on resident blocks per SM
   int comb_rg = 0;        // PKV_ATTN_COMB_RG: record groups of the combine (1, 2, 4 or 8)
+  int mma_g1 = 0;         // PKV_ATTN_MMA_G1: tensor-core consumers for single query heads on
+                          // fp16/bf16 caches: 0 never, 1 at head_dim 64, 2 at every head_dim
 };
 
 std::mutex g_tuning_mu;
@@ -53,6 +55,7 @@ void read_tuning_locked() {
   t.stages = env_int("PKV_ATTN_STAGES", 0);
   t.ctas_per_sm = env_int("PKV_ATTN_CTAS_PER_SM", 0);
   t.comb_rg = env_int("PKV_ATTN_COMB_RG", 0);
+  t.mma_g1 = env_int("PKV_ATTN_MMA_G1", 0);
   g_tuning = t;
   g_tuning_read = true;
 }
@@ -187,11 +190,19 @@ const void* attn_kernel(int kind, int D, int ge, bool mma) {
   }
 }
 
-// The tensor-core variant serves dense query-head groups (G >= 2) when q has
-// the dtype of the products' operands: fp16 for fp16, INT8 and 4-bit caches
-// (codes enter as exact fp16 integers), bf16 for bf16 caches.
-bool use_mma(int kind, int ge, int q_dtype, const Tuning& tn) {
-  if (ge < 2 || tn.mma == 0) return false;
+// The tensor-core variant serves query-head groups (G >= 2) when q has the
+// dtype of the products' operands: fp16 for fp16, INT8 and 4-bit caches
+// (codes enter as exact fp16 integers), bf16 for bf16 caches. Single query
+// heads (MHA, or per-head page lists) on fp16/bf16 caches, whose rows enter
+// the products as stored, may take it too (PKV_ATTN_MMA_G1); by default they
+// stay on the CUDA-core consumer, which measured faster for them (MHA at
+// head_dim 64: 91 against 94 us; at 128: 22.4 against 28.5 us per call).
+bool use_mma(int kind, int ge, int D, int q_dtype, const Tuning& tn) {
+  if (tn.mma == 0) return false;
+  if (ge < 2) {
+    if (kind != KV_F16 && kind != KV_BF16) return false;
+    if (tn.mma_g1 == 0 || (tn.mma_g1 == 1 && D != 64)) return false;
+  }
   return kind == KV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16;
 }
 
@@ -272,7 +283,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
   pl.units = batch * (sparse == 1 ? num_q_heads : c->num_kv_heads);
   const int kind = kv_kind(c);
   const Tuning tn = tuning();
-  pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, q_dtype, tn);
+  pl.mma = q_dtype >= 0 && use_mma(kind, pl.ge, c->head_dim, q_dtype, tn);
   pl.fn = attn_kernel(kind, c->head_dim, pl.ge, pl.mma);
   if (!pl.fn) return PKV_ERR_UNSUPPORTED;
   DeviceInfo di;
@@ -325,7 +336,10 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     int nb = 0;
     st = blocks_per_sm(pl.fn, pl.mma, nb);
     if (st != PKV_OK) return st;
-    if (q_dtype < 0 && pl.ge >= 2) {   // the tensor-core variant may fit more blocks
+    // sizing for any q dtype: the tensor-core variant, where a call may use
+    // it, may fit more blocks
+    const int mma_q = kind == KV_BF16 ? PKV_BF16 : PKV_F16;
+    if (q_dtype < 0 && (pl.ge >= 2 || use_mma(kind, pl.ge, c->head_dim, mma_q, tn))) {
       int nb2 = 0;
       const void* f2 = attn_kernel(kind, c->head_dim, pl.ge, true);
       if (f2 && blocks_per_sm(f2, true, nb2) == PKV_OK && nb2 > nb) nb = nb2;

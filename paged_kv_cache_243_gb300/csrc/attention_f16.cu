@@ -1,6 +1,6 @@
 // Instantiations of the paged attention kernel for one KV storage kind:
 // head_dim 64/128 x query heads per unit 1/2/4/8, CUDA-core path, and the
-// tensor-core path for query-head groups of 2/4/8.
+// tensor-core path (for these 16-bit caches also for single query heads).
 #include "attention_kernel.cuh"
 #include "pkv_internal.h"
 
@@ -12,8 +12,8 @@ const void* attn_kernel_f16(int D, int GE, bool mma) {
     return reinterpret_cast<const void*>(&paged_attention_kernel<d, ge, KV_F16, tc>);
   PKV_CASE(64, 1, false) PKV_CASE(64, 2, false) PKV_CASE(64, 4, false) PKV_CASE(64, 8, false)
   PKV_CASE(128, 1, false) PKV_CASE(128, 2, false) PKV_CASE(128, 4, false) PKV_CASE(128, 8, false)
-  PKV_CASE(64, 2, true) PKV_CASE(64, 4, true) PKV_CASE(64, 8, true)
-  PKV_CASE(128, 2, true) PKV_CASE(128, 4, true) PKV_CASE(128, 8, true)
+  PKV_CASE(64, 1, true) PKV_CASE(64, 2, true) PKV_CASE(64, 4, true) PKV_CASE(64, 8, true)
+  PKV_CASE(128, 1, true) PKV_CASE(128, 2, true) PKV_CASE(128, 4, true) PKV_CASE(128, 8, true)
 #undef PKV_CASE
   return nullptr;
 }

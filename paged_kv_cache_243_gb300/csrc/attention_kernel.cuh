@@ -1158,7 +1158,13 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
     }
   };
   auto flush_to = [&](float* rec) {   // global or shared memory
-    if constexpr (PACK) {   // lo columns (threads t + G/2) into the hi ones
+    if constexpr (GE == 1) {   // the lo column 1 sits beside the hi column 0
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][0] += acc[mt][1];
+        acc[mt][2] += acc[mt][3];
+      }
+    } else if constexpr (PACK) {   // lo columns (threads t + G/2) into the hi ones
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -1416,7 +1422,9 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       // ---- P.V on the tensor cores, into a zeroed accumulator per m-tile;
       // the running state takes it as acc = acc * alpha + chunk (fp32 fma)
       float a0s = al[0], a1s = al[1];
-      if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
+      if constexpr (GE == 1) {   // columns 0 and 1: hi and lo parts of head 0
+        a1s = al[0];
+      } else if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
         const int src = t >= GE / 2 ? lane - GE / 2 : lane;
         a0s = __shfl_sync(0xffffffffu, al[0], src);
         a1s = __shfl_sync(0xffffffffu, al[1], src);

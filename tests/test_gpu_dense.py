@@ -225,3 +225,25 @@ def test_dense_32k_bf16_all_outputs():
         t = L - 1
         assert np.array_equal(kp[ld.bt[b][t // w.page_size], :, t % w.page_size], kb[b])
     assert int(ld.status.item()) == 0
+
+
+@pytest.mark.parametrize("g1", ["0", "2"])
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16"), (64, "bf16"), (128, "f16")])
+def test_single_query_heads_on_tensor_cores(monkeypatch, g1, d, dt):
+    # one query head per kv head: the tensor-core consumer (PKV_ATTN_MMA_G1=2,
+    # every head_dim) against the CUDA-core one (0) and the oracle, ragged
+    # lengths, an empty sequence and split counts from one block per unit to
+    # more blocks than chunks
+    set_knobs(monkeypatch, PKV_ATTN_MMA_G1=g1)
+    w = synth.Workload(name="t", seed=501 + d, batch=5, layers=1, num_q_heads=6, num_kv_heads=6,
+                       head_dim=d, page_size=16, dtype=dt, quant="none", seq_len=None,
+                       seq_len_range=(1, 700))
+    lens = np.array([700, 1, 0, 333, 64], dtype=np.int32)
+    ld = load_workload(w, lens=lens)
+    q, qf = queries_dev(w)
+    ref = oracle_dense(ld, qf)
+    for splits in (0, 1, 3, 1000):
+        out = run_attention(ld, q, num_splits=splits).cpu().numpy()
+        assert max_abs_err(out, ref) <= TOL[dt], splits
+        assert (out[2] == 0).all()
+    assert int(ld.status.item()) == 0

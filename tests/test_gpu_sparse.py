@@ -320,3 +320,21 @@ def test_tied_page_scores_keep_the_lowest_pages(d, Hkv, patterns):
         r = oracle.page_scores(qf[h:h + 1], mn, mx, 1)[0]
         assert cnt[0, h] == top_k
         assert np.array_equal(sel[0, h], oracle.select_top_k(r, top_k)), h
+
+
+@pytest.mark.parametrize("g1", ["0", "2"])
+def test_per_head_lists_on_tensor_cores(monkeypatch, g1):
+    # per-query-head page lists (units of one query head) on both consumers
+    from helpers import set_knobs
+    set_knobs(monkeypatch, PKV_ATTN_MMA_G1=g1)
+    w = synth.Workload(name="sph", seed=611, batch=3, layers=1, num_q_heads=8, num_kv_heads=2,
+                       head_dim=128, page_size=16, dtype="bf16", quant="none", seq_len=None,
+                       seq_len_range=(1, 500))
+    ld = load_workload(w, lens=np.array([500, 33, 260], dtype=np.int32), with_meta=True)
+    q, qf = queries_dev(w)
+    sel, cnt, scores, out = run_sparse(ld, q, 5)
+    chosen = check_selection(ld, qf, 5, sel, cnt, scores)
+    res = oracle_sparse(ld, qf, chosen, list(chosen))
+    for (b, h), o in res.items():
+        assert np.abs(out[b, h] - o).max() <= TOL["bf16"], (b, h)
+    assert int(ld.status.item()) == 0
