@@ -1562,17 +1562,20 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
 // the unit is the block's last and its four warps were merged in the block,
 // and four (one per warp, some empty) from a block that moves on past it:
 //   M = max m_r,  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r
-// (the log2-domain partial states of the attention kernel). The 256 threads
-// of block (u, y) form RG = comb_groups record groups of OB = 256 / RG
+// (the log2-domain partial states of the attention kernel). The 128 threads
+// of block (u, y) form RG = comb_groups record groups of OB = 128 / RG
 // threads; thread (g, i) folds records g, g + RG, ... of output y OB + i of
 // unit u, and group 0 merges the RG partials. The host picks RG from the
 // expected records per unit (more groups when units span many blocks).
 // Dense calls compute the unit's chunk range from the sequence lengths before
 // waiting for the attention kernel (the lengths are inputs, not its output),
 // so only the record loads follow the wait.
-constexpr int kCombineThreads = 256;
+// 128 threads: more of these blocks are resident beside the attention blocks
+// than of 256-thread ones (W2 22.5 -> 22.2 us per call in a chain, W4 31.8 ->
+// 31.2 us), so the next call's kernel is released sooner.
+constexpr int kCombineThreads = 128;
 template <int D, int GE>
-__global__ void __launch_bounds__(kCombineThreads, 2) attn_combine_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 4) attn_combine_kernel(const AttnParams p) {
   constexpr int RS = rec_floats(GE, D), HDR = rec_hdr(GE);
   constexpr int BATCH = 8;    // records in flight per thread
   constexpr int NWC = kCombineThreads / 32;
