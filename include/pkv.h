@@ -290,9 +290,15 @@ pkv_status pkv_paged_decode_attention(const pkv_cache* cache, int32_t batch, int
  *   Other arguments as pkv_paged_decode_attention in dense mode; with
  *   fresh_rows >= 0 the work before the call must also leave the new rows
  *   alone (the kernel writes them before it waits for that work).
- * Caches: fp16/bf16, per-token INT8 and 4-bit without page metadata; per-group INT8
- * (which re-quantises the whole open group) and caches with page boxes return
- * PKV_ERR_UNSUPPORTED (use pkv_kv_append and pkv_paged_decode_attention).
+ * Caches: fp16/bf16, per-token INT8 and 4-bit without page metadata take the
+ * single launch above. Per-group INT8 caches (the append re-quantises the whole
+ * open group of up to 64 rows, which the attention's streaming does not hold)
+ * and caches with page boxes take two launches: the kv_append of the new token,
+ * which waits for all earlier work, then the attention, which starts under it
+ * (as with fresh_rows = 1 after that append); the caller's fresh_rows is then
+ * not needed, and the results equal those of pkv_kv_append followed by
+ * pkv_paged_decode_attention. For those caches the arguments of both calls are
+ * checked before either is launched.
  * Sequences with seq_lens[b] = 0 get no token.
  */
 pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,

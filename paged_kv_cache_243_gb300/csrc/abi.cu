@@ -551,11 +551,65 @@ pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, in
                                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
   pkv_status st = check_cache(cache, true);
   if (st != PKV_OK) return st;
-  if (cache->quant == PKV_QUANT_PER_GROUP64 || cache->page_meta) return PKV_ERR_UNSUPPORTED;
   if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
+  if (cache->quant == PKV_QUANT_PER_GROUP64 || cache->page_meta) {
+    // Two launches: the kv_append of each sequence's token at seq_lens[b] - 1
+    // (per-group INT8 re-quantises the open group; page boxes are refreshed),
+    // then the attention, which starts under the append: that kernel writes
+    // only the new rows (and their open group and boxes), and it waits for
+    // all earlier work before it touches anything.
+    if (batch < 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!block_table || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (cache->quant == PKV_QUANT_PER_GROUP64 &&
+        (!cache->tail || !aligned16(cache->tail) || cache->tail_rows < batch))
+      return PKV_ERR_INVALID_ARG;
+    if (batch > 65535 || cache->num_kv_heads > 32767) return PKV_ERR_UNSUPPORTED;
+    // the attention call's own argument checks and plan come first, so that a
+    // call refused for them changes nothing
+    AttnPlan pl;
+    const long long max_chunks = (long long)batch * cache->num_kv_heads *
+                                 (((long long)max_pages * cache->page_size + kChunk - 1) / kChunk);
+    st = plan_attention(cache, batch, num_q_heads, 0, num_splits, q_dtype, pl, max_chunks);
+    if (st != PKV_OK) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < pl.ws_bytes)
+      return PKV_ERR_WORKSPACE;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_F16 && q_dtype != PKV_BF16 && q_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32) return PKV_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || !(sm_scale < 1e30f) || fresh_rows < -1) return PKV_ERR_INVALID_ARG;
+    AppendParams ap = {};
+    ap.k_pages = cache->k_pages;
+    ap.v_pages = cache->v_pages;
+    ap.kv_sz = cache->kv_sz;
+    ap.tail = cache->tail;
+    ap.page_meta = cache->page_meta;
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.block_table = block_table;
+    ap.positions = seq_lens;
+    ap.pos_bias = -1;
+    ap.new_lens = nullptr;
+    ap.dev_status = dev_status;
+    ap.num_pages = cache->num_pages;
+    ap.page_size = cache->page_size;
+    ap.num_kv_heads = cache->num_kv_heads;
+    ap.head_dim = cache->head_dim;
+    ap.kv_dtype = cache->kv_dtype;
+    ap.quant = cache->quant;
+    ap.src_dtype = src_dtype;
+    ap.batch = batch;
+    ap.t_new = 1;
+    ap.max_pages = max_pages;
+    st = launch_append(ap, static_cast<cudaStream_t>(stream));
+    if (st != PKV_OK) return st;
+    return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
+                          nullptr, nullptr, 0, 0, out, out_dtype, num_splits, 1, nullptr, nullptr, PKV_F16,
+                          workspace, workspace_bytes, dev_status, stream);
+  }
   if ((cache->kv_dtype == PKV_F16 || cache->kv_dtype == PKV_BF16) && src_dtype != cache->kv_dtype)
     return PKV_ERR_UNSUPPORTED;
-  if (batch > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
                         nullptr, nullptr, 0, 0, out, out_dtype, num_splits, fresh_rows, k_new, v_new,
                         src_dtype, workspace, workspace_bytes, dev_status, stream);
@@ -577,7 +631,7 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
     return PKV_ERR_INVALID_ARG;
   if ((long long)t_new > (long long)max_pages * cache->page_size) return PKV_ERR_INVALID_ARG;
   if (batch > 65535 || cache->num_kv_heads > 32767) return PKV_ERR_UNSUPPORTED;   // grid y / z limits
-  AppendParams p;
+  AppendParams p = {};
   p.k_pages = cache->k_pages;
   p.v_pages = cache->v_pages;
   p.kv_sz = cache->kv_sz;
@@ -599,6 +653,7 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
   p.batch = batch;
   p.t_new = t_new;
   p.max_pages = max_pages;
+  p.pos_bias = 0;
   return launch_append(p, static_cast<cudaStream_t>(stream));
 }
 

@@ -24,7 +24,7 @@ __device__ __forceinline__ float load_src(const void* p, int dtype, size_t i) {
 }
 
 __device__ __forceinline__ bool row_window(const AppendParams& p, int b, int& pos, int& n) {
-  pos = p.positions[b];
+  pos = p.positions[b] + p.pos_bias;
   n = p.new_lens ? p.new_lens[b] : p.t_new;
   if (n > p.t_new || n < 0 || pos < 0 || (long long)pos + n > (long long)p.max_pages * p.page_size) {
     flag_status(p.dev_status, PKV_DEV_BAD_POSITION);

@@ -20,6 +20,7 @@ struct AppendParams {
   int num_pages, page_size, num_kv_heads, head_dim;
   int kv_dtype, quant, src_dtype;
   int batch, t_new, max_pages;
+  int pos_bias;   // added to positions[b] (-1: positions are the lengths after the append)
 };
 
 struct TopkParams {

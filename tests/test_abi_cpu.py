@@ -92,12 +92,12 @@ def test_argument_checks_before_cuda(B):
         B.page_score_topk(with_meta, 1, 2, 0x4000, B.F16, 0x5000, 4, 0x6000, 2, 0x9000, 0xA000, 0, 0, 0,
                           group_mode=3)
     assert e.value.status == B.ERR_INVALID_ARG
-    for desc, src, want in ((_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000, tail=0x3100,
-                                   tail_rows=1, page_size=64), B.F16, B.ERR_UNSUPPORTED),
-                            (_desc(B, page_meta=0xB000), B.F16, B.ERR_UNSUPPORTED),
+    for desc, src, want in ((_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000,
+                                   page_size=64), B.F16, B.ERR_INVALID_ARG),   # per-group without a tail
+                            (_desc(B, page_meta=0xB000), B.I8, B.ERR_INVALID_ARG),   # boxes, bad source
                             (good, B.BF16, B.ERR_UNSUPPORTED),     # fp16 cache, bf16 source
                             (good, B.I8, B.ERR_INVALID_ARG)):
-        with pytest.raises(B.PkvError) as e:   # fused append + attention: what it refuses
+        with pytest.raises(B.PkvError) as e:   # one-call decode step: what it refuses
             B.append_decode_attention(desc, 1, 2, 0xC000, 0xD000, src, 0x4000, B.F16, 0.125, 0x5000, 4,
                                       0x6000, 0x7000, B.F32, 0, -1, 0x8000, 1 << 20, 0, 0)
         assert e.value.status == want
