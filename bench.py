@@ -322,8 +322,12 @@ class Replica:
             c.append(self.knews[i][s], self.vnews[i][s], self.bts[i], self.pos_list[s],
                      dev_status=self.status, stream=stream)
         if sparse:
+            # early start: the kernel before the scoring (another layer's
+            # combine) writes nothing it reads; after this step's append (which
+            # refreshes the boxes) it waits
             c.score_topk(self.qs[i], self.bts[i], self.len_list[s], self.top_k, dev_status=self.status,
-                         sel=self.sel[i], count=self.cnt[i], stream=stream, group_mode=self.group_mode)
+                         sel=self.sel[i], count=self.cnt[i], stream=stream, group_mode=self.group_mode,
+                         early_start=EARLY_START and not append)
         if attention:
             # early start: after this step's append, the kernel before the
             # attention writes only the new token's rows (fresh_rows = 1); after
@@ -595,7 +599,8 @@ def sparse_breakdown(peak: float) -> List[Dict]:
 
         def score_only():
             c.score_topk(rep.qs[0], rep.bts[0], rep.len_list[0], K, dev_status=rep.status, sel=rep.sel[0],
-                         count=rep.cnt[0], stream=torch.cuda.current_stream(), group_mode=gm)
+                         count=rep.cnt[0], stream=torch.cuda.current_stream(), group_mode=gm,
+                         early_start=EARLY_START)
 
         def attention_only():
             c.attention(rep.qs[0], rep.bts[0], rep.len_list[0], sm_scale=w.sm_scale, sel=rep.sel[0],

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 4
+#define PKV_ABI_VERSION 5
 
 typedef enum {
   PKV_OK = 0,
@@ -184,6 +184,15 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new,
  *   sel_count  : int32 [batch][R].
  *   scores_out : fp32 [batch][R][max_pages] or NULL (the row's scores); entries
  *                past the sequence's pages are -inf.
+ *   early_start: 0, or 1: a promise that the work launched just before this
+ *                call on `stream` (one kernel, or both kernels of a preceding
+ *                attention call) writes nothing this call reads: q, the block
+ *                table, the lengths and the page boxes. The call then reads and
+ *                scores at once and waits for that work only before its first
+ *                write (sel_pages, sel_count, scores_out, which may be shared
+ *                with that work); only dev_status flags can be raised before
+ *                the wait. Not after an append that refreshed the boxes (pass
+ *                0 there). A false promise gives wrong results, not a fault.
  * Needs cache->page_meta. Pages per sequence are limited to 16384.
  * Device errors: PKV_DEV_BAD_PAGE (that page scores -inf).
  */
@@ -191,8 +200,8 @@ pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t nu
                                const void* q, pkv_dtype q_dtype,
                                const int32_t* block_table, int32_t max_pages,
                                const int32_t* seq_lens, int32_t top_k, int32_t group_mode,
-                               int32_t* sel_pages, int32_t* sel_count, float* scores_out,
-                               int32_t* dev_status, void* stream);
+                               int32_t early_start, int32_t* sel_pages, int32_t* sel_count,
+                               float* scores_out, int32_t* dev_status, void* stream);
 
 /*
  * Workspace bytes needed by pkv_paged_decode_attention for these shapes.

@@ -69,7 +69,7 @@ def lib() -> ctypes.CDLL:
         "pkv_abi_version": (i32, []),
         "pkv_tuning_reload": (None, []),
         "pkv_kv_append": (c_int, [P, i32, i32, vp, vp, c_int, vp, i32, vp, vp, vp, vp]),
-        "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, i32, vp, vp, vp, vp, vp]),
+        "pkv_page_score_topk": (c_int, [P, i32, i32, vp, c_int, vp, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp]),
         "pkv_attention_workspace_bytes": (c_size_t, [P, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (c_int, [P, i32, i32, vp, c_int, c_float, vp, i32, vp, vp, vp,
                                                i32, i32, vp, c_int, i32, i32, vp, c_size_t, vp, vp]),
@@ -122,11 +122,13 @@ def kv_append(cache: PkvCache, batch: int, t_new: int, k_new: int, v_new: int, s
 def page_score_topk(cache: PkvCache, batch: int, num_q_heads: int, q: int, q_dtype: int,
                     block_table: int, max_pages: int, seq_lens: int, top_k: int, sel_pages: int,
                     sel_count: int, scores_out: int, dev_status: int, stream: int,
-                    group_mode: int = SELECT_PER_HEAD) -> None:
-    """group_mode comes last here (keyword) and goes after top_k in the C call."""
+                    group_mode: int = SELECT_PER_HEAD, early_start: int = 0) -> None:
+    """group_mode and early_start come last here (keywords) and go after top_k in
+    the C call."""
     _check(lib().pkv_page_score_topk(ctypes.byref(cache), batch, num_q_heads, q, q_dtype,
-                                     block_table, max_pages, seq_lens, top_k, group_mode, sel_pages,
-                                     sel_count, scores_out or None, dev_status or None, stream or None),
+                                     block_table, max_pages, seq_lens, top_k, group_mode, early_start,
+                                     sel_pages, sel_count, scores_out or None, dev_status or None,
+                                     stream or None),
            "page_score_topk")
 
 

@@ -116,10 +116,14 @@ class PagedKVCache:
                    top_k: int, want_scores: bool = False, dev_status: Optional[torch.Tensor] = None,
                    sel: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
                    scores: Optional[torch.Tensor] = None,
-                   stream: Optional[torch.cuda.Stream] = None, group_mode: int = 0):
+                   stream: Optional[torch.cuda.Stream] = None, group_mode: int = 0,
+                   early_start: bool = False):
         """Top-K pages per row: per (sequence, query head), or with group_mode 1 / 2
         (sum / max of the group's scores) per (sequence, kv head). Returns
-        (sel [B][R][K], count [B][R], scores [B][R][max_pages] or None)."""
+        (sel [B][R][K], count [B][R], scores [B][R][max_pages] or None).
+
+        early_start: the kernel launched just before on the stream writes nothing
+        this call reads (q, tables, lengths, boxes), so the scoring starts under it."""
         _need(q, "q", device=self.device)
         Bsz, Hq = q.shape[0], q.shape[1]
         R = Hq if group_mode == 0 else self.num_kv_heads
@@ -132,7 +136,8 @@ class PagedKVCache:
             scores = torch.empty((Bsz, R, mp), dtype=torch.float32, device=self.device)
         B.page_score_topk(self._desc, Bsz, Hq, q.data_ptr(), pkv_dtype(q), block_table.data_ptr(),
                           mp, seq_lens.data_ptr(), top_k, sel.data_ptr(), count.data_ptr(),
-                          _ptr(scores), _ptr(dev_status), _stream(stream), group_mode=group_mode)
+                          _ptr(scores), _ptr(dev_status), _stream(stream), group_mode=group_mode,
+                          early_start=1 if early_start else 0)
         return sel, count, scores
 
     # --------------------------------------------------------------- attention

@@ -660,8 +660,8 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
 pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t num_q_heads,
                                const void* q, pkv_dtype q_dtype, const int32_t* block_table,
                                int32_t max_pages, const int32_t* seq_lens, int32_t top_k,
-                               int32_t group_mode, int32_t* sel_pages, int32_t* sel_count,
-                               float* scores_out, int32_t* dev_status, void* stream) {
+                               int32_t group_mode, int32_t early_start, int32_t* sel_pages,
+                               int32_t* sel_count, float* scores_out, int32_t* dev_status, void* stream) {
   pkv_status st = check_cache(cache, false);
   if (st != PKV_OK) return st;
   if (!cache->page_meta) return PKV_ERR_INVALID_ARG;
@@ -669,10 +669,11 @@ pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t nu
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (max_pages <= 0 || top_k < 1) return PKV_ERR_INVALID_ARG;
   if (group_mode < PKV_SELECT_PER_HEAD || group_mode > PKV_SELECT_GROUP_MAX) return PKV_ERR_INVALID_ARG;
+  if (early_start != 0 && early_start != 1) return PKV_ERR_INVALID_ARG;
   if (max_pages > 16384) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
   if (!q || !block_table || !seq_lens || !sel_pages || !sel_count) return PKV_ERR_INVALID_ARG;
-  TopkParams p;
+  TopkParams p = {};
   p.page_meta = cache->page_meta;
   p.q = q;
   p.block_table = block_table;
@@ -692,6 +693,7 @@ pkv_status pkv_page_score_topk(const pkv_cache* cache, int32_t batch, int32_t nu
   p.top_k = top_k;
   p.q_dtype = q_dtype;
   p.group_mode = group_mode;
+  p.early = early_start;
   return launch_topk(p, static_cast<cudaStream_t>(stream));
 }
 

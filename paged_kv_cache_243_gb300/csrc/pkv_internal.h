@@ -35,6 +35,7 @@ struct TopkParams {
   int num_pages, page_size, num_kv_heads, head_dim;
   int num_q_heads, group, batch, max_pages, top_k, q_dtype;
   int group_mode;  // PKV_SELECT_*: rows are query heads, or kv heads (group sum / max)
+  int early;       // 1: read and score before waiting for the preceding work
 };
 
 pkv_status launch_append(const AppendParams& p, cudaStream_t st);

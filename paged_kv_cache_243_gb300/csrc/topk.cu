@@ -202,8 +202,13 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   __shared__ int hist[256];
   __shared__ int warp_tot[kTopkWarps];
   __shared__ int sel_digit, sel_remaining;
-  pdl_wait();
-  pdl_launch_dependents();
+  // early start: the caller promises that the preceding work writes nothing
+  // read here, so the boxes are read and scored at once; every block waits
+  // before its first global write (below), and so before it completes
+  if (!p.early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -344,6 +349,10 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     }
   }
   __syncthreads();
+  if (p.early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   if (p.scores_out) {
     for (int r = 0; r < NR; ++r) {
       float* so = p.scores_out + ((size_t)b * rows_per_b + row0 + r) * p.max_pages;

@@ -92,6 +92,10 @@ def test_argument_checks_before_cuda(B):
         B.page_score_topk(with_meta, 1, 2, 0x4000, B.F16, 0x5000, 4, 0x6000, 2, 0x9000, 0xA000, 0, 0, 0,
                           group_mode=3)
     assert e.value.status == B.ERR_INVALID_ARG
+    with pytest.raises(B.PkvError) as e:   # early_start must be 0 or 1
+        B.page_score_topk(with_meta, 1, 2, 0x4000, B.F16, 0x5000, 4, 0x6000, 2, 0x9000, 0xA000, 0, 0, 0,
+                          early_start=2)
+    assert e.value.status == B.ERR_INVALID_ARG
     for desc, src, want in ((_desc(B, kv_dtype=B.I8, quant=B.QUANT_PER_GROUP64, kv_sz=0x3000,
                                    page_size=64), B.F16, B.ERR_INVALID_ARG),   # per-group without a tail
                             (_desc(B, page_meta=0xB000), B.I8, B.ERR_INVALID_ARG),   # boxes, bad source

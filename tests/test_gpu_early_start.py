@@ -229,3 +229,38 @@ def test_early_sparse_lists_shorter_than_their_stride():
             o = O.sparse_decode_attention(qf[b, h:h + 1], sd.k[:, h:h + 1], sd.v[:, h:h + 1], w.sm_scale,
                                           [sel[b, h, :cnt[b, h]]], 16)[0]
             assert np.abs(out[b, h] - o).max() <= T["f16"], (b, h)
+
+
+@pytest.mark.parametrize("group_mode", [0, 1])
+def test_scoring_started_under_the_previous_attention(group_mode):
+    # layers in a row on one set of list buffers: each scoring starts early
+    # (early_start) under the previous sparse attention call, which may still
+    # read the lists the scoring overwrites; lists and outputs equal those of
+    # scorings that wait up front
+    w = synth.Workload(name="early-score", seed=720 + group_mode, batch=4, layers=1, num_q_heads=16,
+                       num_kv_heads=4, head_dim=128, page_size=16, dtype="f16", quant="per_token",
+                       seq_len=None, seq_len_range=(1, 600), outlier_channels=4, outlier_scale=15.0,
+                       page_offset_std=0.5)
+    ld = load_workload(w, lens=np.array([600, 17, 333, 129], dtype=np.int32), with_meta=True)
+    shared = group_mode != 0
+    R = w.num_kv_heads if shared else w.num_q_heads
+    top_k = 6
+    qs = [queries_dev(w, step=s)[0] for s in range(4)]
+    res = {}
+    for early in (True, False):
+        sel = torch.empty((w.batch, R, top_k), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((w.batch, R), dtype=torch.int32, device="cuda")
+        outs = []
+        for s in range(4):
+            # (an attention that read lists already overwritten would differ)
+            ld.cache.score_topk(qs[s], ld.bt_dev, ld.lens_dev, top_k, dev_status=ld.status, sel=sel, count=cnt,
+                                group_mode=group_mode, early_start=early and s > 0)
+            outs.append(ld.cache.attention(qs[s], ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, sel=sel,
+                                           sel_count=cnt, sel_shared=shared, dev_status=ld.status, fresh_rows=0))
+        torch.cuda.synchronize()
+        res[early] = ([o.cpu().numpy() for o in outs], sel.cpu().numpy(), cnt.cpu().numpy())
+    assert np.array_equal(res[True][1], res[False][1])
+    assert np.array_equal(res[True][2], res[False][2])
+    for s in range(4):
+        assert np.abs(res[True][0][s] - res[False][0][s]).max() <= 1e-6, s
+    assert int(ld.status.item()) == 0
