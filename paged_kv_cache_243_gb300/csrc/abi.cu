@@ -24,6 +24,14 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// log2(page_size) for a power of two, else -1 (the append kernels then divide)
+int page_shift(int ps) {
+  if (ps <= 0 || (ps & (ps - 1)) != 0) return -1;
+  int s = 0;
+  while ((1 << s) < ps) ++s;
+  return s;
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (!v || !*v) return dflt;
@@ -602,6 +610,7 @@ pkv_status pkv_append_decode_attention(const pkv_cache* cache, int32_t batch, in
     ap.batch = batch;
     ap.t_new = 1;
     ap.max_pages = max_pages;
+    ap.ps_shift = page_shift(cache->page_size);
     st = launch_append(ap, static_cast<cudaStream_t>(stream));
     if (st != PKV_OK) return st;
     return attention_impl(cache, batch, num_q_heads, q, q_dtype, sm_scale, block_table, max_pages, seq_lens,
@@ -654,6 +663,7 @@ pkv_status pkv_kv_append(const pkv_cache* cache, int32_t batch, int32_t t_new, c
   p.t_new = t_new;
   p.max_pages = max_pages;
   p.pos_bias = 0;
+  p.ps_shift = page_shift(cache->page_size);
   return launch_append(p, static_cast<cudaStream_t>(stream));
 }
 

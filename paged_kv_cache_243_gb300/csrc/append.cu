@@ -33,6 +33,15 @@ __device__ __forceinline__ bool row_window(const AppendParams& p, int b, int& po
   return n > 0;
 }
 
+// Position -> (logical page, row in the page): a shift and a mask for the
+// usual power-of-two page sizes, else an integer division.
+__device__ __forceinline__ int page_div(const AppendParams& p, int x) {
+  return p.ps_shift >= 0 ? x >> p.ps_shift : x / p.page_size;
+}
+__device__ __forceinline__ int page_mod(const AppendParams& p, int x) {
+  return p.ps_shift >= 0 ? x & (p.page_size - 1) : x % p.page_size;
+}
+
 __device__ __forceinline__ int page_of(const AppendParams& p, int b, int lp) {
   const int phys = p.block_table[(size_t)b * p.max_pages + lp];
   if (phys < 0 || phys >= p.num_pages) {
@@ -73,9 +82,9 @@ __global__ void append_copy_kernel(const AppendParams p) {
   int pos, n;
   if (!row_window(p, b, pos, n) || t >= n) return;
   const int tp = pos + t;
-  const int phys = page_of(p, b, tp / p.page_size);
+  const int phys = page_of(p, b, page_div(p, tp));
   if (phys < 0) return;
-  const int slot = tp % p.page_size;
+  const int slot = page_mod(p, tp);
   auto put = [&](int idx, uint4 v) {
     int kv, g, e8;
     src_of(idx, kv, g, e8);
@@ -114,7 +123,7 @@ __global__ void append_copy_kernel(const AppendParams p) {
 // is processed (and before the position and block-table lookups), so a warp
 // keeps 2 KB of loads in flight.
 constexpr int kTokPerWarp = 8;
-template <int D, bool U4>
+template <int D, bool U4, bool SRC_BF16>
 __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -140,7 +149,7 @@ __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParam
 #pragma unroll
   for (int gi = 0; gi < 2; ++gi) {
     const int t = wt + 4 * gi + sub;
-    phys[gi] = t < n ? p.block_table[(size_t)b * p.max_pages + (pos + t) / p.page_size] : -1;
+    phys[gi] = t < n ? p.block_table[(size_t)b * p.max_pages + page_div(p, pos + t)] : -1;
   }
 #pragma unroll
   for (int gi = 0; gi < 2; ++gi) {
@@ -148,7 +157,7 @@ __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParam
     float x[EPL];
 #pragma unroll
     for (int e = 0; e < EPL / 4; ++e) {
-      const float4 f = widen4(raw[gi][e], p.src_dtype);
+      const float4 f = widen4_t<SRC_BF16>(raw[gi][e]);
       x[4 * e] = f.x; x[4 * e + 1] = f.y; x[4 * e + 2] = f.z; x[4 * e + 3] = f.w;
     }
     float mn = x[0], mx = x[0];
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParam
     const float s = __fdiv_rn(__fsub_rn(mx, mn), U4 ? 15.f : 255.f);
     const float z = mn;
     const float rs = quant_recip(s);
-    const size_t row = ((size_t)ph * H + g) * p.page_size + (pos + t) % p.page_size;
+    const size_t row = ((size_t)ph * H + g) * p.page_size + page_mod(p, pos + t);
     if constexpr (U4) {
       uint32_t w[EPL / 8];
       quant_nibbles<EPL>(x, s, z, rs, w);
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(cons
                        : load_src4(sp, p.src_dtype, (((size_t)b * p.t_new + (tok - pos)) * H + g) * D + e);
     }
   }
-  if (threadIdx.x == 0) ok_s = page_of(p, b, t0 / p.page_size);
+  if (threadIdx.x == 0) ok_s = page_of(p, b, page_div(p, t0));
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int k = 0; k < kGroupVec4; ++k) {
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(cons
   const float s = __fdiv_rn(__fsub_rn(mx, mn), 255.f);
   const float z = mn;
   const float rs = quant_recip(s);
-  const int off0 = t0 % p.page_size;
+  const int off0 = page_mod(p, t0);
   int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) +
                 (((size_t)phys * H + g) * p.page_size + off0) * D;
   float* tw = tail_row(p, b, g, kv, gi & 1);
@@ -326,7 +335,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_group_bulk_kernel(con
       vr[k] = *reinterpret_cast<const uint2*>(vs + idx);
     }
   }
-  if (threadIdx.x == 0) phys_s = page_of(p, b, t0 / p.page_size);
+  if (threadIdx.x == 0) phys_s = page_of(p, b, page_div(p, t0));
   float kmn = INFINITY, kmx = -INFINITY, vmn = INFINITY, vmx = -INFINITY;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_group_bulk_kernel(con
   }
   const float sk = __fdiv_rn(__fsub_rn(kmx, kmn), 255.f), sv = __fdiv_rn(__fsub_rn(vmx, vmn), 255.f);
   const float rk = quant_recip(sk), rv = quant_recip(sv);
-  const int off0 = t0 % p.page_size;
+  const int off0 = page_mod(p, t0);
   const size_t base = (((size_t)phys * H + g) * p.page_size + off0) * D;
   int8_t* kd = reinterpret_cast<int8_t*>(p.k_pages) + base;
   int8_t* vd = reinterpret_cast<int8_t*>(p.v_pages) + base;
@@ -437,8 +446,8 @@ __global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) 
   if (g >= H) return;
   int pos, n;
   if (!row_window(p, b, pos, n)) return;
-  const int lp = pos / ps + blockIdx.x;
-  if (lp > (pos + n - 1) / ps) return;
+  const int lp = page_div(p, pos) + blockIdx.x;
+  if (lp > page_div(p, pos + n - 1)) return;
   const int phys = page_of(p, b, lp);
   if (phys < 0) return;
   const int nv = min(ps, pos + n - lp * ps);
@@ -454,28 +463,38 @@ __global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) 
   for (int r0 = 0; r0 < nv; r0 += 2 * RPL) {
     uint32_t w[RPL][RW];
     float2 sc[RPL];
+    // rows of this pass: all valid (the usual case: one base, constant
+    // offsets), or clamped to the last valid row (a repeated row leaves the
+    // bounds unchanged)
+    auto load_rows = [&](auto full_t) {
+      constexpr bool FULL = decltype(full_t)::value;
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-      const int t = min(r0 + ro + 2 * i, nv - 1);   // a repeated row leaves the bounds unchanged
-      const uint8_t* src = kb + (size_t)t * ROWB;
-      if constexpr (RB == 16) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src);
-        w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
-      } else if constexpr (RB == 8) {
-        const uint2 v = *reinterpret_cast<const uint2*>(src);
-        w[i][0] = v.x; w[i][1] = v.y;
-      } else if constexpr (RB == 4) {
-        w[i][0] = *reinterpret_cast<const uint32_t*>(src);
-      } else {
-        w[i][0] = *reinterpret_cast<const uint16_t*>(src);
+      for (int i = 0; i < RPL; ++i) {
+        const int t = FULL ? r0 + ro + 2 * i : min(r0 + ro + 2 * i, nv - 1);
+        const uint8_t* src = FULL ? kb + (size_t)(r0 + ro) * ROWB + 2 * i * ROWB : kb + (size_t)t * ROWB;
+        if constexpr (RB == 16) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+        } else if constexpr (RB == 8) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          w[i][0] = v.x; w[i][1] = v.y;
+        } else if constexpr (RB == 4) {
+          w[i][0] = *reinterpret_cast<const uint32_t*>(src);
+        } else {
+          w[i][0] = *reinterpret_cast<const uint16_t*>(src);
+        }
+        if constexpr (KV == KV_I8T || KV == KV_U4T)
+          sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (row0 + t) * 4);
+        else if constexpr (KV == KV_I8G)
+          sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + t / 64) * 4);
+        else
+          sc[i] = make_float2(0.f, 0.f);
       }
-      if constexpr (KV == KV_I8T || KV == KV_U4T)
-        sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (row0 + t) * 4);
-      else if constexpr (KV == KV_I8G)
-        sc[i] = *reinterpret_cast<const float2*>(p.kv_sz + (((size_t)phys * H + g) * (ps / 64) + t / 64) * 4);
-      else
-        sc[i] = make_float2(0.f, 0.f);
-    }
+    };
+    if (r0 + 2 * RPL <= nv)
+      load_rows(std::true_type{});
+    else
+      load_rows(std::false_type{});
     // channels (c, c + 1) of every row i: values (a[i], b[i]), then the chains
     auto fold = [&](int c, const float (&a)[RPL], const float (&bb)[RPL]) {
       float l0 = mn[c], h0 = mx[c], l1 = mn[c + 1], h1 = mx[c + 1];
@@ -551,12 +570,14 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st) {
   } else if (p.quant == PKV_QUANT_PER_TOKEN) {
     const int warps = min(8, (p.t_new + kTokPerWarp - 1) / kTokPerWarp);
     const dim3 grid((p.t_new + warps * kTokPerWarp - 1) / (warps * kTokPerWarp), H * 2, p.batch);
-    const bool u4 = p.kv_dtype == PKV_U4;
-    const void* fn = p.head_dim == 128
-                         ? (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<128, true>)
-                               : reinterpret_cast<const void*>(&append_per_token_kernel<128, false>))
-                         : (u4 ? reinterpret_cast<const void*>(&append_per_token_kernel<64, true>)
-                               : reinterpret_cast<const void*>(&append_per_token_kernel<64, false>));
+    const bool u4 = p.kv_dtype == PKV_U4, bf = p.src_dtype == PKV_BF16;
+    const void* fn = nullptr;
+#define PKV_PT(d, q4, sb) \
+    if (p.head_dim == d && u4 == q4 && bf == sb) fn = reinterpret_cast<const void*>(&append_per_token_kernel<d, q4, sb>);
+    PKV_PT(128, false, false) PKV_PT(128, false, true) PKV_PT(128, true, false) PKV_PT(128, true, true)
+    PKV_PT(64, false, false) PKV_PT(64, false, true) PKV_PT(64, true, false) PKV_PT(64, true, true)
+#undef PKV_PT
+    if (!fn) return PKV_ERR_UNSUPPORTED;
     e = launch_pdl(fn, grid, dim3(32 * warps), 0, st, args1);
   } else {
     const int groups = (p.t_new + 63) / 64 + 1;

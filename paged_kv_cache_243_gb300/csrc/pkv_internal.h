@@ -21,6 +21,7 @@ struct AppendParams {
   int kv_dtype, quant, src_dtype;
   int batch, t_new, max_pages;
   int pos_bias;   // added to positions[b] (-1: positions are the lengths after the append)
+  int ps_shift;   // log2(page_size) when it is a power of two, else -1
 };
 
 struct TopkParams {

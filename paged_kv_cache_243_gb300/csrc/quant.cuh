@@ -97,12 +97,29 @@ __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float 
 // at most 15). N values (N even) -> N / 2 bytes, value 2i in the low
 // nibble of byte i; w[k] holds bytes 4k .. 4k + 3.
 // Packs quant_rint's results as 4-bit codes, value 2i in the low nibble of byte i.
+// The codes sit in the low bytes of m (at most 15); for whole words byte
+// permutes gather the even and the odd values' bytes of eight values, and one
+// shift and or merges them.
 template <int N>
 __device__ __forceinline__ void pack_nibbles(const float (&m)[N], uint32_t (&w)[(N + 7) / 8]) {
+  if constexpr (N % 8 != 0) {   // a partial word: value by value
 #pragma unroll
-  for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
+    for (int k = 0; k < (N + 7) / 8; ++k) w[k] = 0u;
 #pragma unroll
-  for (int e = 0; e < N; ++e) w[e / 8] |= (__float_as_uint(m[e]) & 0xFu) << (4 * (e % 8));
+    for (int e = 0; e < N; ++e) w[e / 8] |= (__float_as_uint(m[e]) & 0xFu) << (4 * (e % 8));
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < N / 8; ++k) {
+    const float* v = m + 8 * k;
+    const uint32_t e01 = __byte_perm(__float_as_uint(v[0]), __float_as_uint(v[2]), 0x0040);
+    const uint32_t e23 = __byte_perm(__float_as_uint(v[4]), __float_as_uint(v[6]), 0x0040);
+    const uint32_t o01 = __byte_perm(__float_as_uint(v[1]), __float_as_uint(v[3]), 0x0040);
+    const uint32_t o23 = __byte_perm(__float_as_uint(v[5]), __float_as_uint(v[7]), 0x0040);
+    const uint32_t ev = __byte_perm(e01, e23, 0x5410);   // bytes: values 0, 2, 4, 6
+    const uint32_t od = __byte_perm(o01, o23, 0x5410);   // bytes: values 1, 3, 5, 7
+    w[k] = ev | (od << 4);
+  }
 }
 
 template <int N>
@@ -116,6 +133,19 @@ __device__ __forceinline__ void quant_nibbles(const float (&x)[N], float s, floa
   float m[N];
   quant_rint<N>(x, s, z, rs, m);
   pack_nibbles<N>(m, w);
+}
+
+// Four 16-bit source values (f16/bf16, as loaded) widened to fp32; the
+// compile-time form for kernels specialised on the source dtype.
+template <bool BF16>
+__device__ __forceinline__ float4 widen4_t(uint2 w) {
+  if constexpr (BF16)
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+  return make_float4(__half2float(__ushort_as_half((unsigned short)(w.x & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.x >> 16))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y & 0xffffu))),
+                     __half2float(__ushort_as_half((unsigned short)(w.y >> 16))));
 }
 
 // Four 16-bit source values (f16/bf16, as loaded) widened to fp32.
