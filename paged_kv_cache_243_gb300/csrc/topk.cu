@@ -366,10 +366,27 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   cluster.sync();
   for (int r = rank; r < NR; r += CS) {
     __syncthreads();   // the previous row's select is done with keys
-    for (int rr = 0; rr < CS; ++rr) {
-      const float* remote = cluster.map_shared_rank(own, rr) + (size_t)r * span;
-      const int a0 = (int)((long long)P * rr / CS), a1 = (int)((long long)P * (rr + 1) / CS);
-      for (int i = a0 + tid; i < a1; i += kTopkThreads) keys[i] = __float_as_uint(remote[i - a0]);
+    // page i sits in block rr = floor(((i + 1) CS - 1) / P) of the cluster, at
+    // i - floor(P rr / CS); a thread's remote loads (up to GR pages) are all
+    // issued before the first is stored
+    constexpr int GR = 4;
+    for (int i0 = 0; i0 < P; i0 += GR * kTopkThreads) {
+      uint32_t v[GR];
+#pragma unroll
+      for (int j = 0; j < GR; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        v[j] = 0u;
+        if (i < P) {
+          const int rr = (int)(((long long)(i + 1) * CS - 1) / P);
+          const int a0 = (int)((long long)P * rr / CS);
+          v[j] = __float_as_uint(cluster.map_shared_rank(own, rr)[(size_t)r * span + (i - a0)]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < GR; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        if (i < P) keys[i] = v[j];
+      }
     }
     __syncthreads();
     const size_t bh = (size_t)b * rows_per_b + row0 + r;
