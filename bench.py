@@ -886,8 +886,10 @@ def run_ours(args) -> None:
            "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
            "how": "per step: one graph replay (one copy of all layers' pinned-host q and new K/V "
-                  "tokens in, 32 x (kv_append, paged_decode_attention) C-ABI calls, one copy of all "
-                  "outputs to pinned host memory) then a host wait for the outputs; host clock"}
+                  "tokens in, the step's C-ABI calls for every layer (as in the timed step: one "
+                  "append_decode_attention per layer, or kv_append + paged_decode_attention where "
+                  "that path is off), one copy of all outputs to pinned host memory) then a host "
+                  "wait for the outputs; host clock"}
 
     extras = None
     del ga, ge
