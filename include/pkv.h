@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 5
+#define PKV_ABI_VERSION 6
 
 typedef enum {
   PKV_OK = 0,
@@ -86,14 +86,15 @@ typedef enum {
  *
  * Layouts (all row-major, device memory, caller-owned):
  *   k_pages, v_pages : [num_pages][num_kv_heads][page_size][head_dim] of kv_dtype
- *                      (U4: [..][head_dim / 2] bytes, channel 2i in the low
- *                      nibble of byte i). Token slot s of logical page i of a
- *                      sequence holds its token i * page_size + s.
+ *                      (I8: unsigned bytes u = code + 128; U4: [..][head_dim / 2]
+ *                      bytes, channel 2i in the low nibble of byte i). Token
+ *                      slot s of logical page i of a sequence holds its token
+ *                      i * page_size + s.
  *   kv_sz            : I8 and U4 only, fp32 [num_pages][num_kv_heads][page_size / gran][4]
  *                      with gran = 1 (per token) or 64 (per group, I8 only); the
  *                      4 floats are (k_scale, k_zero, v_scale, v_zero).
- *                      Restoration: x = (code + 128) * scale + zero for I8
- *                      (signed codes), x = u * scale + zero for U4 (u in [0, 15]).
+ *                      Restoration: x = u * scale + zero, u the stored byte
+ *                      (I8: u = code + 128 in [0, 255]; U4: u in [0, 15]).
  *   tail             : PER_GROUP64 only, fp32
  *                      [tail_rows][num_kv_heads][2 (K, V)][2 (group parity)][64][head_dim]:
  *                      original values of each sequence's open (partially filled)
@@ -155,8 +156,9 @@ void pkv_tuning_reload(void);
  * (closed groups never change). If page_meta is set, the bounding box of every
  * page the append touched is recomputed from the stored keys.
  * Quantiser (bit-exact definition, fp32 ops, ties to even):
- *   I8: s = (max - min) / 255; z = min; code = clamp(rint((x - z) / s), 0, 255) - 128;
- *       a constant block stores s = 0 and codes -128.
+ *   I8: s = (max - min) / 255; z = min; code = clamp(rint((x - z) / s), 0, 255) - 128,
+ *       stored as the byte u = code + 128; a constant block stores s = 0 and
+ *       codes -128 (bytes 0).
  *   U4: s = (max - min) / 15; z = min; u = clamp(rint((x - z) / s), 0, 15);
  *       a constant row stores s = 0 and codes 0.
  * Device errors: PKV_DEV_BAD_POSITION (slot beyond max_pages * page_size or

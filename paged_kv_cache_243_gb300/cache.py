@@ -16,8 +16,8 @@ from . import binding as B
 
 _TORCH_TO_PKV = {torch.float16: B.F16, torch.bfloat16: B.BF16, torch.float32: B.F32}
 _NAME_TO_PKV = {"f16": B.F16, "bf16": B.BF16, "int8": B.I8, "u4": B.U4}
-_PKV_TO_TORCH = {B.F16: torch.float16, B.BF16: torch.bfloat16, B.F32: torch.float32, B.I8: torch.int8,
-                 B.U4: torch.uint8}
+_PKV_TO_TORCH = {B.F16: torch.float16, B.BF16: torch.bfloat16, B.F32: torch.float32, B.I8: torch.uint8,
+                 B.U4: torch.uint8}   # I8 pools hold the bytes u = code + 128
 _QUANT = {"none": B.QUANT_NONE, "per_token": B.QUANT_PER_TOKEN, "per_group64": B.QUANT_PER_GROUP64}
 
 

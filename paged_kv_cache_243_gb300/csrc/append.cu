@@ -9,7 +9,8 @@
 // The quantisers are exact fp32 operation sequences (correctly rounded
 // subtract and divide, round half to even), so codes, scales and zero-points
 // are bit-identical to any other IEEE implementation of the same sequence:
-//   INT8: s = (max - min) / 255, z = min, code = clamp(rint((x - z) / s), 0, 255) - 128;
+//   INT8: s = (max - min) / 255, z = min, code = clamp(rint((x - z) / s), 0, 255) - 128,
+//   stored as the byte u = code + 128;
 //   4-bit: s = (max - min) / 15, z = min, u = clamp(rint((x - z) / s), 0, 15).
 #include "pkv_internal.h"
 #include "quant.cuh"
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(256) append_per_token_kernel(const AppendParam
     } else {
       uint32_t w[EPL / 4];
       quant_words<EPL>(x, s, z, rs, w);
-      int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? p.v_pages : p.k_pages) + row * D + part * EPL;
       if constexpr (EPL == 16)
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       else
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_per_group_kernel(cons
   const float z = mn;
   const float rs = quant_recip(s);
   const int off0 = page_mod(p, t0);
-  int8_t* dst = reinterpret_cast<int8_t*>(kv ? p.v_pages : p.k_pages) +
+  uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? p.v_pages : p.k_pages) +
                 (((size_t)phys * H + g) * p.page_size + off0) * D;
   float* tw = tail_row(p, b, g, kv, gi & 1);
   const bool keep = write_tail && t_end - t0 < 64;
@@ -376,8 +377,8 @@ __global__ void __launch_bounds__(kGroupThreads, 4) append_group_bulk_kernel(con
   const float rk = quant_recip(sk), rv = quant_recip(sv);
   const int off0 = page_mod(p, t0);
   const size_t base = (((size_t)phys * H + g) * p.page_size + off0) * D;
-  int8_t* kd = reinterpret_cast<int8_t*>(p.k_pages) + base;
-  int8_t* vd = reinterpret_cast<int8_t*>(p.v_pages) + base;
+  uint8_t* kd = reinterpret_cast<uint8_t*>(p.k_pages) + base;
+  uint8_t* vd = reinterpret_cast<uint8_t*>(p.v_pages) + base;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int f = threadIdx.x + k * kGroupThreads;
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(128) append_meta_kernel(const AppendParams p) 
         for (int jp = 0; jp < 4 && 4 * q + jp < C; jp += 2) {
           float a[RPL], bv[RPL];
 #pragma unroll
-          for (int i = 0; i < RPL; ++i) deq(i, u8pair(w[i][q] ^ 0x80808080u, jp), a[i], bv[i]);
+          for (int i = 0; i < RPL; ++i) deq(i, u8pair(w[i][q], jp), a[i], bv[i]);
           fold(4 * q + jp, a, bv);
         }
       } else if constexpr (KV == KV_U4T) {   // word q: channels 8q .. 8q + 7

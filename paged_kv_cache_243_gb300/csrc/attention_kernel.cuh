@@ -175,7 +175,7 @@ __device__ __forceinline__ int qk_dim(int j, int e) {
 }
 
 // Load this lane's D/8 channels of token row `row` (score layout) as packed
-// fp32 pairs (INT8: u = code + 128; 4-bit: u = the code).
+// fp32 pairs (INT8: the stored byte u = code + 128; 4-bit: u = the code).
 template <int D, int KV>
 __device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, uint64_t (&k2)[D / 16]) {
   if constexpr (KV == KV_F16 || KV == KV_BF16) {
@@ -209,12 +209,12 @@ __device__ __forceinline__ void load_k_slice(const uint8_t* row, int j, uint64_t
   } else {
     if constexpr (D == 128) {
       const uint4 a = *reinterpret_cast<const uint4*>(row + j * 16);
-      const uint32_t w[4] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u, a.z ^ 0x80808080u, a.w ^ 0x80808080u};
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) k2[i] = u8pair(w[i >> 1], (i & 1) * 2);
     } else {
       const uint2 a = *reinterpret_cast<const uint2*>(row + j * 8);
-      const uint32_t w[2] = {a.x ^ 0x80808080u, a.y ^ 0x80808080u};
+      const uint32_t w[2] = {a.x, a.y};
 #pragma unroll
       for (int i = 0; i < 4; ++i) k2[i] = u8pair(w[i >> 1], (i & 1) * 2);
     }
@@ -245,11 +245,11 @@ __device__ __forceinline__ void load_v_slice(const uint8_t* row, int lane, uint6
     }
   } else {
     if constexpr (D == 128) {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(row + lane * 4) ^ 0x80808080u;
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(row + lane * 4);
       v2[0] = u8pair(a, 0);
       v2[1] = u8pair(a, 2);
     } else {
-      const uint32_t a = (uint32_t)(*reinterpret_cast<const uint16_t*>(row + lane * 2)) ^ 0x8080u;
+      const uint32_t a = (uint32_t)(*reinterpret_cast<const uint16_t*>(row + lane * 2));
       v2[0] = u8pair(a, 0);
     }
   }
@@ -305,7 +305,7 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[GE], int j) {
 // ------------------------------------------------------------ tensor-core path
 // Warp-level mma.sync m16n8k16 with fp32 accumulation, for query-head groups
 // (G >= 2): q.K^T as [16 tokens] x [8 heads] and P.V as [16 channels] x [8 heads]
-// per 16-token chunk. INT8 codes enter as exact fp16 integers u = c + 128.
+// per 16-token chunk. INT8 codes enter as exact fp16 integers.
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -322,11 +322,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
   }
 }
 
-// Two bytes of a sign-flipped INT8 word (selected by sel: 0x4140 -> bytes 0, 1;
+// Two stored INT8 bytes u of a word (selected by sel: 0x4140 -> bytes 0, 1;
 // 0x4342 -> bytes 2, 3) as the centred codes (u0 - 128, u1 - 128) in fp16:
 // 0x64xx is the fp16 value 1024 + xx, and subtracting 1152 is exact.
-__device__ __forceinline__ uint32_t u8x2_to_h2c(uint32_t wflip, uint32_t sel) {
-  const uint32_t h = __byte_perm(wflip, 0x64646464u, sel);
+__device__ __forceinline__ uint32_t u8x2_to_h2c(uint32_t w, uint32_t sel) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
   return r;
@@ -1308,8 +1308,8 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
           const int wi = ((4 * kk) % E) * ESZ / 4;
           uint32_t a0, a1, a2, a3;
           if constexpr (ESZ == 1) {
-            const uint32_t w0 = word_of(k0[m], wi) ^ 0x80808080u;
-            const uint32_t w1 = word_of(k1[m], wi) ^ 0x80808080u;
+            const uint32_t w0 = word_of(k0[m], wi);
+            const uint32_t w1 = word_of(k1[m], wi);
             a0 = u8x2_to_h2c(w0, 0x4140u);
             a2 = u8x2_to_h2c(w0, 0x4342u);
             a1 = u8x2_to_h2c(w1, 0x4140u);
@@ -1476,11 +1476,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
           const uint8_t* src = vrow + r * Geo::ROW + phys_block(r, g) * DPT;
           if constexpr (DPT == 16) {
             const uint4 v = *reinterpret_cast<const uint4*>(src);
-            rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
-            rw[jr][2] = v.z ^ 0x80808080u; rw[jr][3] = v.w ^ 0x80808080u;
+            rw[jr][0] = v.x; rw[jr][1] = v.y; rw[jr][2] = v.z; rw[jr][3] = v.w;
           } else {
             const uint2 v = *reinterpret_cast<const uint2*>(src);
-            rw[jr][0] = v.x ^ 0x80808080u; rw[jr][1] = v.y ^ 0x80808080u;
+            rw[jr][0] = v.x; rw[jr][1] = v.y;
           }
         }
         // Masked tokens (stale codes) need no clearing: every code is a

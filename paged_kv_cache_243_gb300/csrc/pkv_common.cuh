@@ -40,11 +40,10 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& a, float& b) {
   }
 }
 
-// INT8 codes c (stored with a -128 bias) as u = c + 128 in [0, 255], exactly:
-// flipping the sign bit of the byte gives u; placing u in the low mantissa
-// byte of 2^23 and subtracting 2^23 gives float(u).
-__device__ __forceinline__ float u8_as_float(uint32_t wflip, int i) {
-  return __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i)) - 8388608.0f;
+// Stored INT8 byte i of a word (u = code + 128, in [0, 255]) as float(u),
+// exactly: u in the low mantissa byte of 2^23, minus 2^23.
+__device__ __forceinline__ float u8_as_float(uint32_t w, int i) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + (uint32_t)i)) - 8388608.0f;
 }
 
 __device__ __forceinline__ float load_q_elem(const void* q, int dtype, size_t idx) {
@@ -126,10 +125,10 @@ __device__ __forceinline__ uint64_t u4pair(uint32_t lo, uint32_t hi, int i) {
   return fsub2(pack2f(a, b), pack2f(8388608.0f, 8388608.0f));
 }
 
-// Bytes i, i+1 of a sign-flipped INT8 word as the pair (u_i, u_i+1), u = code + 128.
-__device__ __forceinline__ uint64_t u8pair(uint32_t wflip, int i) {
-  const float a = __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i));
-  const float b = __uint_as_float(__byte_perm(wflip, 0x4B000000u, 0x7440u + (uint32_t)i + 1));
+// Stored INT8 bytes i, i+1 of a word as the pair (u_i, u_i+1), u = code + 128.
+__device__ __forceinline__ uint64_t u8pair(uint32_t w, int i) {
+  const float a = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + (uint32_t)i));
+  const float b = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + (uint32_t)i + 1));
   return fsub2(pack2f(a, b), pack2f(8388608.0f, 8388608.0f));
 }
 

@@ -2,9 +2,9 @@
 // append in the attention kernel [HBM-layout page, section 二 per-token;
 // Gemini page, 第一章 per-64-token group; 4-bit: KV-practice page, section
 // 3.2]: s = (max - min) / 255 (4-bit: / 15), z = min,
-// code = clamp(rint((x - z) / s), 0, 255) - 128 (4-bit: u in [0, 15]), every
-// step a correctly rounded fp32 operation, so codes are bit-identical to any
-// IEEE implementation.
+// code = clamp(rint((x - z) / s), 0, 255) - 128, stored as the byte
+// u = code + 128 (4-bit: u in [0, 15]), every step a correctly rounded fp32
+// operation, so codes are bit-identical to any IEEE implementation.
 #pragma once
 
 #include "pkv_common.cuh"
@@ -62,17 +62,16 @@ __device__ __forceinline__ void quant_rint(const float (&x)[N], float s, float z
   }
 }
 
-// Codes of N values as bytes (code + 128 = u in [0, 255], stored as the int8
-// u - 128, i.e. u ^ 0x80), packed 4 per word: w[k] holds values 4k .. 4k+3.
-// The quotient q lies in [0, 255 (1 + 2^-22)], so rint(q) needs no clamp.
-// Packs quant_rint's results as INT8 codes (byte u ^ 0x80 per value).
+// Codes of N values as the stored bytes u = code + 128 in [0, 255], packed 4
+// per word: w[k] holds values 4k .. 4k+3. The quotient q lies in [0, 255 (1 +
+// 2^-22)], so rint(q) needs no clamp, and its low mantissa byte is u.
 template <int N>
 __device__ __forceinline__ void pack_words(const float (&m)[N], uint32_t (&w)[N / 4]) {
 #pragma unroll
   for (int k = 0; k < N / 4; ++k) {
     const uint32_t lo = __byte_perm(__float_as_uint(m[4 * k]), __float_as_uint(m[4 * k + 1]), 0x0040);
     const uint32_t hi = __byte_perm(__float_as_uint(m[4 * k + 2]), __float_as_uint(m[4 * k + 3]), 0x0040);
-    w[k] = __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
+    w[k] = __byte_perm(lo, hi, 0x5410);
   }
 }
 
@@ -81,7 +80,7 @@ __device__ __forceinline__ void quant_words(const float (&x)[N], float s, float 
                                             uint32_t (&w)[N / 4]) {
   if (s == 0.f) {
 #pragma unroll
-    for (int k = 0; k < N / 4; ++k) w[k] = 0x80808080u;   // every code -128
+    for (int k = 0; k < N / 4; ++k) w[k] = 0u;   // every code -128 (stored byte 0)
     return;
   }
   float m[N];

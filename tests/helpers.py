@@ -175,6 +175,11 @@ def max_abs_err(gpu_out: np.ndarray, ref: dict) -> float:
     return max(float(np.abs(gpu_out[b, h].astype(np.float64) - o).max()) for (b, h), o in ref.items())
 
 
+def int8_codes(pool_bytes: np.ndarray) -> np.ndarray:
+    """INT8 codes (the oracle's c in [-128, 127]) from stored bytes u = c + 128."""
+    return (pool_bytes.astype(np.int16) - 128).astype(np.int8)
+
+
 def pools(ld):
     c = ld.cache
     return (c.k_pages.cpu().numpy(), c.v_pages.cpu().numpy(), c.kv_sz.cpu().numpy())
@@ -187,7 +192,7 @@ def check_per_token_codes(ld):
         L = int(ld.lens[b])
         for x, pool, col in ((ld.seqs[b].k, kp, 0), (ld.seqs[b].v, vp, 2)):
             c, s, z = oracle.quantize_per_token(x)
-            assert np.array_equal(gather(pool, ld.bt[b], L, ps), c)
+            assert np.array_equal(int8_codes(gather(pool, ld.bt[b], L, ps)), c)
             g = gather(sz, ld.bt[b], L, ps)             # [L][Hkv][4]
             assert np.array_equal(g[:, :, col].view(np.uint32), s.view(np.uint32))
             assert np.array_equal(g[:, :, col + 1].view(np.uint32), z.view(np.uint32))
@@ -200,7 +205,7 @@ def check_per_group_codes(ld):
         L = int(ld.lens[b])
         for x, pool, col in ((ld.seqs[b].k, kp, 0), (ld.seqs[b].v, vp, 2)):
             c, s, z = oracle.quantize_per_group(x)
-            assert np.array_equal(gather(pool, ld.bt[b], L, ps), c)
+            assert np.array_equal(int8_codes(gather(pool, ld.bt[b], L, ps)), c)
             ng = s.shape[0]
             t0 = np.arange(ng) * 64
             gs = sz[ld.bt[b][t0 // ps], :, (t0 % ps) // 64]   # [ng][Hkv][4]

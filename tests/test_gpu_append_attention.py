@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from helpers import TOL, bits_to_torch, gather, load_workload, queries_dev, set_knobs
+from helpers import TOL, bits_to_torch, gather, int8_codes, load_workload, queries_dev, set_knobs
 from oracle.quant import per_group_dequant, per_token_dequant
 
 pytestmark = pytest.mark.gpu
@@ -73,8 +73,8 @@ def test_append_attention_steps(monkeypatch, name, dt, quant, d, Hq, Hkv, ps, mm
             kc, ks, kz = oracle.quantize_per_token(K[b])
             vc, vs, vz = oracle.quantize_per_token(V[b])
             sz = gather(c.kv_sz.cpu().numpy(), ld.bt[b], L, ps)
-            assert np.array_equal(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps), kc)
-            assert np.array_equal(gather(c.v_pages.cpu().numpy(), ld.bt[b], L, ps), vc)
+            assert np.array_equal(int8_codes(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps)), kc)
+            assert np.array_equal(int8_codes(gather(c.v_pages.cpu().numpy(), ld.bt[b], L, ps)), vc)
             assert np.array_equal(sz[:, :, 0].view(np.uint32), ks.view(np.uint32))
             assert np.array_equal(sz[:, :, 1].view(np.uint32), kz.view(np.uint32))
             assert np.array_equal(sz[:, :, 2].view(np.uint32), vs.view(np.uint32))
@@ -147,12 +147,12 @@ def test_append_attention_two_launch_caches(name, dt, quant, d, Hq, Hkv, ps, box
             assert np.array_equal(gather(kp, ld.bt[b], L, ps), Kb[b])
         elif quant == "per_token":
             kc, ks, kz = oracle.quantize_per_token(K[b])
-            assert np.array_equal(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps), kc)
+            assert np.array_equal(int8_codes(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps)), kc)
         else:
             kc, ks, kz = oracle.quantize_per_group(K[b])
             vc, vs, vz = oracle.quantize_per_group(V[b])
-            assert np.array_equal(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps), kc)
-            assert np.array_equal(gather(c.v_pages.cpu().numpy(), ld.bt[b], L, ps), vc)
+            assert np.array_equal(int8_codes(gather(c.k_pages.cpu().numpy(), ld.bt[b], L, ps)), kc)
+            assert np.array_equal(int8_codes(gather(c.v_pages.cpu().numpy(), ld.bt[b], L, ps)), vc)
         if boxes:
             sd = synth.SeqData(k_bits=Kb[b], v_bits=Vb[b], k=K[b], v=V[b])
             mn, mx = oracle.page_bounding_boxes(oracle_bbox_keys(w, sd), ps)
