@@ -332,6 +332,11 @@ __device__ __forceinline__ uint32_t u8x2_to_h2c(uint32_t w, uint32_t sel) {
   return r;
 }
 
+// Two stored INT8 bytes u of a word (sel as above) as the fp16 pair 1024 + u.
+__device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel) {
+  return __byte_perm(w, 0x64646464u, sel);
+}
+
 // Two 4-bit codes of a word as centred fp16 (u - 8): the nibbles at bit
 // offsets 4s and 4s + 16 (mask 0x000F000F after the shift) placed in the low
 // mantissa bits of fp16 1024 (0x6400), minus 1032, exact.
@@ -1116,9 +1121,12 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // the MMA accumulator drifts with the number of chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
   constexpr bool U4 = (KV == KV_U4T);
-  // codes enter q.K^T as u - KCEN_K (4-bit: 16 + u) and P.V as u - KCEN_V
-  // (centred); the scale and zero-point terms take the rest
-  constexpr float KCEN_K = U4 ? -16.f : 128.f;
+  // codes enter q.K^T as u - KCEN_K (INT8: 1024 + u, 4-bit: 16 + u) and P.V as
+  // u - KCEN_V (centred); the scale and zero-point terms take the rest. The
+  // offset in q.K^T is common to every token of a head, so it only shifts the
+  // products the tensor cores sum; P.V stays centred because a weight that
+  // loses bits there would carry the offset into the output.
+  constexpr float KCEN_K = U4 ? -16.f : -1024.f;
   constexpr float KCEN_V = U4 ? 8.f : 128.f;
   constexpr int ESZ = Geo::ESZ;
   constexpr int E = 16 / ESZ;                 // channels per 16-byte block
@@ -1310,10 +1318,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
           if constexpr (ESZ == 1) {
             const uint32_t w0 = word_of(k0[m], wi);
             const uint32_t w1 = word_of(k1[m], wi);
-            a0 = u8x2_to_h2c(w0, 0x4140u);
-            a2 = u8x2_to_h2c(w0, 0x4342u);
-            a1 = u8x2_to_h2c(w1, 0x4140u);
-            a3 = u8x2_to_h2c(w1, 0x4342u);
+            a0 = u8x2_to_h2(w0, 0x4140u);
+            a2 = u8x2_to_h2(w0, 0x4342u);
+            a1 = u8x2_to_h2(w1, 0x4140u);
+            a3 = u8x2_to_h2(w1, 0x4342u);
           } else {
             a0 = word_of(k0[m], wi);
             a2 = word_of(k0[m], wi + 1);
@@ -1343,7 +1351,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
         vs0 = z0.z; vz0 = fmaf(KCEN_V, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN_V, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
         const float4 z = *reinterpret_cast<const float4*>(sz);
-        const float kc = fmaf(KCEN_K, z.x, z.y);   // centred codes, as for per-token scales
+        const float kc = fmaf(KCEN_K, z.x, z.y);   // as for per-token scales
         sc[0] = fmaf(z.x, sc[0], kc * qs[0]);
         sc[1] = fmaf(z.x, sc[1], kc * qs[1]);
         sc[2] = fmaf(z.x, sc[2], kc * qs[0]);
