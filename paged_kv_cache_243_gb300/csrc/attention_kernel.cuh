@@ -1102,11 +1102,10 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // 4t .. 4t + 3 (swizzled tiles: 2t, 2t + 1, 2t + 8, 2t + 9) of the chunk
   // enter the product's k slots. With swizzled tiles every quarter-warp of a
   // fragment load touches 8 distinct 16-byte blocks: no bank conflicts.
-  // INT8 K codes enter q.K^T centred (c = u - 128, exact in fp16). 4-bit K
-  // codes enter offset, as 16 + u (exact in fp16, one shift and one logic op
-  // per pair, no subtraction); the offset's product (16 x the q sum) leaves
-  // with the zero-point term, and the accumulated magnitude stays within a
-  // few times that of centred codes.
+  // K codes enter q.K^T offset, INT8 as 1024 + u (one byte permute per pair)
+  // and 4-bit as 16 + u (one shift and one logic op per pair), both exact in
+  // fp16 and without a subtraction; the offset's product (the offset x the q
+  // sum) is common to a head's tokens and leaves with the zero-point term.
   // 4-bit codes (64-byte rows at D = 128, whose 16-byte fragment loads are
   // already free of conflicts): thread t reads block t of a K row, 32
   // channels; a register pairs channels c and c + 4 of one word (k slots
