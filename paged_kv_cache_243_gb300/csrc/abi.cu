@@ -50,6 +50,8 @@ struct Tuning {
   int comb_rg = 0;        // PKV_ATTN_COMB_RG: record groups of the combine (1, 2, 4 or 8)
   int mma_g1 = 0;         // PKV_ATTN_MMA_G1: tensor-core consumers for single query heads on
                           // fp16/bf16 caches: 0 never, 1 at head_dim 64, 2 at every head_dim
+  int self_fed = 1;       // PKV_ATTN_SELF: self-fed tensor-core blocks 0 never, 1 where the
+                          // plan below picks them, 2 for every early-start call
 };
 
 std::mutex g_tuning_mu;
@@ -64,6 +66,7 @@ void read_tuning_locked() {
   t.ctas_per_sm = env_int("PKV_ATTN_CTAS_PER_SM", 0);
   t.comb_rg = env_int("PKV_ATTN_COMB_RG", 0);
   t.mma_g1 = env_int("PKV_ATTN_MMA_G1", 0);
+  t.self_fed = env_int("PKV_ATTN_SELF", 1);
   g_tuning = t;
   g_tuning_read = true;
 }
@@ -188,13 +191,13 @@ const void* attn_combine(int D, int ge) {
   return nullptr;
 }
 
-const void* attn_kernel(int kind, int D, int ge, bool mma) {
+const void* attn_kernel(int kind, int D, int ge, bool mma, bool self_fed = false) {
   switch (kind) {
-    case KV_F16: return attn_kernel_f16(D, ge, mma);
-    case KV_BF16: return attn_kernel_bf16(D, ge, mma);
-    case KV_I8T: return attn_kernel_i8t(D, ge, mma);
-    case KV_U4T: return attn_kernel_u4t(D, ge, mma);
-    default: return attn_kernel_i8g(D, ge, mma);
+    case KV_F16: return attn_kernel_f16(D, ge, mma, self_fed);
+    case KV_BF16: return attn_kernel_bf16(D, ge, mma, self_fed);
+    case KV_I8T: return attn_kernel_i8t(D, ge, mma, self_fed);
+    case KV_U4T: return attn_kernel_u4t(D, ge, mma, self_fed);
+    default: return attn_kernel_i8g(D, ge, mma, self_fed);
   }
 }
 
@@ -222,6 +225,7 @@ struct AttnPlan {
   size_t smem = 0;
   size_t off_wrec = 0, ws_bytes = 0;
   int comb_groups = 1;
+  bool self_fed = false;   // the tensor-core kernel without a producer warp
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -280,7 +284,8 @@ pkv_status pool_tensor_map(const void* base, uint64_t rows, CUtensorMap& out) {
 // max_chunks > 0: an upper bound on the call's chunk count (from the block table's
 // width or the page lists' stride), used to give small calls fewer blocks.
 pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads, int sparse,
-                          int32_t num_splits, int q_dtype, AttnPlan& pl, long long max_chunks = 0) {
+                          int32_t num_splits, int q_dtype, AttnPlan& pl, long long max_chunks = 0,
+                          int fresh_rows = -1) {
   pkv_status st = check_cache(c, false);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -338,6 +343,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
       pkv_status r = prepare_kernel(fn, kAttnThreads, smem, nb);
       int cap = tn.ctas_per_sm;
       if (cap <= 0 && !mma && stage >= 8192) cap = 2;
+      if (cap <= 0 && mma) cap = 3;   // three per SM whichever tensor-core form runs
       if (cap > 0 && cap < nb) nb = cap;
       return r;
     };
@@ -389,6 +395,28 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
         best = cost;
         pl.comb_groups = rg;
       }
+    }
+    // Self-fed tensor-core blocks (no producer warp; three per SM, three warps
+    // per SM sub-partition) leave room for one 128-thread combine block per SM.
+    // The attention kernel then releases the combine at entry, its blocks wait
+    // beside the attention blocks, and where its grid has at most one block per
+    // SM (record group 1) the next call of a chain, released once every combine
+    // block is resident, streams while this call merges. The self-fed
+    // consumers stream ~5 % slower (their copies sit on their own path: W3
+    // 96.3 against 91.2 us when forced), which that overlap repays only on
+    // short calls: early-start calls with no fresh rows (an attention call
+    // after another; after an append, the next append waits for the merge
+    // anyway: W4's decode step 44.0 against 33.0 us when forced) of at most
+    // ~128 chunks per block (W4's attention chain: 26.4 against 29.6 us).
+    const void* self_fn = pl.mma && tn.self_fed ? attn_kernel(kind, c->head_dim, pl.ge, true, true) : nullptr;
+    const int ob1 = kCombineThreads;
+    const bool fits = units * ((outs + ob1 - 1) / ob1) <= di.sms;
+    const bool short_call = max_chunks > 0 && max_chunks <= 128LL * pl.ctas;
+    if (self_fn && num_splits == 0 &&
+        ((tn.self_fed == 1 && fresh_rows == 0 && fits && short_call) || (tn.self_fed == 2 && fresh_rows >= 0))) {
+      pl.self_fed = true;
+      pl.fn = self_fn;
+      if (fits) pl.comb_groups = 1;
     }
     const int forced_rg = tn.comb_rg;
     if (forced_rg == 1 || forced_rg == 2 || forced_rg == 4 || forced_rg == 8) pl.comb_groups = forced_rg;
@@ -469,12 +497,12 @@ pkv_status attention_impl(const pkv_cache* cache, int32_t batch, int32_t num_q_h
       (long long)batch * units_per_b *
       (sparse ? (long long)sel_stride * (cache->page_size / kChunk)
               : ((long long)max_pages * cache->page_size + kChunk - 1) / kChunk);
-  st = plan_attention(cache, batch, num_q_heads, mode, num_splits, q_dtype, pl, max_chunks);
+  st = plan_attention(cache, batch, num_q_heads, mode, num_splits, q_dtype, pl, max_chunks, fresh_rows);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < pl.ws_bytes)
     return PKV_ERR_WORKSPACE;
   int nb = 0;
-  st = prepare_kernel(pl.fn, kAttnThreads, pl.smem, nb);
+  st = prepare_kernel(pl.fn, attn_threads(pl.self_fed), pl.smem, nb);
   if (st != PKV_OK) return st;
 
   AttnParams p = {};
@@ -522,7 +550,7 @@ pkv_status attention_impl(const pkv_cache* cache, int32_t batch, int32_t num_q_h
   p.src_dtype = src_dtype;
   void* args[] = {&p};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(kAttnThreads), pl.smem, cs, args);
+  cudaError_t e = launch_pdl(pl.fn, dim3(pl.ctas), dim3(attn_threads(pl.self_fed)), pl.smem, cs, args);
   if (e == cudaSuccess) {
     const void* comb = attn_combine(cache->head_dim, pl.ge);
     const int outs = pl.ge * cache->head_dim;

@@ -6,7 +6,14 @@
 
 namespace pkv {
 
-const void* attn_kernel_bf16(int D, int GE, bool mma) {
+const void* attn_kernel_bf16(int D, int GE, bool mma, bool self_fed) {
+  if (self_fed) {   // tensor cores at head_dim 128, no producer warp
+    if (!mma || D != 128) return nullptr;
+    if (GE == 2) return reinterpret_cast<const void*>(&paged_attention_kernel<128, 2, KV_BF16, true, true>);
+    if (GE == 4) return reinterpret_cast<const void*>(&paged_attention_kernel<128, 4, KV_BF16, true, true>);
+    if (GE == 8) return reinterpret_cast<const void*>(&paged_attention_kernel<128, 8, KV_BF16, true, true>);
+    return nullptr;
+  }
 #define PKV_CASE(d, ge, tc) \
   if (D == d && GE == ge && mma == tc) \
     return reinterpret_cast<const void*>(&paged_attention_kernel<d, ge, KV_BF16, tc>);

@@ -52,6 +52,13 @@ namespace pkv {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+// Threads of a block. The self-fed tensor-core variant has no producer warp
+// (its consumer warps copy their own chunks), so three of its blocks, three
+// warps per SM sub-partition, leave room for a block of the combine beside
+// them.
+__host__ __device__ constexpr int attn_threads(bool self_fed) {
+  return self_fed ? kConsumerWarps * 32 : kAttnThreads;
+}
 // Small shared scratch: [8, 8 + warps) the unit prefix scan's warp totals.
 constexpr int kMiscInts = 32;
 constexpr int kQStageBytes = 2048;   // shared-memory copy of q for a block's first units (small: it must
@@ -482,10 +489,12 @@ __device__ __forceinline__ void append_token_row(const AttnParams& p, int u, int
 }
 
 // The tensor-core variant is held to 3 resident blocks per SM (<= 136 registers)
-// so that 12 consumer warps hide its per-chunk latency.
-template <int D, int GE, int KV, bool MMA>
-__global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
+// so that 12 consumer warps hide its per-chunk latency; the self-fed one
+// (SELF) to 128 registers.
+template <int D, int GE, int KV, bool MMA, bool SELF = false>
+__global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
     paged_attention_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(!SELF || MMA, "only the tensor-core consumers copy their own chunks");
   using Geo = AttnGeom<D, KV>;
   constexpr int QD = Geo::QD, PD = Geo::PD, KB = Geo::KB, SZB = Geo::SZB;
   // swizzled K/V tiles (tensor copies), scales in their own array
@@ -494,6 +503,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   constexpr int PBUF = AttnSmem<GE>::PBUF;
   constexpr int DUP = 8 / GE;  // lanes (per token) that hold the same head after the scatter
   constexpr int NW = kConsumerWarps;
+  constexpr int NT = attn_threads(SELF);
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.stages;
@@ -531,15 +541,20 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // promise; griddepcontrol.wait comes before the producer copies a chunk
   // holding fresh rows, before any other global write (the preceding work
   // may still read the output or the workspace), and in every block before
-  // it exits, so this grid never completes, or lets its dependents start,
-  // before the preceding one has completed.
+  // it exits, so this grid never completes before the preceding one has.
+  // The producer warp lets dependents start only after that wait. The
+  // self-fed variant lets them start at once: its dependent is this call's
+  // combine, which reads only the call's inputs before its own wait for this
+  // grid, and whose blocks then wait beside this grid's.
   const bool early = p.fresh_rows >= 0;
   if (!early) {
     pdl_wait();
     pdl_launch_dependents();
+  } else if constexpr (SELF) {
+    pdl_launch_dependents();
   }
   // ---- sequence lengths (clamped to the block table) and unit chunk counts
-  for (int b = tid; b < p.batch; b += kAttnThreads) {
+  for (int b = tid; b < p.batch; b += NT) {
     int L = p.seq_lens[b];
     int cap = p.max_pages * ps;
     if (L < 0 || L > cap) {
@@ -556,7 +571,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   fence_mbar_init();
   __syncthreads();
 
-  const int per = (U + kAttnThreads - 1) / kAttnThreads;
+  const int per = (U + NT - 1) / NT;
   const int ua0 = min(U, tid * per), ua1 = min(U, ua0 + per);
   int my_sum = 0;
   for (int u = ua0; u < ua1; ++u) {
@@ -600,7 +615,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       prefix[u] = run;
       run += n;
     }
-    if (tid == kAttnThreads - 1) prefix[U] = wpre + incl;
+    if (tid == NT - 1) prefix[U] = wpre + incl;
   }
   __syncthreads();
 
@@ -616,7 +631,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
   // chunks, else in its merge phase (after its wait in early mode)
   if (blockIdx.x == 0 && lo >= hi) {
     if (early) pdl_wait();
-    for (int u = tid; u <= U; u += kAttnThreads) p.ws_prefix[u] = prefix[u];
+    for (int u = tid; u <= U; u += NT) p.ws_prefix[u] = prefix[u];
   }
   // ---- units without any chunk produce zeros (block u mod N writes them)
   if (warp < NW) {
@@ -634,78 +649,96 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
     return;
   }
 
+  // ---- chunk lookups: chunk x of the block's range -> unit, table entries,
+  // addresses (the producer warp's, or each self-fed consumer warp's)
+  const uint64_t pol = policy_evict_first();
+  const int cpp = ps / kChunk;
+  // raw lookup of chunk x: unit, chunk-in-unit, and the loaded table entries
+  // (l2: the sparse second-level entry was loaded by lookup2)
+  struct Raw {
+    int u, k, sp, phys, l2;
+  };
+  auto fetch = [&](int x, Raw& r) {   // issues the global loads
+    r.u = -1; r.k = 0; r.sp = 0; r.phys = -1; r.l2 = 0;
+    if (x >= hi) return;
+    r.u = find_unit(prefix, U, x);
+    r.k = x - prefix[r.u];
+    const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
+    if (!sparse) {
+      const int lp = (r.k * kChunk) / ps;
+      if (r.k * kChunk < lens[b]) r.phys = p.block_table[(size_t)b * p.max_pages + lp];
+    } else {
+      const size_t row = (size_t)b * p.units_per_b + hu;
+      if (early && r.k / cpp >= min(max(p.sel_count[row], 0), p.sel_stride)) {
+        r.sp = kSkipSelected;   // past the unit's list: no page, no error
+        return;
+      }
+      r.sp = p.sel_pages[row * p.sel_stride + r.k / cpp];
+    }
+  };
+  auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
+    ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
+    ci.nvalid = 0; ci.valid = 0; ci.fresh = 0; ci.last = 0; ci.row = 0;
+    if (r.u < 0) return;
+    const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
+    const int L = lens[b];
+    int t0, g, phys = r.phys;
+    if (!sparse) {
+      t0 = r.k * kChunk;
+      g = hu;
+    } else {
+      if (r.sp == kSkipSelected) return;
+      g = p.unit_is_q ? hu / p.group : hu;
+      if (r.sp < 0 || (long long)r.sp * ps >= L) {
+        flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
+        return;
+      }
+      t0 = r.sp * ps + (r.k % cpp) * kChunk;
+      if (t0 < L) phys = r.l2 ? r.phys : p.block_table[(size_t)b * p.max_pages + t0 / ps];
+    }
+    const int nv = min(kChunk, L - t0);
+    if (nv <= 0) return;
+    if (phys < 0 || phys >= p.num_pages) {
+      flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
+      return;
+    }
+    const int off = t0 % ps;
+    const size_t row0 = ((size_t)phys * p.num_kv_heads + g) * ps + off;
+    ci.k = p.k_pages + row0 * Geo::ROW;
+    ci.v = p.v_pages + row0 * Geo::ROW;
+    ci.row = (int)row0;   // the host keeps pool rows below 2^31 for tensor copies
+    if constexpr (Geo::PTOK) ci.sz = p.kv_sz + row0 * 4;
+    if constexpr (KV == KV_I8G)
+      ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
+    ci.nvalid = nv;
+    ci.valid = 1;
+    ci.last = !sparse && t0 + nv == L;
+    if (early) {
+      int bnd = L - p.fresh_rows;   // first row the preceding kernel may write
+      if constexpr (KV == KV_I8G) bnd = bnd <= 0 ? 0 : bnd / 64 * 64;
+      ci.fresh = t0 + nv > bnd;
+    }
+  };
+  // sparse: the table entry of the selected page (issues the dependent load
+  // ahead of resolve; an out-of-range page is left to resolve to report)
+  auto lookup2 = [&](Raw& r) {
+    if (!sparse || r.u < 0 || r.sp == kSkipSelected) return;
+    const int b = r.u / p.units_per_b;
+    const int L = lens[b];
+    if (r.sp < 0 || (long long)r.sp * ps >= L) return;
+    const int t0 = r.sp * ps + (r.k % cpp) * kChunk;
+    if (t0 < L) {
+      r.phys = p.block_table[(size_t)b * p.max_pages + t0 / ps];
+      r.l2 = 1;
+    }
+  };
+
+  if constexpr (!SELF) {
   if (warp == NW) {
     // ================================================================ producer
     // Lane l resolves chunk base + l of each batch of 32. The table entries of
     // batch k + 1 are loaded right after batch k's copies are issued, so their
     // latency overlaps the streaming of batch k.
-    const uint64_t pol = policy_evict_first();
-    const int cpp = ps / kChunk;
-    // raw lookup of chunk x: unit, chunk-in-unit, and the loaded table entries
-    struct Raw {
-      int u, k, sp, phys;
-    };
-    auto fetch = [&](int x, Raw& r) {   // issues the global loads
-      r.u = -1; r.k = 0; r.sp = 0; r.phys = -1;
-      if (x >= hi) return;
-      r.u = find_unit(prefix, U, x);
-      r.k = x - prefix[r.u];
-      const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
-      if (!sparse) {
-        const int lp = (r.k * kChunk) / ps;
-        if (r.k * kChunk < lens[b]) r.phys = p.block_table[(size_t)b * p.max_pages + lp];
-      } else {
-        const size_t row = (size_t)b * p.units_per_b + hu;
-        if (early && r.k / cpp >= min(max(p.sel_count[row], 0), p.sel_stride)) {
-          r.sp = kSkipSelected;   // past the unit's list: no page, no error
-          return;
-        }
-        r.sp = p.sel_pages[row * p.sel_stride + r.k / cpp];
-      }
-    };
-    auto resolve = [&](const Raw& r, ChunkInfo& ci) {   // consumes the loads
-      ci.k = nullptr; ci.v = nullptr; ci.sz = nullptr; ci.u = r.u < 0 ? 0 : r.u;
-      ci.nvalid = 0; ci.valid = 0; ci.fresh = 0; ci.last = 0; ci.row = 0;
-      if (r.u < 0) return;
-      const int b = r.u / p.units_per_b, hu = r.u - b * p.units_per_b;
-      const int L = lens[b];
-      int t0, g, phys = r.phys;
-      if (!sparse) {
-        t0 = r.k * kChunk;
-        g = hu;
-      } else {
-        if (r.sp == kSkipSelected) return;
-        g = p.unit_is_q ? hu / p.group : hu;
-        if (r.sp < 0 || (long long)r.sp * ps >= L) {
-          flag_status(p.dev_status, PKV_DEV_BAD_SELECTED);
-          return;
-        }
-        t0 = r.sp * ps + (r.k % cpp) * kChunk;
-        if (t0 < L) phys = p.block_table[(size_t)b * p.max_pages + t0 / ps];
-      }
-      const int nv = min(kChunk, L - t0);
-      if (nv <= 0) return;
-      if (phys < 0 || phys >= p.num_pages) {
-        flag_status(p.dev_status, PKV_DEV_BAD_PAGE);
-        return;
-      }
-      const int off = t0 % ps;
-      const size_t row0 = ((size_t)phys * p.num_kv_heads + g) * ps + off;
-      ci.k = p.k_pages + row0 * Geo::ROW;
-      ci.v = p.v_pages + row0 * Geo::ROW;
-      ci.row = (int)row0;   // the host keeps pool rows below 2^31 for tensor copies
-      if constexpr (Geo::PTOK) ci.sz = p.kv_sz + row0 * 4;
-      if constexpr (KV == KV_I8G)
-        ci.sz = p.kv_sz + (((size_t)phys * p.num_kv_heads + g) * (ps / 64) + off / 64) * 4;
-      ci.nvalid = nv;
-      ci.valid = 1;
-      ci.last = !sparse && t0 + nv == L;
-      if (early) {
-        int bnd = L - p.fresh_rows;   // first row the preceding kernel may write
-        if constexpr (KV == KV_I8G) bnd = bnd <= 0 ? 0 : bnd / 64 * 64;
-        ci.fresh = t0 + nv > bnd;
-      }
-    };
     // Copies are issued by up to S lanes at once (one per ring stage): a single
     // issuing thread serialises the bulk-copy instructions and cannot keep the
     // ring full. Lane l owns chunk nbase + l of the batch; it waits for its
@@ -803,6 +836,7 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       }
     }
     return;
+  }
   }
 
   // q of the block's first units, staged in shared memory by the consumer
@@ -1248,13 +1282,114 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
     zs2[0] = zs2[1] = 0.f;
   };
 
+  // ---- self-fed (SELF): the warp copies its own chunks. Block chunk
+  // n = warp + NW j (the warp's chunk j) sits in stage n mod S at phase n / S;
+  // S is a multiple of NW, so the warp's stages are its own. Its first S / NW
+  // chunks are copied up front, and chunk j + S / NW into chunk j's stage once
+  // the warp is done with chunk j. Lane l holds the lookups of the warp's
+  // chunk 32 cb + l (resolved) and 32 (cb + 1) + l (fetched; the second-level
+  // entries of sparse calls are loaded half way through batch cb).
+  const int DW = S / NW;
+  const int span = hi - lo;
+  const int nown = span > warp ? (span - warp + NW - 1) / NW : 0;
+  unsigned long long a_row = 0;   // pool row of the warp's chunk 32 cb + lane
+  int a_u = 0, a_fl = 0;           // its unit; nvalid | valid << 5 | fresh << 6
+  Raw rb;
+  int cb = 0;
+  bool rb_l2 = false;
+  bool waited = !early;
+  auto own_x = [&](int j) { return j < nown ? lo + warp + NW * j : hi; };
+  auto take_batch = [&](const Raw& r) {
+    ChunkInfo ci;
+    resolve(r, ci);
+    a_row = ci.valid ? (unsigned long long)((ci.k - p.k_pages) / Geo::ROW) : 0ull;
+    a_u = ci.u;
+    a_fl = ci.nvalid | (ci.valid << 5) | (ci.fresh << 6);
+    if constexpr (KV != KV_I8G) {
+      // the new token of each unit ending in the batch (fused append), written
+      // by the warp before the chunk holding it is copied; with early start
+      // the caller promises that the work still running leaves these rows alone
+      unsigned todo = p.k_new ? __ballot_sync(0xffffffffu, ci.valid && ci.last) : 0u;
+      if (todo) {
+        while (todo) {
+          const int src = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const unsigned long long pk = __shfl_sync(0xffffffffu, (unsigned long long)ci.k, src);
+          const unsigned long long pv = __shfl_sync(0xffffffffu, (unsigned long long)ci.v, src);
+          const unsigned long long pz = __shfl_sync(0xffffffffu, (unsigned long long)ci.sz, src);
+          append_token_row<D, KV>(p, __shfl_sync(0xffffffffu, ci.u, src),
+                                  __shfl_sync(0xffffffffu, ci.nvalid, src) - 1,
+                                  reinterpret_cast<uint8_t*>(pk), reinterpret_cast<uint8_t*>(pv),
+                                  reinterpret_cast<float*>(pz), lane);
+        }
+        __syncwarp();
+        // written through the generic proxy, copied through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+    }
+  };
+  // copy the warp's chunk j into its stage s (warp-uniform; the warp has used
+  // every value it read from the stage's previous chunk)
+  auto issue = [&](int j, int s) {
+    if ((j >> 5) != cb) {
+      if (!rb_l2) lookup2(rb);
+      take_batch(rb);
+      cb = j >> 5;
+      fetch(own_x(32 * (cb + 1) + lane), rb);
+      rb_l2 = false;
+    } else if (!rb_l2 && (j & 31) >= 16) {
+      lookup2(rb);
+      rb_l2 = true;
+    }
+    // the lane holding chunk j's lookups issues its copies
+    if (lane == (j & 31)) {
+      const unsigned long long row = a_row;
+      const int u = a_u, fl = a_fl;
+      if (((fl >> 6) & 1) && !waited) {   // fresh rows: the preceding grid may still write them
+        pdl_wait();
+        waited = true;
+      }
+      hdr[s] = make_int4(u, fl & 31, (fl >> 5) & 1, 0);
+      const uint32_t fb = smem_u32(&full[s]);
+      if ((fl >> 5) & 1) {
+        uint8_t* st = ring + (size_t)s * STAGE;
+        const float* szp = nullptr;
+        if constexpr (Geo::PTOK) szp = p.kv_sz + row * 4;
+        if constexpr (KV == KV_I8G) szp = p.kv_sz + (row / 64) * 4;   // page_size is a multiple of 64
+        mbar_arrive_expect_tx(fb, 2 * KB + SZB);
+        if constexpr (SWZ) {
+          tma_load_2d(smem_u32(st), &p.tmap_k, 0, (int)row, fb, pol);
+          tma_load_2d(smem_u32(st + KB), &p.tmap_v, 0, (int)row, fb, pol);
+          bulk_g2s(smem_u32(szring + (size_t)s * SZB), szp, SZB, fb, pol);
+        } else {
+          bulk_g2s(smem_u32(st), p.k_pages + row * Geo::ROW, KB, fb, pol);
+          bulk_g2s(smem_u32(st + KB), p.v_pages + row * Geo::ROW, KB, fb, pol);
+          if constexpr (SZB > 0) bulk_g2s(smem_u32(st + 2 * KB), szp, SZB, fb, pol);
+        }
+      } else {
+        mbar_arrive(fb);
+      }
+    }
+  };
+  if constexpr (SELF) {
+    Raw r0;
+    fetch(own_x(lane), r0);
+    lookup2(r0);
+    take_batch(r0);
+    fetch(own_x(32 + lane), rb);
+    for (int j = 0; j < DW && j < nown; ++j) issue(j, warp + NW * j);
+  }
+
   bool abort = false;
+  int jstop = 0;   // self-fed: the chunk whose wait gave up
   // chunk n of the block's range sits in stage n mod S at phase n / S; both
   // are stepped, not divided (S is a multiple of NW, so s wraps exactly)
-  for (int n = warp, s = warp, use = 0; lo + n < hi; n += NW, s += NW, use += (s >= S), s -= (s >= S) ? S : 0) {
+  for (int j = 0, n = warp, s = warp, use = 0; lo + n < hi;
+       ++j, n += NW, s += NW, use += (s >= S), s -= (s >= S) ? S : 0) {
     if (!mbar_wait_bounded(smem_u32(&full[s]), use & 1)) {
       flag_status(p.dev_status, PKV_DEV_TIMEOUT);
       abort = true;
+      jstop = j;
       break;
     }
     const int4 h4 = hdr[s];
@@ -1542,7 +1677,18 @@ __global__ void __launch_bounds__(kAttnThreads, MMA ? 3 : 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    if constexpr (SELF) {
+      if (j + DW < nown) issue(j + DW, s);
+    } else {
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+  }
+  if constexpr (SELF) {
+    if (abort) {   // let the copies still in flight land before the block exits
+      for (int j = jstop; j < nown && j < jstop + DW; ++j) {
+        if (!mbar_wait_bounded(smem_u32(&full[warp + NW * (j % DW)]), (j / DW) & 1)) break;
+      }
+    }
   }
   if (!abort) {
     if (u_cur >= 0 && u_cur != ub) {

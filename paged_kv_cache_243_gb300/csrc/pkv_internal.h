@@ -43,12 +43,13 @@ pkv_status launch_append(const AppendParams& p, cudaStream_t st);
 pkv_status launch_topk(const TopkParams& p, cudaStream_t st);
 
 // Attention kernels, one getter per KV kind (each in its own translation unit).
-// mma: the tensor-core variant (query-head groups of 2, 4 or 8).
-const void* attn_kernel_f16(int D, int GE, bool mma);
-const void* attn_kernel_bf16(int D, int GE, bool mma);
-const void* attn_kernel_i8t(int D, int GE, bool mma);
-const void* attn_kernel_i8g(int D, int GE, bool mma);
-const void* attn_kernel_u4t(int D, int GE, bool mma);
+// mma: the tensor-core variant (query-head groups of 2, 4 or 8); self_fed:
+// its form without a producer warp (head_dim 128; NULL otherwise).
+const void* attn_kernel_f16(int D, int GE, bool mma, bool self_fed);
+const void* attn_kernel_bf16(int D, int GE, bool mma, bool self_fed);
+const void* attn_kernel_i8t(int D, int GE, bool mma, bool self_fed);
+const void* attn_kernel_i8g(int D, int GE, bool mma, bool self_fed);
+const void* attn_kernel_u4t(int D, int GE, bool mma, bool self_fed);
 
 // Bytes of one shared-memory stage (a 16-token chunk of K and V plus its INT8
 // scales), by KV kind and head_dim; swz: the swizzled tensor-copy staging.
