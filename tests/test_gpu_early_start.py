@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from helpers import TOL, bits_to_torch, load_workload, oracle_dense, queries_dev
+from helpers import TOL, bits_to_torch, load_workload, oracle_dense, queries_dev, set_knobs
 from oracle.quant import per_group_dequant, per_token_dequant
 
 pytestmark = pytest.mark.gpu
@@ -40,6 +40,19 @@ CASES = [
 @pytest.mark.parametrize("splits", [0, 3])
 @pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps", CASES)
 def test_append_then_attention_overlapped(name, dt, quant, d, Hq, Hkv, ps, splits):
+    _append_then_attention(name, dt, quant, d, Hq, Hkv, ps, splits)
+
+
+@pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps", [c for c in CASES if c[3] == 128 and c[4] > c[5]])
+def test_self_fed_blocks_overlapped(monkeypatch, name, dt, quant, d, Hq, Hkv, ps):
+    # the tensor-core blocks without a producer warp (each consumer warp copies
+    # its own chunks, the combine released at entry), forced for every
+    # early-start call; by default they serve short chains without fresh rows
+    set_knobs(monkeypatch, PKV_ATTN_SELF=2)
+    _append_then_attention(name, dt, quant, d, Hq, Hkv, ps, 0)
+
+
+def _append_then_attention(name, dt, quant, d, Hq, Hkv, ps, splits):
     w = synth.Workload(name="early-" + name, seed=610 + d + Hq + ps, batch=3, layers=1,
                        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps, dtype=dt,
                        quant=quant, seq_len=None, seq_len_range=(1, 300),
@@ -112,6 +125,19 @@ FUSED_CASES = [
 @pytest.mark.parametrize("layers,fresh", [(2, 0), (1, 2)])
 @pytest.mark.parametrize("name,dt,quant,d,Hq,Hkv,ps", FUSED_CASES)
 def test_fused_steps_enqueued_back_to_back(name, dt, quant, d, Hq, Hkv, ps, layers, fresh):
+    _fused_steps(name, dt, quant, d, Hq, Hkv, ps, layers, fresh)
+
+
+@pytest.mark.parametrize("layers,fresh", [(2, 0), (1, 2)])
+def test_self_fed_fused_steps(monkeypatch, layers, fresh):
+    # one-call steps on GQA per-token INT8 with the self-fed tensor-core blocks
+    # forced: each consumer warp writes the new token of the units ending in
+    # its lookups before copying their chunks
+    set_knobs(monkeypatch, PKV_ATTN_SELF=2)
+    _fused_steps("i8-token-gqa", "f16", "per_token", 128, 16, 4, 16, layers, fresh)
+
+
+def _fused_steps(name, dt, quant, d, Hq, Hkv, ps, layers, fresh):
     # decode steps of one-call append + attention, all enqueued before any
     # synchronisation, so each call may start while the previous call's kernels
     # still run. Two layers: the previous call works on the other cache and
