@@ -412,7 +412,7 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     const int ob1 = kCombineThreads;
     const bool fits = units * ((outs + ob1 - 1) / ob1) <= di.sms;
     const bool short_call = max_chunks > 0 && max_chunks <= 128LL * pl.ctas;
-    if (self_fn && num_splits == 0 &&
+    if (self_fn && num_splits == 0 && pl.units < (1 << 24) &&
         ((tn.self_fed == 1 && fresh_rows == 0 && fits && short_call) || (tn.self_fed == 2 && fresh_rows >= 0))) {
       pl.self_fed = true;
       pl.fn = self_fn;

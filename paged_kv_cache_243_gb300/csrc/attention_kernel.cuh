@@ -45,6 +45,8 @@
 // shared memory.
 #pragma once
 
+#include <type_traits>
+
 #include "pkv_common.cuh"
 #include "quant.cuh"
 
@@ -1292,8 +1294,12 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   const int DW = S / NW;
   const int span = hi - lo;
   const int nown = span > warp ? (span - warp + NW - 1) / NW : 0;
-  unsigned long long a_row = 0;   // pool row of the warp's chunk 32 cb + lane
-  int a_u = 0, a_fl = 0;           // its unit; nvalid | valid << 5 | fresh << 6
+  // pool row of the warp's chunk 32 cb + lane (32 bits for tensor copies,
+  // whose rows the host keeps below 2^31), and its unit << 7 | fresh << 6 |
+  // valid << 5 | nvalid (units stay below 2^24)
+  using RowT = typename std::conditional<SWZ, int, unsigned long long>::type;
+  RowT a_row = 0;
+  int a_uf = 0;
   Raw rb;
   int cb = 0;
   bool rb_l2 = false;
@@ -1302,9 +1308,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   auto take_batch = [&](const Raw& r) {
     ChunkInfo ci;
     resolve(r, ci);
-    a_row = ci.valid ? (unsigned long long)((ci.k - p.k_pages) / Geo::ROW) : 0ull;
-    a_u = ci.u;
-    a_fl = ci.nvalid | (ci.valid << 5) | (ci.fresh << 6);
+    a_row = ci.valid ? (RowT)((ci.k - p.k_pages) / Geo::ROW) : (RowT)0;
+    a_uf = (ci.u << 7) | (ci.fresh << 6) | (ci.valid << 5) | ci.nvalid;
     if constexpr (KV != KV_I8G) {
       // the new token of each unit ending in the batch (fused append), written
       // by the warp before the chunk holding it is copied; with early start
@@ -1337,14 +1342,14 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
       cb = j >> 5;
       fetch(own_x(32 * (cb + 1) + lane), rb);
       rb_l2 = false;
-    } else if (!rb_l2 && (j & 31) >= 16) {
+    } else if (sparse && !rb_l2 && (j & 31) >= 16) {
       lookup2(rb);
       rb_l2 = true;
     }
     // the lane holding chunk j's lookups issues its copies
     if (lane == (j & 31)) {
-      const unsigned long long row = a_row;
-      const int u = a_u, fl = a_fl;
+      const RowT row = a_row;
+      const int u = a_uf >> 7, fl = a_uf & 127;
       if (((fl >> 6) & 1) && !waited) {   // fresh rows: the preceding grid may still write them
         pdl_wait();
         waited = true;
