@@ -1377,6 +1377,11 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
     }
   };
   if constexpr (SELF) {
+    // early sparse calls: the page lists are the preceding kernel's output
+    if (sparse && !waited) {
+      pdl_wait();
+      waited = true;
+    }
     Raw r0;
     fetch(own_x(lane), r0);
     lookup2(r0);

@@ -187,6 +187,19 @@ def _fused_steps(name, dt, quant, d, Hq, Hkv, ps, layers, fresh):
 @pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("none", 64, 8, 8, 16, 7), ("per_token", 128, 16, 4, 16, 5),
                                                      ("none", 128, 8, 2, 32, 3)])
 def test_sparse_attention_overlapping_the_scoring(group_mode, quant, d, Hq, Hkv, ps, top_k):
+    _sparse_after_scoring(group_mode, quant, d, Hq, Hkv, ps, top_k)
+
+
+@pytest.mark.parametrize("group_mode", [0, 1])
+@pytest.mark.parametrize("quant,d,Hq,Hkv,ps,top_k", [("per_token", 128, 16, 4, 16, 5), ("none", 128, 8, 2, 32, 3)])
+def test_self_fed_sparse_after_scoring(monkeypatch, group_mode, quant, d, Hq, Hkv, ps, top_k):
+    # the self-fed tensor-core blocks read the page lists in their own warps'
+    # lookups, which must wait for the scoring that writes them
+    set_knobs(monkeypatch, PKV_ATTN_SELF=2)
+    _sparse_after_scoring(group_mode, quant, d, Hq, Hkv, ps, top_k)
+
+
+def _sparse_after_scoring(group_mode, quant, d, Hq, Hkv, ps, top_k):
     # sparse attention right after the page scoring that writes its lists,
     # started early (fresh_rows = 0): it plans from the lengths and reads the
     # lists only after waiting; results equal the call that waits up front
