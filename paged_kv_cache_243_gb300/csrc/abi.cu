@@ -407,13 +407,17 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     // short calls: early-start calls with no fresh rows (an attention call
     // after another; after an append, the next append waits for the merge
     // anyway: W4's decode step 44.0 against 33.0 us when forced) of at most
-    // ~128 chunks per block (W4's attention chain: 26.4 against 29.6 us).
+    // ~128 chunks per block (W4's attention chain: 26.4 against 29.6 us), and
+    // dense: sparse calls resolve two table levels per chunk in the consumer
+    // warps (W6's sparse attention chain 28.6 against 27.3 us, with a combine
+    // of two outputs per thread so that its grid fitted beside them).
     const void* self_fn = pl.mma && tn.self_fed ? attn_kernel(kind, c->head_dim, pl.ge, true, true) : nullptr;
     const int ob1 = kCombineThreads;
     const bool fits = units * ((outs + ob1 - 1) / ob1) <= di.sms;
     const bool short_call = max_chunks > 0 && max_chunks <= 128LL * pl.ctas;
     if (self_fn && num_splits == 0 && pl.units < (1 << 24) &&
-        ((tn.self_fed == 1 && fresh_rows == 0 && fits && short_call) || (tn.self_fed == 2 && fresh_rows >= 0))) {
+        ((tn.self_fed == 1 && sparse == 0 && fresh_rows == 0 && fits && short_call) ||
+         (tn.self_fed == 2 && fresh_rows >= 0))) {
       pl.self_fed = true;
       pl.fn = self_fn;
       if (fits) pl.comb_groups = 1;
