@@ -29,6 +29,12 @@
 // not see). The block's last unit is the exception: after the stream the four
 // warps' states meet in shared memory and the block writes one merged record.
 //
+// Self-fed tensor-core blocks (SELF) have no producer warp: consumer warp w
+// reads the chunks w, w + 4, ... from its own stages (S is a multiple of 4),
+// so it resolves their lookups and issues their copies itself. Three of these
+// 128-thread blocks per SM leave room for a combine block beside them; the
+// host uses them for short chains of attention calls (see its plan).
+//
 // Merge [TinyServe page, section 3.1 phase 4]: attn_combine_kernel, the next
 // launch on the stream, folds for every unit the records of all blocks whose
 // ranges overlap it:
