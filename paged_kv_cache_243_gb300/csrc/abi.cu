@@ -402,12 +402,12 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
     // beside the attention blocks, and where its grid has at most one block per
     // SM (record group 1) the next call of a chain, released once every combine
     // block is resident, streams while this call merges. The self-fed
-    // consumers stream ~5 % slower (their copies sit on their own path: W3
-    // 96.3 against 91.2 us when forced), which that overlap repays only on
+    // consumers stream ~4 % slower (their copies sit on their own path: W3
+    // 94.9 against 91.5 us when forced), which that overlap repays only on
     // short calls: early-start calls with no fresh rows (an attention call
     // after another; after an append, the next append waits for the merge
-    // anyway: W4's decode step 44.0 against 33.0 us when forced) of at most
-    // ~128 chunks per block (W4's attention chain: 26.4 against 29.6 us), and
+    // anyway: W4's decode step 41.2 against 33.0 us when forced) of at most
+    // ~128 chunks per block (W4's attention chain: 24.6 against 29.6 us), and
     // dense: sparse calls resolve two table levels per chunk in the consumer
     // warps (W6's sparse attention chain 28.6 against 27.3 us, with a combine
     // of two outputs per thread so that its grid fitted beside them).

@@ -1295,8 +1295,10 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // S is a multiple of NW, so the warp's stages are its own. Its first S / NW
   // chunks are copied up front, and chunk j + S / NW into chunk j's stage once
   // the warp is done with chunk j. Lane l holds the lookups of the warp's
-  // chunk 32 cb + l (resolved) and 32 (cb + 1) + l (fetched; the second-level
-  // entries of sparse calls are loaded half way through batch cb).
+  // chunk 32 cb + l. The next batch is looked up when the first of its chunks
+  // is copied: the host plans these blocks for calls of at most ~128 chunks
+  // per block, i.e. one batch per warp, so no lookups are held in flight
+  // across the stream.
   const int DW = S / NW;
   const int span = hi - lo;
   const int nown = span > warp ? (span - warp + NW - 1) / NW : 0;
@@ -1306,9 +1308,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   using RowT = typename std::conditional<SWZ, int, unsigned long long>::type;
   RowT a_row = 0;
   int a_uf = 0;
-  Raw rb;
   int cb = 0;
-  bool rb_l2 = false;
   bool waited = !early;
   auto own_x = [&](int j) { return j < nown ? lo + warp + NW * j : hi; };
   auto take_batch = [&](const Raw& r) {
@@ -1343,14 +1343,11 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // every value it read from the stage's previous chunk)
   auto issue = [&](int j, int s) {
     if ((j >> 5) != cb) {
-      if (!rb_l2) lookup2(rb);
-      take_batch(rb);
       cb = j >> 5;
-      fetch(own_x(32 * (cb + 1) + lane), rb);
-      rb_l2 = false;
-    } else if (sparse && !rb_l2 && (j & 31) >= 16) {
-      lookup2(rb);
-      rb_l2 = true;
+      Raw r;
+      fetch(own_x(32 * cb + lane), r);
+      lookup2(r);
+      take_batch(r);
     }
     // the lane holding chunk j's lookups issues its copies
     if (lane == (j & 31)) {
@@ -1392,7 +1389,6 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
     fetch(own_x(lane), r0);
     lookup2(r0);
     take_batch(r0);
-    fetch(own_x(32 + lane), rb);
     for (int j = 0; j < DW && j < nown; ++j) issue(j, warp + NW * j);
   }
 
