@@ -427,7 +427,20 @@ pkv_status plan_attention(const pkv_cache* c, int32_t batch, int32_t num_q_heads
          (tn.self_fed == 2 && fresh_rows >= 0))) {
       pl.self_fed = true;
       pl.fn = self_fn;
-      if (fits) pl.comb_groups = 1;
+      if (fits) {
+        // one record group while it folds a unit's records in at most 5 rounds
+        // (W4, 28 blocks per unit: 24.7 against 25.1 us with 2 groups); past
+        // that, the most groups whose grid still fits one block per SM (GQA
+        // INT8, B = 1, L = 16384, 57 blocks per unit: 14.6 us with 4 groups,
+        // 17.7 with 1, 16.6 with the producer-warp kernel)
+        pl.comb_groups = 1;
+        if ((rbar + 7) / 8 > 5) {
+          for (int rg = 2; rg <= 8; rg *= 2) {
+            const int ob = kCombineThreads / rg;
+            if (units * ((outs + ob - 1) / ob) <= di.sms) pl.comb_groups = rg;
+          }
+        }
+      }
     }
     const int forced_rg = tn.comb_rg;
     if (forced_rg == 1 || forced_rg == 2 || forced_rg == 4 || forced_rg == 8) pl.comb_groups = forced_rg;
