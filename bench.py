@@ -516,35 +516,38 @@ def extra_workloads(peak: float) -> Dict:
 
 
 def sweep(peak: float) -> Dict:
-    """Attention call time over batch x context for the Llama-2-7B head shapes (bf16,
-    32 q heads over 32 or 8 kv heads, d = 128, page 16): each point is a chain of
-    attention calls over distinct layers (early start, as in the bench's step), with
-    enough layers that the chain's K/V exceed L2; points whose layer exceeds 4.3 GB
-    are skipped."""
+    """Attention call time over batch x context for the Llama-2-7B head shapes (32 q
+    heads over 32 or 8 kv heads, d = 128, page 16): bf16 caches, then per-token INT8
+    caches with 8 kv heads (the GQA INT8 workload's quantisation and outliers). Each
+    point is a chain of attention calls over distinct layers (early start, as in the
+    bench's step), with enough layers that the chain's K/V exceed L2; points whose
+    layer exceeds 4.3 GB (bf16) or 2.2 GB (INT8) are skipped."""
     import dataclasses as dc
     import torch
-    base = synth.WORKLOADS["w2_llama7b_bf16"]
     res = []
-    for hkv in (32, 8):
+    families = [("bf16", synth.WORKLOADS["w2_llama7b_bf16"], hkv, 2 * 128 * 2, 4.3e9, 1.0e9, 32)
+                for hkv in (32, 8)]
+    families.append(("int8 per-token", synth.WORKLOADS["w3_gqa_int8_token"], 8, (128 + 16) * 2, 2.2e9, 0.6e9, 16))
+    for cache, base, hkv, bytes_per_token_head, max_layer, chain_bytes, max_layers in families:
         for B in (1, 4, 16, 64):
             for L in (1024, 4096, 16384, 32768):
-                per_layer = B * L * hkv * base.head_dim * 2 * 2
-                if per_layer > 4.3e9:
+                per_layer = B * L * hkv * bytes_per_token_head
+                if per_layer > max_layer:
                     continue
-                layers = int(min(32, max(2, math.ceil(1.0e9 / per_layer))))
-                w = dc.replace(base, name="sweep", batch=B, num_kv_heads=hkv, seq_len=L, layers=layers,
-                               pool_pages=None, description="")
+                layers = int(min(max_layers, max(2, math.ceil(chain_bytes / per_layer))))
+                w = dc.replace(base, name="sweep", batch=B, num_kv_heads=hkv, seq_len=L, seq_len_range=None,
+                               layers=layers, pool_pages=None, description="")
                 rep = Replica(w, w.seed, layers=layers)
                 ga, _ = rep.capture(append=False, attention=True)
                 ms = time_graph(ga, 20, 3) / layers
                 byts = algorithmic_bytes(w, rep.lens, append_tokens=0)["attention"]
-                res.append({"kv_heads": hkv, "batch": B, "seq_len": L, "layers": layers,
+                res.append({"cache": cache, "kv_heads": hkv, "batch": B, "seq_len": L, "layers": layers,
                             "attention_us": round(ms * 1e3, 2),
                             "gb_s": round(byts / (ms * 1e-3) / 1e9, 1),
                             "frac_of_hbm_peak": round(byts / (ms * 1e-3) / 1e9 / peak, 4)})
                 del rep, ga
                 torch.cuda.empty_cache()
-    return {"metric": "attention call GB/s over batch x context (bf16, 32 q heads, d 128, page 16)",
+    return {"metric": "attention call GB/s over batch x context (32 q heads, d 128, page 16)",
             "peak_gbs": peak, "points": res}
 
 
