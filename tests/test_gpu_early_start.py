@@ -303,3 +303,30 @@ def test_scoring_started_under_the_previous_attention(group_mode):
     for s in range(4):
         assert np.abs(res[True][0][s] - res[False][0][s]).max() <= 1e-6, s
     assert int(ld.status.item()) == 0
+
+
+@pytest.mark.parametrize("quant,dt", [("per_group64", "f16"), ("none", "bf16")])
+def test_self_fed_plan_on_a_long_context_chain(quant, dt):
+    # few units of long sequences (the shape for which the plan picks the
+    # self-fed blocks by itself: 16-128 chunks per block, a combine of at most
+    # one block per SM), attention calls enqueued back to back without fresh
+    # rows, each call's merge overlapping the next call
+    w = synth.Workload(name="early-self-chain", seed=720, batch=2, layers=1, num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=256, dtype=dt, quant=quant, seq_len=None,
+                       seq_len_range=(1, 8192), outlier_channels=4 if quant != "none" else 0,
+                       outlier_scale=15.0)
+    ld = load_workload(w, lens=np.array([8192, 7000], dtype=np.int32))
+    qs = [queries_dev(w, step=i) for i in range(3)]
+    outs = [torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device="cuda") for _ in qs]
+    torch.cuda.synchronize()
+    for i, (q, _) in enumerate(qs):
+        ld.cache.attention(q, ld.bt_dev, ld.lens_dev, sm_scale=w.sm_scale, out=outs[i],
+                           dev_status=ld.status, fresh_rows=0)
+    torch.cuda.synchronize()
+    tol = TOL["int8"] if quant != "none" else TOL[dt]
+    units = [(b, h) for b in range(w.batch) for h in range(0, w.num_q_heads, 3)]
+    for i, (_, qf) in enumerate(qs):
+        ref = oracle_dense(ld, qf, units)
+        got = outs[i].cpu().numpy()
+        assert max(float(np.abs(got[b, h] - o).max()) for (b, h), o in ref.items()) <= tol, i
+    assert int(ld.status.item()) == 0
