@@ -353,12 +353,19 @@ __device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel) {
 }
 
 // Two 4-bit codes of a word as centred fp16 (u - 8): the nibbles at bit
-// offsets 4s and 4s + 16 (mask 0x000F000F after the shift) placed in the low
-// mantissa bits of fp16 1024 (0x6400), minus 1032, exact.
+// offsets 4s and 4s + 16. At s = 1 they already sit in mantissa bits 4-7 of
+// fp16 64 (0x5400), i.e. 64 + u, so no shift is needed; other s are shifted
+// into the low mantissa bits of fp16 1024 (0x6400), 1024 + u. Then one exact
+// subtraction (72, or 1032).
 __device__ __forceinline__ uint32_t nib2h(uint32_t w, int s) {
-  const uint32_t h = ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
   uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+  if (s == 1) {
+    const uint32_t h = (w & 0x00F000F0u) | 0x54005400u;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x54805480u));
+  } else {
+    const uint32_t h = ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+  }
   return r;
 }
 
