@@ -1163,10 +1163,11 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // of one channel (a byte permute and a mask).
   // V codes enter P.V centred (u - 128, u - 8); see the P.V step for why.
   //
-  // Each chunk's P.V goes into a zeroed MMA accumulator, and the running state
-  // takes it with one fp32 fma (acc = acc * alpha + chunk): the tensor cores'
-  // fp32 accumulation is not IEEE round-to-nearest, and a running sum kept in
-  // the MMA accumulator drifts with the number of chunks a warp streams.
+  // The running P.V state is the MMA accumulator itself: a chunk first scales
+  // it by alpha (skipped, warp-wide, while no running maximum moved) and its
+  // products then accumulate into it. With centred V codes the tensor cores'
+  // fp32 accumulation (not IEEE round-to-nearest) adds no error that grows
+  // with the chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
   constexpr bool U4 = (KV == KV_U4T);
   // codes enter q.K^T as u - KCEN_K (INT8: 1024 + u, 4-bit: 16 + u) and P.V as
@@ -1580,8 +1581,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         bh0 = bl0;
         bh1 = bl1;
       }
-      // ---- P.V on the tensor cores, into a zeroed accumulator per m-tile;
-      // the running state takes it as acc = acc * alpha + chunk (fp32 fma)
+      // ---- P.V on the tensor cores, accumulated into the running state
       float a0s = al[0], a1s = al[1];
       if constexpr (GE == 1) {   // columns 0 and 1: hi and lo parts of head 0
         a1s = al[0];
@@ -1590,12 +1590,15 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         a0s = __shfl_sync(0xffffffffu, al[0], src);
         a1s = __shfl_sync(0xffffffffu, al[1], src);
       }
-      auto fold = [&](int mt, const float (&d)[4]) {
-        acc[mt][0] = fmaf(acc[mt][0], a0s, d[0]);
-        acc[mt][1] = fmaf(acc[mt][1], a1s, d[1]);
-        acc[mt][2] = fmaf(acc[mt][2], a0s, d[2]);
-        acc[mt][3] = fmaf(acc[mt][3], a1s, d[3]);
-      };
+      if (__any_sync(0xffffffffu, a0s != 1.f || a1s != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          acc[mt][0] *= a0s;
+          acc[mt][1] *= a1s;
+          acc[mt][2] *= a0s;
+          acc[mt][3] *= a1s;
+        }
+      }
       const uint8_t* vrow = st + KB;
       if constexpr (U4) {
         // 4-bit: channels [g DPT, (g+1) DPT) = DPT / 2 bytes of tokens vtok(0 .. 3)
@@ -1623,10 +1626,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
           const uint32_t a0 = nib2h(t01, 0), a1 = nib2h(t01, 1);
           const uint32_t a2 = nib2h(t23, 0), a3 = nib2h(t23, 1);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
-          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
-          fold(mt, d);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       } else if constexpr (ESZ == 1) {
         // int8: dims [g DPT, (g+1) DPT) of tokens vtok(0 .. 3) (DPT bytes per row)
@@ -1657,10 +1658,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
           const uint32_t a0 = u8x2_to_h2c(t01, 0x4140u), a1 = u8x2_to_h2c(t01, 0x4342u);
           const uint32_t a2 = u8x2_to_h2c(t23, 0x4140u), a3 = u8x2_to_h2c(t23, 0x4342u);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
-          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
-          fold(mt, d);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       } else {
         // fp16 / bf16: dims [g DPT, (g+1) DPT) of tokens vtok(0 .. 3) (2 DPT bytes per row)
@@ -1688,10 +1687,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           const uint32_t a1 = __byte_perm(rw[0][mt], rw[1][mt], 0x7632u);
           const uint32_t a2 = __byte_perm(rw[2][mt], rw[3][mt], 0x5410u);
           const uint32_t a3 = __byte_perm(rw[2][mt], rw[3][mt], 0x7632u);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816<BF>(d, a0, a1, a2, a3, bh0, bh1);
-          if constexpr (!PACK) mma16816<BF>(d, a0, a1, a2, a3, bl0, bl1);
-          fold(mt, d);
+          mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
+          if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       }
     }
