@@ -352,28 +352,22 @@ __device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel) {
   return __byte_perm(w, 0x64646464u, sel);
 }
 
-// Two 4-bit codes of a word as centred fp16 (u - 8): the nibbles at bit
-// offsets 4s and 4s + 16. At s = 1 they already sit in mantissa bits 4-7 of
-// fp16 64 (0x5400), i.e. 64 + u, so no shift is needed; other s are shifted
-// into the low mantissa bits of fp16 1024 (0x6400), 1024 + u. Then one exact
-// subtraction (72, or 1032).
-__device__ __forceinline__ uint32_t nib2h(uint32_t w, int s) {
-  uint32_t r;
-  if (s == 1) {
-    const uint32_t h = (w & 0x00F000F0u) | 0x54005400u;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x54805480u));
-  } else {
-    const uint32_t h = ((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
-  }
-  return r;
-}
+// 4-bit codes as fp16 subnormals. A code u masked into mantissa bits 0-3 of a
+// 16-bit half is the fp16 value u 2^-24; in bits 4-7 it is u 2^-20. Both are
+// exact, and the tensor cores and the half-precision fma take subnormal
+// operands as they are, so one mask per pair of codes makes an MMA operand.
+constexpr uint32_t kNibLo = 0x000F000Fu;   // nibbles at bit offsets 0 and 16
+constexpr uint32_t kNibHi = 0x00F000F0u;   // nibbles at bit offsets 4 and 20
+constexpr uint32_t kH2x16 = 0x4C004C00u;   // fp16 pair (16, 16)
+constexpr uint32_t kH2x2p15 = 0x78007800u; // 2^15
+constexpr uint32_t kH2x2p11 = 0x68006800u; // 2^11
+constexpr uint32_t kH2m2pm6 = 0xA400A400u; // -2^-6 = -8 * 2^-9
 
-// Two 4-bit codes of a word (nibbles at bit offsets 4s and 4s + 16) as the
-// fp16 pair 16 + u: the nibble goes to mantissa bits 6-9 of fp16 16 (0x4C00).
-__device__ __forceinline__ uint32_t nib16(uint32_t w, int s) {
-  const uint32_t x = s == 0 ? (w << 6) : (s == 1 ? (w << 2) : (s == 2 ? (w >> 2) : (w >> 6)));
-  return (x & 0x03C003C0u) | 0x4C004C00u;
+// fp16x2 a * b + c, one rounding to nearest even (subnormals kept)
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -1151,17 +1145,22 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // 4t .. 4t + 3 (swizzled tiles: 2t, 2t + 1, 2t + 8, 2t + 9) of the chunk
   // enter the product's k slots. With swizzled tiles every quarter-warp of a
   // fragment load touches 8 distinct 16-byte blocks: no bank conflicts.
-  // K codes enter q.K^T offset, INT8 as 1024 + u (one byte permute per pair)
-  // and 4-bit as 16 + u (one shift and one logic op per pair), both exact in
-  // fp16 and without a subtraction; the offset's product (the offset x the q
+  // INT8 K codes enter q.K^T offset, as 1024 + u (one byte permute per pair,
+  // exact in fp16, no subtraction); the offset's product (the offset x the q
   // sum) is common to a head's tokens and leaves with the zero-point term.
+  // 4-bit K codes enter as fp16 subnormals (one mask per pair): u 2^-24 for
+  // the nibbles at bits 0-3 of a half, u 2^-20 for those at bits 4-7. The q
+  // values of the first kind's k slots are multiplied by 16 once per unit, so
+  // every product is q u 2^-20 and the key scale takes the 2^20.
   // 4-bit codes (64-byte rows at D = 128, whose 16-byte fragment loads are
   // already free of conflicts): thread t reads block t of a K row, 32
   // channels; a register pairs channels c and c + 4 of one word (k slots
   // 2t, 2t + 1 of a k-step); V tokens 4 jr + t enter k slots (2t, 2t + 1,
   // 2t + 8, 2t + 9) for jr = 0 .. 3, and a register pairs two tokens' nibbles
   // of one channel (a byte permute and a mask).
-  // V codes enter P.V centred (u - 128, u - 8); see the P.V step for why.
+  // V codes enter P.V centred (u - 128; 4-bit: (u - 8) 2^-9, the masked
+  // subnormal times 2^15 or 2^11 minus 2^-6 in one fp16 fma, all exact, the
+  // 2^-9 taken back at flush); see the P.V step for why they are centred.
   //
   // The running P.V state is the MMA accumulator itself: a chunk first scales
   // it by alpha (skipped, warp-wide, while no running maximum moved) and its
@@ -1170,12 +1169,12 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // with the chunks a warp streams.
   constexpr bool BF = (KV == KV_BF16);
   constexpr bool U4 = (KV == KV_U4T);
-  // codes enter q.K^T as u - KCEN_K (INT8: 1024 + u, 4-bit: 16 + u) and P.V as
+  // codes enter q.K^T as u - KCEN_K (INT8: 1024 + u, 4-bit: u) and P.V as
   // u - KCEN_V (centred); the scale and zero-point terms take the rest. The
   // offset in q.K^T is common to every token of a head, so it only shifts the
   // products the tensor cores sum; P.V stays centred because a weight that
   // loses bits there would carry the offset into the output.
-  constexpr float KCEN_K = U4 ? -16.f : -1024.f;
+  constexpr float KCEN_K = U4 ? 0.f : -1024.f;
   constexpr float KCEN_V = U4 ? 8.f : 128.f;
   constexpr int ESZ = Geo::ESZ;
   constexpr int E = 16 / ESZ;                 // channels per 16-byte block
@@ -1244,9 +1243,10 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         float* dst = rec + WHDR + h * D + g * DPT;
 #pragma unroll
         for (int mt = 0; mt < MT; mt += 2) {
+          constexpr float VS = U4 ? 512.f : 1.f;   // 4-bit V entered as (u - 8) 2^-9
           *reinterpret_cast<float4*>(dst + 2 * mt) =
-              make_float4(acc[mt][jj] + zs2[jj], acc[mt][2 + jj] + zs2[jj], acc[mt + 1][jj] + zs2[jj],
-                          acc[mt + 1][2 + jj] + zs2[jj]);
+              make_float4(fmaf(acc[mt][jj], VS, zs2[jj]), fmaf(acc[mt][2 + jj], VS, zs2[jj]),
+                          fmaf(acc[mt + 1][jj], VS, zs2[jj]), fmaf(acc[mt + 1][2 + jj], VS, zs2[jj]));
         }
         if (g == 0) {
           rec[h] = m2[jj];
@@ -1281,9 +1281,12 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           w1 = qrow[ch / 2 + 1];
         }
       }
+      part += h2lo_f(w0, BF) + h2hi_f(w0, BF) + h2lo_f(w1, BF) + h2hi_f(w1, BF);
+      // 4-bit: the k slots of w0 meet the codes at bits 0-3 (u 2^-24); x 16
+      // (exact; the -0 addend keeps a -0)
+      if constexpr (U4) w0 = hfma2_rn(w0, kH2x16, 0x80008000u);
       qb[kk][0] = w0;
       qb[kk][1] = w1;
-      part += h2lo_f(w0, BF) + h2hi_f(w0, BF) + h2lo_f(w1, BF) + h2hi_f(w1, BF);
     }
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     part += __shfl_xor_sync(0xffffffffu, part, 2);     // q sum of head g
@@ -1447,9 +1450,12 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         }
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
+          // k-step 2w + h: channels (c, c + 4) at bits 0-3 of each half of
+          // word w >> 8h, (c + 1, c + 5) at bits 4-7
           const int w = kk >> 1, h = kk & 1;
-          const uint32_t a0 = nib16(kw0[w], 2 * h), a2 = nib16(kw0[w], 2 * h + 1);
-          const uint32_t a1 = nib16(kw1[w], 2 * h), a3 = nib16(kw1[w], 2 * h + 1);
+          const uint32_t x0 = h ? kw0[w] >> 8 : kw0[w], x1 = h ? kw1[w] >> 8 : kw1[w];
+          const uint32_t a0 = x0 & kNibLo, a2 = x0 & kNibHi;
+          const uint32_t a1 = x1 & kNibLo, a3 = x1 & kNibHi;
           if (kk & 1)
             mma16816<BF>(sco, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
           else
@@ -1497,10 +1503,11 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
         // s (u - KCEN_K) + (z + KCEN_K s) = s u + z
         const float kc0 = fmaf(KCEN_K, z0.x, z0.y), kc1 = fmaf(KCEN_K, z1.x, z1.y);
-        sc[0] = fmaf(z0.x, sc[0], kc0 * qs[0]);
-        sc[1] = fmaf(z0.x, sc[1], kc0 * qs[1]);
-        sc[2] = fmaf(z1.x, sc[2], kc1 * qs[0]);
-        sc[3] = fmaf(z1.x, sc[3], kc1 * qs[1]);
+        const float ks0 = U4 ? z0.x * 0x1p20f : z0.x, ks1 = U4 ? z1.x * 0x1p20f : z1.x;
+        sc[0] = fmaf(ks0, sc[0], kc0 * qs[0]);
+        sc[1] = fmaf(ks0, sc[1], kc0 * qs[1]);
+        sc[2] = fmaf(ks1, sc[2], kc1 * qs[0]);
+        sc[3] = fmaf(ks1, sc[3], kc1 * qs[1]);
         // V codes enter P.V centred: vs (u - KCEN_V) + (vz + KCEN_V vs) = vs u + vz
         vs0 = z0.z; vz0 = fmaf(KCEN_V, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN_V, z1.z, z1.w);
       } else if constexpr (KV == KV_I8G) {
@@ -1624,8 +1631,10 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           const uint32_t sel = (uint32_t)(bsel | (bsel << 4) | ((bsel + 4) << 8) | ((bsel + 4) << 12));
           const uint32_t t01 = __byte_perm(rw[0][wi], rw[1][wi], sel);
           const uint32_t t23 = __byte_perm(rw[2][wi], rw[3][wi], sel);
-          const uint32_t a0 = nib2h(t01, 0), a1 = nib2h(t01, 1);
-          const uint32_t a2 = nib2h(t23, 0), a3 = nib2h(t23, 1);
+          const uint32_t a0 = hfma2_rn(t01 & kNibLo, kH2x2p15, kH2m2pm6);
+          const uint32_t a1 = hfma2_rn(t01 & kNibHi, kH2x2p11, kH2m2pm6);
+          const uint32_t a2 = hfma2_rn(t23 & kNibLo, kH2x2p15, kH2m2pm6);
+          const uint32_t a3 = hfma2_rn(t23 & kNibHi, kH2x2p11, kH2m2pm6);
           mma16816<BF>(acc[mt], a0, a1, a2, a3, bh0, bh1);
           if constexpr (!PACK) mma16816<BF>(acc[mt], a0, a1, a2, a3, bl0, bl1);
         }
