@@ -359,6 +359,8 @@ __device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel) {
 constexpr uint32_t kNibLo = 0x000F000Fu;   // nibbles at bit offsets 0 and 16
 constexpr uint32_t kNibHi = 0x00F000F0u;   // nibbles at bit offsets 4 and 20
 constexpr uint32_t kH2x16 = 0x4C004C00u;   // fp16 pair (16, 16)
+constexpr uint32_t kH2x1o16 = 0x2C002C00u; // 1/16
+constexpr uint32_t kH2m0 = 0x80008000u;    // -0: an fma addend that keeps a -0
 constexpr uint32_t kH2x2p15 = 0x78007800u; // 2^15
 constexpr uint32_t kH2x2p11 = 0x68006800u; // 2^11
 constexpr uint32_t kH2m2pm6 = 0xA400A400u; // -2^-6 = -8 * 2^-9
@@ -1150,8 +1152,9 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // sum) is common to a head's tokens and leaves with the zero-point term.
   // 4-bit K codes enter as fp16 subnormals (one mask per pair): u 2^-24 for
   // the nibbles at bits 0-3 of a half, u 2^-20 for those at bits 4-7. The q
-  // values of the first kind's k slots are multiplied by 16 once per unit, so
-  // every product is q u 2^-20 and the key scale takes the 2^20.
+  // values of the first kind's k slots are multiplied by 16 once per unit
+  // (or, where that would overflow fp16, the others by 1/16), so every
+  // product carries one factor, which the key scale takes back.
   // 4-bit codes (64-byte rows at D = 128, whose 16-byte fragment loads are
   // already free of conflicts): thread t reads block t of a K row, 32
   // channels; a register pairs channels c and c + 4 of one word (k slots
@@ -1200,6 +1203,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
 
   uint32_t qb[KS][2];
   float qs[2];
+  float kmul = 0x1p20f;   // 4-bit: the key scale's factor for the codes' 2^-20 or 2^-24
   float acc[MT][4];
   float m2[2], l2[2], zs2[2];
   int u_cur = -1, next_unit = ua;
@@ -1282,11 +1286,28 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         }
       }
       part += h2lo_f(w0, BF) + h2hi_f(w0, BF) + h2lo_f(w1, BF) + h2hi_f(w1, BF);
-      // 4-bit: the k slots of w0 meet the codes at bits 0-3 (u 2^-24); x 16
-      // (exact; the -0 addend keeps a -0)
-      if constexpr (U4) w0 = hfma2_rn(w0, kH2x16, 0x80008000u);
       qb[kk][0] = w0;
       qb[kk][1] = w1;
+    }
+    if constexpr (U4) {
+      // The k slots of qb[.][0] meet the codes at bits 0-3 (u 2^-24), those of
+      // qb[.][1] the codes at bits 4-7 (u 2^-20). The first are scaled by 16
+      // (exact), so every product is q u 2^-20; where some |q| > 4094 (16 q
+      // would overflow fp16) the second are scaled by 1/16 instead, and every
+      // product is q u 2^-24.
+      float qa = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+        qa = fmaxf(qa, fmaxf(fabsf(h2lo_f(qb[kk][0], false)), fabsf(h2hi_f(qb[kk][0], false))));
+      const bool wide = __any_sync(0xffffffffu, qa > 4094.f);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        if (wide)
+          qb[kk][1] = hfma2_rn(qb[kk][1], kH2x1o16, kH2m0);
+        else
+          qb[kk][0] = hfma2_rn(qb[kk][0], kH2x16, kH2m0);
+      }
+      kmul = wide ? 0x1p24f : 0x1p20f;
     }
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     part += __shfl_xor_sync(0xffffffffu, part, 2);     // q sum of head g
@@ -1503,7 +1524,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
         // s (u - KCEN_K) + (z + KCEN_K s) = s u + z
         const float kc0 = fmaf(KCEN_K, z0.x, z0.y), kc1 = fmaf(KCEN_K, z1.x, z1.y);
-        const float ks0 = U4 ? z0.x * 0x1p20f : z0.x, ks1 = U4 ? z1.x * 0x1p20f : z1.x;
+        const float ks0 = U4 ? z0.x * kmul : z0.x, ks1 = U4 ? z1.x * kmul : z1.x;
         sc[0] = fmaf(ks0, sc[0], kc0 * qs[0]);
         sc[1] = fmaf(ks0, sc[1], kc0 * qs[1]);
         sc[2] = fmaf(ks1, sc[2], kc1 * qs[0]);

@@ -77,6 +77,42 @@ def test_u4_constant_rows():
     assert (gv[9, 1] == 0).all() and gs[9, 1, 2] == 0 and gs[9, 1, 3] == np.float32(-2.0)
 
 
+@pytest.mark.parametrize("mma", ["1", "0"])
+@pytest.mark.parametrize("big", [0.0, 5000.0])
+def test_u4_large_queries(monkeypatch, big, mma):
+    # On the tensor-core path a q value beyond 4094 in magnitude switches the
+    # unit's q scaling (16 q would overflow fp16). K channels 0 and 1 hold -0.25
+    # in every token, each token's minimum, so they restore exactly and only
+    # shift all scores of a head by the same amount.
+    set_knobs(monkeypatch, PKV_ATTN_MMA=mma)
+    from paged_kv_cache_243_gb300.cache import PagedKVCache
+    d, Hq, Hkv, ps, L = 128, 8, 2, 16, 200
+    rng = np.random.default_rng(17)
+    k = np.abs(rng.standard_normal((1, L, Hkv, d))).astype(np.float16)
+    k[..., :2] = -0.25
+    v = rng.standard_normal((1, L, Hkv, d)).astype(np.float16)
+    q = rng.standard_normal((1, Hq, d)).astype(np.float16)
+    q[0, :Hq // Hkv, 0] = big          # the first kv head's query group only
+    q[0, :Hq // Hkv, 1] = -big / 2
+    cache = PagedKVCache(16, ps, Hkv, d, kv_dtype="u4", quant="per_token", poison=True)
+    pages = rng.permutation(16)[:(L + ps - 1) // ps].astype(np.int32)
+    bt = torch.from_numpy(pages[None, :]).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache.append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), bt,
+                 torch.zeros(1, dtype=torch.int32, device="cuda"), dev_status=st)
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    sm = 1.0 / np.sqrt(d)
+    kr = oracle.per_token_u4_dequant(*oracle.quantize_per_token_u4(k[0].astype(np.float32)))
+    vr = oracle.per_token_u4_dequant(*oracle.quantize_per_token_u4(v[0].astype(np.float32)))
+    ref = oracle.decode_attention(q[0].astype(np.float64), kr, vr, sm)
+    for splits in (0, 3):
+        out = cache.attention(torch.from_numpy(q).cuda(), bt, lens, sm_scale=sm, num_splits=splits,
+                              dev_status=st).cpu().numpy()[0]
+        assert np.isfinite(out).all(), splits
+        assert np.abs(out - ref).max() <= TOL["int8"], splits
+    assert int(st.item()) == 0
+
+
 def test_u4_boxes_and_sparse():
     from test_gpu_sparse import check_group_selection, check_meta, check_selection, run_group_sparse, run_sparse
     w = small_u4(870, 128, 8, 2, 16, batch=3, offsets=0.5)
