@@ -1139,7 +1139,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   } else {
   // ============================================== consumers, tensor-core path
   // Thread (g = lane / 4, t = lane % 4). Scores: C fragment of the [16 tok] x
-  // [8 head] product, i.e. tokens g and g + 8, heads 2t and 2t + 1. The channel
+  // [8 head] product, i.e. tokens g and g + 8, heads 2t and 2t + 1 (with G = 4
+  // the softmax runs on token g + 8 (t >> 1) of heads 2 (t & 1), + 1). The channel
   // axis is permuted so that thread t reads whole 16-byte blocks of a row:
   // blocks t, t + 4, ... or, with swizzled tiles, blocks 2t and 2t + 1.
   // Values: O^T [16 channels] x [8 heads] per m-tile; thread (g, t) owns
@@ -1189,6 +1190,10 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // (columns [0, G) hi, [G, 2G) lo), halving the P.V tensor work; the lo
   // columns are added to the hi ones at flush.
   constexpr bool PACK = GE <= 4;
+  // With G = 4 the score columns of lanes t = 2, 3 are idle (heads 4 .. 7):
+  // those lanes take over the token g + 8 scores of lanes t - 2, so every lane
+  // runs the softmax of one token for heads 2 (t & 1), 2 (t & 1) + 1.
+  constexpr bool RED = GE == 4;
   const int g = lane >> 2, t = lane & 3;
   float* pb = pbuf_all + warp * PBUF;
   // logical 16-byte block m (of NB) of a row that thread t reads, and where a
@@ -1230,12 +1235,13 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mt][e] += __shfl_down_sync(0xffffffffu, acc[mt][e], GE / 2);
     }
-    // l and the zero-point sum are kept per lane (tokens g, g + 8); sum the 8
-    // lanes of each head here instead of on every chunk
+    // l and the zero-point sum are kept per lane (tokens g, g + 8; with G = 4
+    // one of them, the other in lane t ^ 2); sum the lanes of each head here
+    // instead of on every chunk
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
+      for (int off = RED ? 2 : 4; off < 32; off <<= 1) {
         l2[jj] += __shfl_xor_sync(0xffffffffu, l2[jj], off);
         if constexpr (KV != KV_F16 && KV != KV_BF16) zs2[jj] += __shfl_xor_sync(0xffffffffu, zs2[jj], off);
       }
@@ -1311,8 +1317,9 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
     }
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     part += __shfl_xor_sync(0xffffffffu, part, 2);     // q sum of head g
-    qs[0] = __shfl_sync(0xffffffffu, part, (2 * t) * 4);
-    qs[1] = __shfl_sync(0xffffffffu, part, (2 * t + 1) * 4);
+    const int qh = RED ? 2 * (t & 1) : 2 * t;
+    qs[0] = __shfl_sync(0xffffffffu, part, qh * 4);
+    qs[1] = __shfl_sync(0xffffffffu, part, (qh + 1) * 4);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -1517,69 +1524,126 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[e] += sco[e];
       }
-      // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
-      float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
-      if constexpr (Geo::PTOK) {
-        const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
-        const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
-        // s (u - KCEN_K) + (z + KCEN_K s) = s u + z
-        const float kc0 = fmaf(KCEN_K, z0.x, z0.y), kc1 = fmaf(KCEN_K, z1.x, z1.y);
-        const float ks0 = U4 ? z0.x * kmul : z0.x, ks1 = U4 ? z1.x * kmul : z1.x;
-        sc[0] = fmaf(ks0, sc[0], kc0 * qs[0]);
-        sc[1] = fmaf(ks0, sc[1], kc0 * qs[1]);
-        sc[2] = fmaf(ks1, sc[2], kc1 * qs[0]);
-        sc[3] = fmaf(ks1, sc[3], kc1 * qs[1]);
-        // V codes enter P.V centred: vs (u - KCEN_V) + (vz + KCEN_V vs) = vs u + vz
-        vs0 = z0.z; vz0 = fmaf(KCEN_V, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN_V, z1.z, z1.w);
-      } else if constexpr (KV == KV_I8G) {
-        const float4 z = *reinterpret_cast<const float4*>(sz);
-        const float kc = fmaf(KCEN_K, z.x, z.y);   // as for per-token scales
-        sc[0] = fmaf(z.x, sc[0], kc * qs[0]);
-        sc[1] = fmaf(z.x, sc[1], kc * qs[1]);
-        sc[2] = fmaf(z.x, sc[2], kc * qs[0]);
-        sc[3] = fmaf(z.x, sc[3], kc * qs[1]);
-        vs0 = vs1 = z.z;
-        vz0 = vz1 = fmaf(KCEN_V, z.z, z.w);   // centred codes, as for per-token scales
-      }
-      const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[e] *= p.q_scale;
-      if (!ok0) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-      if (!ok1) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
-      // ---- online softmax per head 2t + jj
-      float al[2], pw[4];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float cm = fmaxf(sc[jj], sc[2 + jj]);
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
-        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-        const float mn = fmaxf(m2[jj], cm);
-        al[jj] = fast_exp2(m2[jj] - mn);
-        const float p0 = fast_exp2(sc[jj] - mn), p1 = fast_exp2(sc[2 + jj] - mn);
-        // lane-local running sums (rescaled like the accumulator; the lanes
-        // of a head are summed at flush)
-        l2[jj] = fmaf(l2[jj], al[jj], p0 + p1);
+      float al[2];
+      if constexpr (RED) {
+        const int hf = t >> 1;   // 0: token g, 1: token g + 8 (lanes t - 2's)
+        const float x2 = __shfl_up_sync(0xffffffffu, sc[2], 2);
+        const float x3 = __shfl_up_sync(0xffffffffu, sc[3], 2);
+        float s2[2] = {hf ? x2 : sc[0], hf ? x3 : sc[1]};
+        const int tok = g + 8 * hf;
+        float vs = 0.f, vz = 0.f;
         if constexpr (Geo::PTOK) {
-          const float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
-          zs2[jj] = fmaf(zs2[jj], al[jj], pz);
-          pw[jj] = ok0 ? p0 * vs0 : 0.f;
-          pw[2 + jj] = ok1 ? p1 * vs1 : 0.f;
+          const float4 z = *reinterpret_cast<const float4*>(sz + tok * 4);
+          const float kc = fmaf(KCEN_K, z.x, z.y);   // s (u - KCEN_K) + (z + KCEN_K s)
+          const float ks = U4 ? z.x * kmul : z.x;
+          s2[0] = fmaf(ks, s2[0], kc * qs[0]);
+          s2[1] = fmaf(ks, s2[1], kc * qs[1]);
+          vs = z.z;
+          vz = fmaf(KCEN_V, z.z, z.w);   // centred V codes
         } else if constexpr (KV == KV_I8G) {
-          zs2[jj] = fmaf(zs2[jj], al[jj], vz0 * (p0 + p1));
-          pw[jj] = p0 * vs0;
-          pw[2 + jj] = p1 * vs1;
-        } else {
-          pw[jj] = p0;
-          pw[2 + jj] = p1;
+          const float4 z = *reinterpret_cast<const float4*>(sz);
+          const float kc = fmaf(KCEN_K, z.x, z.y);
+          s2[0] = fmaf(z.x, s2[0], kc * qs[0]);
+          s2[1] = fmaf(z.x, s2[1], kc * qs[1]);
+          vs = z.z;
+          vz = fmaf(KCEN_V, z.z, z.w);
         }
-        m2[jj] = mn;
+        const bool ok = tok < nvalid;
+        s2[0] *= p.q_scale;
+        s2[1] *= p.q_scale;
+        if (!ok) { s2[0] = -INFINITY; s2[1] = -INFINITY; }
+        // ---- online softmax per head 2 (t & 1) + jj, over the 16 tokens of
+        // lanes (g, t) and (g, t ^ 2)
+        float pw2[2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          float cm = s2[jj];
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+          const float mn = fmaxf(m2[jj], cm);
+          al[jj] = fast_exp2(m2[jj] - mn);
+          const float p0 = fast_exp2(s2[jj] - mn);
+          l2[jj] = fmaf(l2[jj], al[jj], p0);
+          if constexpr (Geo::PTOK) {
+            zs2[jj] = fmaf(zs2[jj], al[jj], ok ? p0 * vz : 0.f);
+            pw2[jj] = ok ? p0 * vs : 0.f;
+          } else if constexpr (KV == KV_I8G) {
+            zs2[jj] = fmaf(zs2[jj], al[jj], vz * p0);
+            pw2[jj] = p0 * vs;
+          } else {
+            pw2[jj] = p0;
+          }
+          m2[jj] = mn;
+        }
+        pb[(2 * (t & 1)) * kChunk + tok] = pw2[0];
+        pb[(2 * (t & 1) + 1) * kChunk + tok] = pw2[1];
+      } else {
+        // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
+        float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
+        if constexpr (Geo::PTOK) {
+          const float4 z0 = *reinterpret_cast<const float4*>(sz + g * 4);
+          const float4 z1 = *reinterpret_cast<const float4*>(sz + (g + 8) * 4);
+          // s (u - KCEN_K) + (z + KCEN_K s) = s u + z
+          const float kc0 = fmaf(KCEN_K, z0.x, z0.y), kc1 = fmaf(KCEN_K, z1.x, z1.y);
+          const float ks0 = U4 ? z0.x * kmul : z0.x, ks1 = U4 ? z1.x * kmul : z1.x;
+          sc[0] = fmaf(ks0, sc[0], kc0 * qs[0]);
+          sc[1] = fmaf(ks0, sc[1], kc0 * qs[1]);
+          sc[2] = fmaf(ks1, sc[2], kc1 * qs[0]);
+          sc[3] = fmaf(ks1, sc[3], kc1 * qs[1]);
+          // V codes enter P.V centred: vs (u - KCEN_V) + (vz + KCEN_V vs) = vs u + vz
+          vs0 = z0.z; vz0 = fmaf(KCEN_V, z0.z, z0.w); vs1 = z1.z; vz1 = fmaf(KCEN_V, z1.z, z1.w);
+        } else if constexpr (KV == KV_I8G) {
+          const float4 z = *reinterpret_cast<const float4*>(sz);
+          const float kc = fmaf(KCEN_K, z.x, z.y);   // as for per-token scales
+          sc[0] = fmaf(z.x, sc[0], kc * qs[0]);
+          sc[1] = fmaf(z.x, sc[1], kc * qs[1]);
+          sc[2] = fmaf(z.x, sc[2], kc * qs[0]);
+          sc[3] = fmaf(z.x, sc[3], kc * qs[1]);
+          vs0 = vs1 = z.z;
+          vz0 = vz1 = fmaf(KCEN_V, z.z, z.w);   // centred codes, as for per-token scales
+        }
+        const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] *= p.q_scale;
+        if (!ok0) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+        if (!ok1) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+        // ---- online softmax per head 2t + jj
+        float pw[4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          float cm = fmaxf(sc[jj], sc[2 + jj]);
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+          const float mn = fmaxf(m2[jj], cm);
+          al[jj] = fast_exp2(m2[jj] - mn);
+          const float p0 = fast_exp2(sc[jj] - mn), p1 = fast_exp2(sc[2 + jj] - mn);
+          // lane-local running sums (rescaled like the accumulator; the lanes
+          // of a head are summed at flush)
+          l2[jj] = fmaf(l2[jj], al[jj], p0 + p1);
+          if constexpr (Geo::PTOK) {
+            const float pz = (ok0 ? p0 * vz0 : 0.f) + (ok1 ? p1 * vz1 : 0.f);
+            zs2[jj] = fmaf(zs2[jj], al[jj], pz);
+            pw[jj] = ok0 ? p0 * vs0 : 0.f;
+            pw[2 + jj] = ok1 ? p1 * vs1 : 0.f;
+          } else if constexpr (KV == KV_I8G) {
+            zs2[jj] = fmaf(zs2[jj], al[jj], vz0 * (p0 + p1));
+            pw[jj] = p0 * vs0;
+            pw[2 + jj] = p1 * vs1;
+          } else {
+            pw[jj] = p0;
+            pw[2 + jj] = p1;
+          }
+          m2[jj] = mn;
+        }
+        // P' to [head][token] in shared memory, then as the B operand of P.V
+        pb[(2 * t) * kChunk + g] = pw[0];
+        pb[(2 * t + 1) * kChunk + g] = pw[1];
+        pb[(2 * t) * kChunk + g + 8] = pw[2];
+        pb[(2 * t + 1) * kChunk + g + 8] = pw[3];
       }
-      // P' to [head][token] in shared memory, then as the B operand of P.V
-      pb[(2 * t) * kChunk + g] = pw[0];
-      pb[(2 * t + 1) * kChunk + g] = pw[1];
-      pb[(2 * t) * kChunk + g + 8] = pw[2];
-      pb[(2 * t + 1) * kChunk + g + 8] = pw[3];
       __syncwarp();
       // B column g: head g (hi part), or with PACK the lo part of head g - GE;
       // its k slots are the tokens vtok(0 .. 3)
@@ -1613,7 +1677,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
       float a0s = al[0], a1s = al[1];
       if constexpr (GE == 1) {   // columns 0 and 1: hi and lo parts of head 0
         a1s = al[0];
-      } else if constexpr (PACK) {   // lo columns of heads 2 (t - GE/2) + jj
+      } else if constexpr (PACK && !RED) {   // lo columns of heads 2 (t - GE/2) + jj
         const int src = t >= GE / 2 ? lane - GE / 2 : lane;
         a0s = __shfl_sync(0xffffffffu, al[0], src);
         a1s = __shfl_sync(0xffffffffu, al[1], src);
