@@ -1140,7 +1140,8 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   // ============================================== consumers, tensor-core path
   // Thread (g = lane / 4, t = lane % 4). Scores: C fragment of the [16 tok] x
   // [8 head] product, i.e. tokens g and g + 8, heads 2t and 2t + 1 (with G = 4
-  // the softmax runs on token g + 8 (t >> 1) of heads 2 (t & 1), + 1). The channel
+  // the softmax runs on token g + 8 (t >> 1) of heads 2 (t & 1), + 1; with
+  // G = 2 on token g + 8 (t & 1) of heads 0 and 1). The channel
   // axis is permuted so that thread t reads whole 16-byte blocks of a row:
   // blocks t, t + 4, ... or, with swizzled tiles, blocks 2t and 2t + 1.
   // Values: O^T [16 channels] x [8 heads] per m-tile; thread (g, t) owns
@@ -1192,8 +1193,10 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
   constexpr bool PACK = GE <= 4;
   // With G = 4 the score columns of lanes t = 2, 3 are idle (heads 4 .. 7):
   // those lanes take over the token g + 8 scores of lanes t - 2, so every lane
-  // runs the softmax of one token for heads 2 (t & 1), 2 (t & 1) + 1.
-  constexpr bool RED = GE == 4;
+  // runs the softmax of one token for heads 2 (t & 1), 2 (t & 1) + 1. With
+  // G = 2, lane t = 1 takes over those of lane 0 (lanes 2, 3 work on idle rows).
+  constexpr bool RED = GE == 4 || GE == 2;
+  constexpr int RX = GE == 4 ? 2 : 1;   // lane distance of a token pair's halves
   const int g = lane >> 2, t = lane & 3;
   float* pb = pbuf_all + warp * PBUF;
   // logical 16-byte block m (of NB) of a row that thread t reads, and where a
@@ -1236,12 +1239,12 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         for (int e = 0; e < 4; ++e) acc[mt][e] += __shfl_down_sync(0xffffffffu, acc[mt][e], GE / 2);
     }
     // l and the zero-point sum are kept per lane (tokens g, g + 8; with G = 4
-    // one of them, the other in lane t ^ 2); sum the lanes of each head here
-    // instead of on every chunk
+    // or 2 one of them, the other in lane t ^ RX); sum the lanes of each head
+    // here instead of on every chunk
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
 #pragma unroll
-      for (int off = RED ? 2 : 4; off < 32; off <<= 1) {
+      for (int off = RED ? RX : 4; off < 32; off = off == RX ? 4 : off << 1) {
         l2[jj] += __shfl_xor_sync(0xffffffffu, l2[jj], off);
         if constexpr (KV != KV_F16 && KV != KV_BF16) zs2[jj] += __shfl_xor_sync(0xffffffffu, zs2[jj], off);
       }
@@ -1317,7 +1320,7 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
     }
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     part += __shfl_xor_sync(0xffffffffu, part, 2);     // q sum of head g
-    const int qh = RED ? 2 * (t & 1) : 2 * t;
+    const int qh = GE == 4 ? 2 * (t & 1) : (GE == 2 ? 2 * (t >> 1) : 2 * t);
     qs[0] = __shfl_sync(0xffffffffu, part, qh * 4);
     qs[1] = __shfl_sync(0xffffffffu, part, (qh + 1) * 4);
 #pragma unroll
@@ -1526,9 +1529,9 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
       }
       float al[2];
       if constexpr (RED) {
-        const int hf = t >> 1;   // 0: token g, 1: token g + 8 (lanes t - 2's)
-        const float x2 = __shfl_up_sync(0xffffffffu, sc[2], 2);
-        const float x3 = __shfl_up_sync(0xffffffffu, sc[3], 2);
+        const int hf = GE == 4 ? t >> 1 : t & 1;   // 0: token g, 1: token g + 8 (lane t - RX's)
+        const float x2 = __shfl_up_sync(0xffffffffu, sc[2], RX);
+        const float x3 = __shfl_up_sync(0xffffffffu, sc[3], RX);
         float s2[2] = {hf ? x2 : sc[0], hf ? x3 : sc[1]};
         const int tok = g + 8 * hf;
         float vs = 0.f, vz = 0.f;
@@ -1552,13 +1555,13 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
         s2[0] *= p.q_scale;
         s2[1] *= p.q_scale;
         if (!ok) { s2[0] = -INFINITY; s2[1] = -INFINITY; }
-        // ---- online softmax per head 2 (t & 1) + jj, over the 16 tokens of
-        // lanes (g, t) and (g, t ^ 2)
+        // ---- online softmax per head, over the 16 tokens of lanes (g, t) and
+        // (g, t ^ RX)
         float pw2[2];
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           float cm = s2[jj];
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, RX));
           cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
           cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
           cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
@@ -1577,8 +1580,9 @@ __global__ void __launch_bounds__(attn_threads(SELF), SELF ? 4 : (MMA ? 3 : 1))
           }
           m2[jj] = mn;
         }
-        pb[(2 * (t & 1)) * kChunk + tok] = pw2[0];
-        pb[(2 * (t & 1) + 1) * kChunk + tok] = pw2[1];
+        const int prow = GE == 4 ? 2 * (t & 1) : 2 * (t >> 1);   // G = 2: lanes 2, 3 on idle rows
+        pb[prow * kChunk + tok] = pw2[0];
+        pb[(prow + 1) * kChunk + tok] = pw2[1];
       } else {
         // sc: (tok g, head 2t), (tok g, head 2t+1), (tok g+8, head 2t), (tok g+8, head 2t+1)
         float vs0 = 0.f, vz0 = 0.f, vs1 = 0.f, vz1 = 0.f;
